@@ -1,0 +1,321 @@
+"""Plain float64 CPU oracle for Top-theta attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it.  It shares no code with the CUDA library.
+
+Sources (cited below by short name):
+
+* [TopTheta] "Top-Theta Attention: Sparsifying Transformers by Compensated
+  Thresholding" (arXiv 2502.08363v2, HTML).  §2.2 Eq. 1-3 (attention),
+  §3.1 Algorithm 1 (threshold calibration), §3.2.1 Eq. 4 and the three
+  estimators of the discarded mass (SDC), §3.2.2 Eq. 5-7 (VMC), §4.6 (GQA:
+  V rows are counted per group).
+* [Verdict] pith.science verdict on arXiv 2502.08363, "load_bearing_attack":
+  rows longer than the calibrated ones use the nearest calibrated threshold.
+
+Readings where the pages are silent or garbled (each one is listed with its
+reason in the design notes of the repository):
+
+* c1  an element is kept iff x >= theta (ties are kept).
+* c2  the per-sample "(n-k)/n quantile" is the k-th largest valid element
+      (order statistic, no interpolation).
+* c3  a row is keyed by L, the number of keys it sees; the threshold table
+      holds the row with L keys at index L-1.
+* c4  rows with L <= k are dense (theta = -inf).
+* c5  a row id that was never calibrated takes the nearest calibrated row id
+      (ties go to the shorter row); a head with no calibrated row is dense.
+* c6  scores are scaled by 1/sqrt(d); causally masked keys do not exist.
+* c7  post-softmax thresholds are the arithmetic mean of probabilities.
+* c8  the exp-threshold estimate uses the same max-shifted units as R:
+      E~ = gamma (L - k~) exp(theta - m).
+* c9  m is the true row maximum over all valid keys.
+* c10 beta = 1 - sum of the final (after SDC) kept probabilities.
+* c11 mu in causal prefill is the prefix mean of V rows 0..L-1.
+* c12 an empty selection gives num = 0 and R = 0 (pre without SDC: out = 0).
+* c13 std uses ddof = 1; a single sample has std 0.
+* c16 post-softmax with SDC is post-softmax (SDC maps pre onto post).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PRE, POST = 0, 1
+SDC_NONE, SDC_EXACT, SDC_EXPTH = 0, 1, 2
+GAMMA = 0.05          # [TopTheta §3.2.1, exp-threshold estimator]
+BAND_REL = 1e-3       # decisions within this relative distance of theta are not compared
+
+
+# ---------------------------------------------------------------------------
+# Eq. 1: scores of one query row against the keys it sees.
+# ---------------------------------------------------------------------------
+def row_scores(q, K, L):
+    """a_j = q . K_j / sqrt(d) for j < L  ([TopTheta §2.2 Eq. 1], reading c6)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    d = q.shape[-1]
+    return (K[:L] @ q) / math.sqrt(d)
+
+
+def row_softmax(a):
+    """Eq. 2 with the row maximum subtracted first (Eq. 4 writes it this way)."""
+    m = np.max(a)
+    e = np.exp(a - m)
+    return e / e.sum()
+
+
+# ---------------------------------------------------------------------------
+# Algorithm 1: calibration.
+# ---------------------------------------------------------------------------
+def kth_largest(x, k):
+    """The k-th largest element of x (1-based), reading c2."""
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[0]
+    return np.partition(x, n - k)[n - k]
+
+
+def calibration_sample(a, k, mode):
+    """One observed threshold of a calibration row ([TopTheta §3.1, Algorithm 1]).
+
+    Pre-softmax: the quantile is taken on the scores a.  Post-softmax: the same
+    quantile is taken on s = softmax(a) instead ([TopTheta §3.1], the remark
+    after Figure 2).
+    """
+    if mode == PRE:
+        return kth_largest(a, k)
+    return kth_largest(row_softmax(a), k)
+
+
+def collect_thresholds(Qc, Kc, row_len, k, mode, sets=None):
+    """Gather the sets Theta_r of Algorithm 1 for one layer.
+
+    Qc [N][Hq][R][d], Kc [N][Hkv][Nk][d]; query row i of sequence n sees keys
+    0..row_len[i]-1.  Query head h reads KV head h // (Hq // Hkv) (GQA,
+    [TopTheta §2.2]).  ``sets`` maps (h, L) to the list of observed thresholds
+    and is extended in place, so several calls accumulate like one.
+    """
+    Qc = np.asarray(Qc, dtype=np.float64)
+    Kc = np.asarray(Kc, dtype=np.float64)
+    N, Hq, R, _ = Qc.shape
+    Hkv = Kc.shape[1]
+    g = Hq // Hkv
+    if sets is None:
+        sets = {}
+    for n in range(N):
+        for h in range(Hq):
+            for i in range(R):
+                L = int(row_len[i])
+                if L <= k:               # Algorithm 1 starts at row k (reading c4)
+                    continue
+                a = row_scores(Qc[n, h, i], Kc[n, h // g], L)
+                sets.setdefault((h, L), []).append(calibration_sample(a, k, mode))
+    return sets
+
+
+def finalize_thresholds(sets, Hq, Lmax, k, alpha):
+    """theta_r = mean(Theta_r) + alpha * std(Theta_r) ([TopTheta §3.1, Algorithm 1]).
+
+    Returns the table [Hq][Lmax]; entry L-1 belongs to rows with L keys.
+    Rows with L <= k are dense (-inf, reading c4).  Uncalibrated rows take the
+    nearest calibrated row id, ties to the shorter row ([Verdict], reading c5).
+    """
+    theta = np.full((Hq, Lmax), -np.inf)
+    for h in range(Hq):
+        seen = sorted(L for (hh, L) in sets if hh == h and L <= Lmax)
+        value = {}
+        for L in seen:
+            obs = np.asarray(sets[(h, L)], dtype=np.float64)
+            std = float(np.std(obs, ddof=1)) if obs.size > 1 else 0.0
+            value[L] = float(np.mean(obs)) + alpha * std
+        if not seen:
+            continue
+        for L in range(1, Lmax + 1):
+            if L <= k:
+                continue
+            if L in value:
+                theta[h, L - 1] = value[L]
+                continue
+            best = min(seen, key=lambda c: (abs(c - L), c))
+            theta[h, L - 1] = value[best]
+    return theta
+
+
+def calibrate_ref(Qc, Kc, row_len, k, mode, alpha, Lmax):
+    """Algorithm 1 for one layer: returns (theta [Hq][Lmax], sets)."""
+    sets = collect_thresholds(Qc, Kc, row_len, k, mode)
+    return finalize_thresholds(sets, Qc.shape[1], Lmax, k, alpha), sets
+
+
+def theta_for_row(theta_row, L):
+    """Look up the threshold of a row with L keys (readings c3, c5)."""
+    Lmax = theta_row.shape[-1]
+    return float(theta_row[min(L, Lmax) - 1])
+
+
+# ---------------------------------------------------------------------------
+# Inference on one attention row: threshold, SDC, VMC.
+# ---------------------------------------------------------------------------
+def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
+               gamma=GAMMA, decide=None):
+    """Top-theta attention of one row.
+
+    a      scores of the L visible keys (Eq. 1)
+    Vrows  [L][d] value rows
+    theta  the row's calibrated threshold (pre: on a, post: on s)
+    decide optional bool [L]; inside the band |x - theta| <= 1e-3 |theta| the
+           oracle adopts these decisions instead of its own.
+
+    Returns a dict with out [d], keep [L], kept (k~), band [L], m, Z, R, E, beta.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    V = np.asarray(Vrows, dtype=np.float64)
+    L = a.shape[0]
+    m = float(np.max(a))
+    e = np.exp(a - m)                       # e^{a_j - max_l a_l}, Eq. 4
+    Z = float(e.sum())
+    s = e / Z                               # Eq. 2
+    x = a if mode == PRE else s
+    keep = x >= theta                       # reading c1
+    if np.isfinite(theta):
+        band = np.abs(x - theta) <= BAND_REL * abs(theta)
+    else:
+        band = np.zeros(L, dtype=bool)
+    if decide is not None:
+        keep = np.where(band, np.asarray(decide, dtype=bool), keep)
+    kt = int(keep.sum())
+    R = float(e[keep].sum())                # Eq. 4: selected exponent sum
+    E = Z - R                               # Eq. 4: discarded exponent sum
+
+    if mode == POST:
+        # post-softmax: the kept s are not renormalised ([TopTheta §3.2.2 case i]);
+        # SDC is the identity here (reading c16).
+        s_kept = e[keep] / Z
+    elif sdc == SDC_NONE:
+        # softmax over the kept scores only ([TopTheta §3 Fig. 1, pre variant]).
+        s_kept = e[keep] / R if R > 0 else np.zeros(kt)
+    else:
+        if sdc == SDC_EXACT:                # [TopTheta §3.2.1, estimator 3]
+            E_est = E
+        else:                               # [TopTheta §3.2.1, estimator 2], reading c8
+            E_est = gamma * (L - kt) * math.exp(theta - m) if L > kt else 0.0
+        # Eq. 4: softmax(a~)_i * R/(R + E~) = e_i / (R + E~)
+        denom = R + E_est
+        s_kept = e[keep] / denom if denom > 0 else np.zeros(kt)
+
+    out = s_kept @ V[keep] if kt else np.zeros(V.shape[1])   # Eq. 7 first term
+    vmc_eligible = mode == POST or sdc != SDC_NONE
+    beta = 1.0 - float(s_kept.sum()) if vmc_eligible else 0.0  # Eq. 6, reading c10
+    if vmc:
+        out = out + beta * np.asarray(mu, dtype=np.float64)    # Eq. 7
+    return dict(out=out, keep=keep, kept=kt, band=band, m=m, Z=Z, R=R, E=E,
+                beta=beta)
+
+
+def vmean_ref(Vrows):
+    """Eq. 5: mean V row."""
+    return np.mean(np.asarray(Vrows, dtype=np.float64), axis=0)
+
+
+def vmean_update_ref(mu, n_old, new_rows):
+    """Running mean of [TopTheta §3.2.2]: mu over n_old rows, then t rows appended."""
+    new_rows = np.asarray(new_rows, dtype=np.float64)
+    t = new_rows.shape[0]
+    return (n_old * np.asarray(mu, dtype=np.float64) + new_rows.sum(axis=0)) / (n_old + t)
+
+
+# ---------------------------------------------------------------------------
+# Decode and prefill drivers (loops over rows, heads and batches).
+# ---------------------------------------------------------------------------
+def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
+               mu=None, gamma=GAMMA, decide=None, heads=None):
+    """One generated token per sequence ([TopTheta §2.2, generative decoding]).
+
+    q [B][Hq][d]; Kc, Vc [B][Hkv][Nmax][d]; seq_len [B] (keys incl. the current
+    token); theta [Hq][Lmax]; mu [B][Hkv][d] (when vmc).  ``decide`` is an
+    optional bool [B][Hq][Nmax] of decisions adopted inside the band.
+    ``heads`` optionally restricts the work to a list of (b, h) pairs.
+
+    Returns dicts keyed by (b, h) of attend_row results, and the union size
+    per (b, kv head) over the heads computed ([TopTheta §4.6]).
+    """
+    B, Hq, _ = q.shape
+    Hkv = Kc.shape[1]
+    g = Hq // Hkv
+    res = {}
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
+    for (b, h) in heads:
+        L = int(seq_len[b])
+        kv = h // g
+        a = row_scores(q[b, h], Kc[b, kv], L)
+        th = theta_for_row(theta[h], L)
+        dec = None if decide is None else decide[b, h, :L]
+        res[(b, h)] = attend_row(a, Vc[b, kv, :L], th, mode, sdc, vmc,
+                                 None if mu is None else mu[b, kv], gamma, dec)
+    union = {}
+    for (b, h), r in res.items():
+        key = (b, h // g)
+        u = union.get(key)
+        union[key] = r["keep"].copy() if u is None else (u | r["keep"])
+    vrows = {key: int(u.sum()) for key, u in union.items()}
+    return res, vrows
+
+
+def prefill_ref(Q, K, V, theta, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA,
+                decide=None, rows=None):
+    """Causal prefill ([TopTheta §2.2, prefill phase]); row i sees keys 0..i.
+
+    Q [B][Hq][S][d]; K, V [B][Hkv][S][d]; theta [Hq][Lmax].  mu for row i is
+    the mean of V rows 0..i (reading c11).  ``rows`` optionally restricts the
+    work to a list of (b, h, i).  Returns a dict keyed by (b, h, i).
+    """
+    B, Hq, S, _ = Q.shape
+    Hkv = K.shape[1]
+    g = Hq // Hkv
+    res = {}
+    if rows is None:
+        rows = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(S)]
+    for (b, h, i) in rows:
+        L = i + 1
+        kv = h // g
+        a = row_scores(Q[b, h, i], K[b, kv], L)
+        th = theta_for_row(theta[h], L)
+        mu = vmean_ref(V[b, kv, :L]) if vmc else None
+        dec = None if decide is None else decide[b, h, i, :L]
+        res[(b, h, i)] = attend_row(a, V[b, kv, :L], th, mode, sdc, vmc, mu,
+                                    gamma, dec)
+    return res
+
+
+def tile_counts_ref(keep_rows, S, tile_m, tile_n):
+    """Count causal (row block, key block) tiles and those holding a kept element.
+
+    keep_rows maps row i to its bool mask over keys 0..i.  A tile is causal if
+    any of its (i, j) has j <= i.  Returns (tiles_with_survivor, causal_tiles).
+    """
+    hit = 0
+    total = 0
+    for rb in range(0, S, tile_m):
+        for cb in range(0, S, tile_n):
+            if cb > min(rb + tile_m, S) - 1:
+                continue
+            total += 1
+            any_kept = False
+            for i in range(rb, min(rb + tile_m, S)):
+                row = keep_rows[i]
+                hi = min(cb + tile_n, i + 1)
+                if hi > cb and bool(np.any(row[cb:hi])):
+                    any_kept = True
+                    break
+            hit += int(any_kept)
+    return hit, total
+
+
+def output_rel_error(out, ref):
+    """max |out - ref| / max |ref| over one output row (the parity metric)."""
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(np.asarray(out, dtype=np.float64) - ref)))
+    return err / scale if scale > 0 else err

@@ -1,0 +1,365 @@
+"""Pins of the float64 oracle to facts the pages and the mathematics fix.
+
+Each check compares the oracle with something other than itself: hand-derived
+closed forms (tests/golden), a library attention routine, brute force on tiny
+rows, and identities of the method (Eq. 4, Eq. 5-7).  The last test plants
+mistakes in the oracle and checks that these pins catch each one.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.topt_ref as ref
+
+MODES = {"pre": ref.PRE, "post": ref.POST}
+SDCS = {"none": ref.SDC_NONE, "exact": ref.SDC_EXACT, "expth": ref.SDC_EXPTH}
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Dense limit: theta = -inf is ordinary softmax attention (Eq. 1-3).
+# ---------------------------------------------------------------------------
+def _sdpa(q, k, v, mask=None, causal=False):
+    out = torch.nn.functional.scaled_dot_product_attention(
+        torch.as_tensor(q), torch.as_tensor(k), torch.as_tensor(v),
+        attn_mask=None if mask is None else torch.as_tensor(mask), is_causal=causal)
+    return out.numpy()
+
+
+def check_dense_decode(seed=0):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, d, Nmax = 2, 4, 2, 16, 23
+    seq_len = np.array([23, 9])
+    q = rng.standard_normal((B, Hq, d))
+    Kc = rng.standard_normal((B, Hkv, Nmax, d)) * 2
+    Vc = rng.standard_normal((B, Hkv, Nmax, d))
+    theta = np.full((Hq, Nmax), -np.inf)
+    for mode in (ref.PRE, ref.POST):
+        res, vrows = ref.decode_ref(q, Kc, Vc, seq_len, theta, mode)
+        g = Hq // Hkv
+        Kr = np.repeat(Kc, g, axis=1)
+        Vr = np.repeat(Vc, g, axis=1)
+        mask = np.zeros((B, 1, 1, Nmax), dtype=bool)
+        for b in range(B):
+            mask[b, 0, 0, :seq_len[b]] = True
+        want = _sdpa(q[:, :, None, :], Kr, Vr, mask)[:, :, 0, :]
+        for (b, h), r in res.items():
+            assert r["kept"] == seq_len[b]
+            np.testing.assert_allclose(r["out"], want[b, h], rtol=1e-12, atol=1e-12)
+        for (b, kv), n in vrows.items():
+            assert n == seq_len[b]
+
+
+def test_dense_decode_matches_library_sdpa():
+    check_dense_decode()
+
+
+def check_dense_prefill(seed=1):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, S, d = 1, 2, 1, 19, 8
+    Q = rng.standard_normal((B, Hq, S, d))
+    K = rng.standard_normal((B, Hkv, S, d))
+    V = rng.standard_normal((B, Hkv, S, d))
+    theta = np.full((Hq, S), -np.inf)
+    want = _sdpa(Q, np.repeat(K, 2, axis=1), np.repeat(V, 2, axis=1), causal=True)
+    for mode, sdc, vmc in [(ref.PRE, ref.SDC_NONE, False), (ref.POST, ref.SDC_NONE, True),
+                           (ref.PRE, ref.SDC_EXACT, True), (ref.PRE, ref.SDC_EXPTH, True)]:
+        res = ref.prefill_ref(Q, K, V, theta, mode, sdc, vmc)
+        for (b, h, i), r in res.items():
+            assert r["kept"] == i + 1
+            assert abs(r["beta"]) < 1e-12          # full mask: nothing discarded
+            np.testing.assert_allclose(r["out"], want[b, h, i], rtol=1e-12, atol=1e-12)
+
+
+def test_dense_prefill_matches_library_causal_sdpa():
+    check_dense_prefill()
+
+
+# ---------------------------------------------------------------------------
+# Hand-derived closed forms of Eq. 4-7 (tests/golden/sdc_vmc_five_keys.json).
+# ---------------------------------------------------------------------------
+def check_golden_sdc_vmc(golden_dir):
+    g = _load(golden_dir, "sdc_vmc_five_keys.json")
+    a = np.array(g["a"])
+    V = np.eye(5)
+    mu = ref.vmean_ref(V)
+    np.testing.assert_allclose(mu, 0.2, rtol=1e-15)
+    for c in g["cases"]:
+        r = ref.attend_row(a, V, c["theta"], MODES[c["mode"]], SDCS[c["sdc"]], c["vmc"], mu)
+        assert r["kept"] == c["kept"], c
+        assert abs(r["beta"] - c["beta"]) < 1e-14, c
+        np.testing.assert_allclose(r["out"], c["out"], rtol=1e-13, atol=1e-15, err_msg=str(c))
+
+
+def test_golden_sdc_vmc_closed_forms(golden_dir):
+    check_golden_sdc_vmc(golden_dir)
+
+
+# ---------------------------------------------------------------------------
+# Algorithm 1 by hand (tests/golden/calibration_two_samples.json).
+# ---------------------------------------------------------------------------
+def check_golden_calibration(golden_dir):
+    g = _load(golden_dir, "calibration_two_samples.json")
+    d, k, L, Lmax = g["d"], g["k"], g["L"], g["Lmax"]
+    S = g["sample_scores"]
+    N = len(S)
+    Qc = np.zeros((N, 1, 1, d))
+    Kc = np.zeros((N, 1, L, d))
+    for n in range(N):
+        Qc[n, 0, 0] = g["q"]
+        Kc[n, 0, :, 0] = S[n]
+    for e in g["expect"]:
+        theta, sets = ref.calibrate_ref(Qc, Kc, [L], k, MODES[e["mode"]], e["alpha"], Lmax)
+        assert len(sets[(0, L)]) == N
+        assert abs(theta[0, L - 1] - e["theta"]) < 1e-14, e
+        for LL in range(1, Lmax + 1):
+            want = -np.inf if LL <= k else e["theta"]
+            assert theta[0, LL - 1] == pytest.approx(want, abs=1e-14), (e, LL)
+
+
+def test_golden_two_sample_calibration(golden_dir):
+    check_golden_calibration(golden_dir)
+
+
+def check_golden_nearest_row(golden_dir):
+    g = _load(golden_dir, "nearest_row.json")
+    d, k, Lmax = g["d"], g["k"], g["Lmax"]
+    Nk = len(g["K_col0"])
+    Qc = np.zeros((1, 1, 2, d))
+    Qc[0, 0, 0] = g["q"][0]
+    Qc[0, 0, 1] = g["q"][1]
+    Kc = np.zeros((1, 1, Nk, d))
+    Kc[0, 0, :, 0] = g["K_col0"]
+    Kc[0, 0, :, 1] = g["K_col1"]
+    theta, _ = ref.calibrate_ref(Qc, Kc, g["row_len"], k, ref.PRE, 0.0, Lmax)
+    want = np.array([float(x) for x in g["theta"]])
+    np.testing.assert_array_equal(np.isinf(theta[0]), np.isinf(want))
+    fin = np.isfinite(want)
+    np.testing.assert_allclose(theta[0][fin], want[fin], rtol=0, atol=1e-15)
+    # beyond the table: the last entry is used
+    assert ref.theta_for_row(theta[0], 10 * Lmax) == want[-1]
+
+
+def test_golden_nearest_calibrated_row(golden_dir):
+    check_golden_nearest_row(golden_dir)
+
+
+# ---------------------------------------------------------------------------
+# Brute force on rows of 4-16 elements: a threshold calibrated on one row and
+# applied to the same row keeps exactly that row's top-k.
+# ---------------------------------------------------------------------------
+def check_bruteforce_topk(seed=2, trials=300):
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        L = int(rng.integers(4, 17))
+        k = int(rng.integers(1, L))
+        d = 4
+        vals = rng.permutation(L).astype(np.float64) * 0.37 - 1.1   # distinct
+        Qc = np.zeros((1, 1, 1, d))
+        Qc[0, 0, 0, 0] = 2.0                                        # a_j = K[j][0]
+        Kc = np.zeros((1, 1, L, d))
+        Kc[0, 0, :, 0] = vals
+        want = set(sorted(range(L), key=lambda j: -vals[j])[:k])
+        for mode in (ref.PRE, ref.POST):
+            theta, _ = ref.calibrate_ref(Qc, Kc, [L], k, mode, 0.0, L)
+            th = ref.theta_for_row(theta[0], L)
+            a = ref.row_scores(Qc[0, 0, 0], Kc[0, 0], L)
+            np.testing.assert_allclose(a, vals, rtol=0, atol=0)
+            r = ref.attend_row(a, np.eye(L), th, mode)
+            assert set(np.flatnonzero(r["keep"])) == want, (L, k, mode)
+            assert r["kept"] == k
+
+
+def test_bruteforce_calibrated_row_selects_topk():
+    check_bruteforce_topk()
+
+
+def test_bruteforce_kth_largest_all_orders():
+    # every permutation of a 5-element row with a repeated value
+    base = [3.0, -1.0, 2.0, 2.0, 0.5]
+    for perm in itertools.permutations(base):
+        srt = sorted(perm, reverse=True)
+        for k in range(1, 6):
+            assert ref.kth_largest(np.array(perm), k) == srt[k - 1]
+
+
+def test_ties_are_all_kept():
+    a = np.array([1.0, 3.0, 2.0, 2.0, 2.0, 0.0])
+    k = 2
+    th = ref.kth_largest(a, k)                 # = 2.0, shared by three keys
+    r = ref.attend_row(a, np.eye(6), th, ref.PRE)
+    assert r["kept"] == 4 and r["kept"] >= k
+    assert list(np.flatnonzero(r["keep"])) == [1, 2, 3, 4]
+
+
+def test_short_rows_are_dense():
+    rng = np.random.default_rng(3)
+    d, k, S = 8, 6, 12
+    Qc = rng.standard_normal((3, 1, S, d))
+    Kc = rng.standard_normal((3, 1, S, d))
+    theta, sets = ref.calibrate_ref(Qc, Kc, np.arange(1, S + 1), k, ref.PRE, 0.0, S)
+    assert all(L > k for (_, L) in sets)
+    assert np.all(np.isneginf(theta[0, :k])) and np.all(np.isfinite(theta[0, k:]))
+
+
+# ---------------------------------------------------------------------------
+# Identities of the method.
+# ---------------------------------------------------------------------------
+def check_sdc_exact_equals_post(seed=4, trials=50):
+    """Eq. 4: for one kept set, pre-softmax + exact SDC equals post-softmax."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        L = int(rng.integers(2, 40))
+        d = 6
+        a = rng.standard_normal(L) * 3
+        V = rng.standard_normal((L, d))
+        mu = ref.vmean_ref(V)
+        k = int(rng.integers(1, L + 1))
+        th_pre = ref.kth_largest(a, k)
+        th_post = ref.kth_largest(ref.row_softmax(a), k)
+        for vmc in (False, True):
+            p = ref.attend_row(a, V, th_pre, ref.PRE, ref.SDC_EXACT, vmc, mu)
+            q = ref.attend_row(a, V, th_post, ref.POST, ref.SDC_NONE, vmc, mu)
+            assert np.array_equal(p["keep"], q["keep"])
+            np.testing.assert_allclose(p["out"], q["out"], rtol=1e-12, atol=1e-13)
+            assert abs(p["beta"] - q["beta"]) < 1e-13
+            # the discarded mass of post-softmax is E/Z
+            assert abs(q["beta"] - q["E"] / q["Z"]) < 1e-13
+
+
+def test_sdc_exact_pre_equals_post_softmax():
+    check_sdc_exact_equals_post()
+
+
+def check_vmc_constant_values(seed=5, trials=40):
+    """Eq. 5-7: if every V row equals v, the compensated output is v for any mask."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        L = int(rng.integers(1, 30))
+        v = rng.standard_normal(5)
+        V = np.tile(v, (L, 1))
+        a = rng.standard_normal(L) * 2
+        mu = ref.vmean_ref(V)
+        th_pre = float(rng.normal(0, 2))
+        th_post = float(rng.uniform(0, 0.6))
+        cases = [(ref.POST, ref.SDC_NONE, th_post), (ref.PRE, ref.SDC_EXACT, th_pre),
+                 (ref.PRE, ref.SDC_EXPTH, th_pre)]
+        for mode, sdc, th in cases:
+            r = ref.attend_row(a, V, th, mode, sdc, True, mu)
+            np.testing.assert_allclose(r["out"], v, rtol=1e-12, atol=1e-12)
+        r = ref.attend_row(a, V, th_pre, ref.PRE, ref.SDC_NONE, True, mu)
+        want = v if r["kept"] else np.zeros(5)
+        np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-12)
+
+
+def test_vmc_constant_value_rows_give_that_row():
+    check_vmc_constant_values()
+
+
+def test_exp_threshold_is_zero_on_a_dense_row():
+    a = np.array([0.3, -0.2, 1.5])
+    V = np.arange(9.0).reshape(3, 3)
+    d = ref.attend_row(a, V, -np.inf, ref.PRE, ref.SDC_NONE)
+    e = ref.attend_row(a, V, -np.inf, ref.PRE, ref.SDC_EXPTH, True, ref.vmean_ref(V))
+    np.testing.assert_allclose(e["out"], d["out"], rtol=1e-14)
+    assert abs(e["beta"]) < 1e-15
+
+
+def test_running_mean_equals_batch_mean():
+    rng = np.random.default_rng(6)
+    V = rng.standard_normal((257, 7))
+    mu = np.zeros(7)
+    n = 0
+    for i in range(40):                         # one row at a time (decode)
+        mu = ref.vmean_update_ref(mu, n, V[i:i + 1])
+        n += 1
+    for lo, hi in [(40, 41), (41, 100), (100, 257)]:   # chunks (prefill)
+        mu = ref.vmean_update_ref(mu, n, V[lo:hi])
+        n = hi
+    np.testing.assert_allclose(mu, V.mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_tile_counts_match_bruteforce():
+    rng = np.random.default_rng(7)
+    for S, tm, tn in [(10, 4, 3), (17, 8, 8), (33, 16, 8)]:
+        keep = {i: rng.random(i + 1) < 0.1 for i in range(S)}
+        hit, total = ref.tile_counts_ref(keep, S, tm, tn)
+        tiles = {}
+        for i in range(S):
+            for j in range(i + 1):
+                key = (i // tm, j // tn)
+                tiles[key] = tiles.get(key, False) or bool(keep[i][j])
+        assert total == len(tiles)
+        assert hit == sum(tiles.values())
+
+
+def test_output_error_metric():
+    assert ref.output_rel_error([1.0, 2.0], [1.0, 2.0]) == 0.0
+    assert ref.output_rel_error([1.0, 2.002], [1.0, 2.0]) == pytest.approx(1e-3)
+
+
+# ---------------------------------------------------------------------------
+# The pins above catch plausible mistakes in the oracle.
+# ---------------------------------------------------------------------------
+def _planted(monkeypatch, name, fn, check):
+    with monkeypatch.context() as m:
+        m.setattr(ref, name, fn)
+        with pytest.raises(AssertionError):
+            check()
+
+
+def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
+    orig_scores, orig_kth = ref.row_scores, ref.kth_largest
+    orig_sample, orig_attend = ref.calibration_sample, ref.attend_row
+
+    # 1/sqrt(d) dropped from Eq. 1
+    _planted(monkeypatch, "row_scores",
+             lambda q, K, L: np.asarray(K, float)[:L] @ np.asarray(q, float),
+             check_dense_decode)
+    # off-by-one order statistic
+    _planted(monkeypatch, "kth_largest",
+             lambda x, k: orig_kth(x, min(k + 1, len(x))), check_bruteforce_topk)
+    # post-softmax quantile taken on a instead of s
+    _planted(monkeypatch, "calibration_sample",
+             lambda a, k, mode: orig_kth(a, k), lambda: check_golden_calibration(golden_dir))
+
+    # wrong sign of the VMC term, wrong gamma, wrong max in the exp-threshold term
+    def flip_beta(*args, **kw):
+        r = orig_attend(*args, **kw)
+        if len(args) > 5 and args[5]:
+            mu = np.asarray(args[6], float)
+            r["out"] = r["out"] - 2 * r["beta"] * mu
+        return r
+    _planted(monkeypatch, "attend_row", flip_beta, lambda: check_golden_sdc_vmc(golden_dir))
+
+    def gamma_doubled(*args, **kw):
+        kw = dict(kw)
+        if len(args) > 7:
+            args = args[:7] + (2 * ref.GAMMA,) + args[8:]
+        else:
+            kw["gamma"] = 2 * ref.GAMMA
+        return orig_attend(*args, **kw)
+    _planted(monkeypatch, "attend_row", gamma_doubled, lambda: check_golden_sdc_vmc(golden_dir))
+
+    # nearest-row rule replaced by "always the first calibrated row"
+    orig_fin = ref.finalize_thresholds
+
+    def first_row(sets, Hq, Lmax, k, alpha):
+        th = orig_fin(sets, Hq, Lmax, k, alpha)
+        for h in range(Hq):
+            fin = np.flatnonzero(np.isfinite(th[h]))
+            if fin.size:
+                th[h, fin] = th[h, fin[0]]
+        return th
+    _planted(monkeypatch, "finalize_thresholds", first_row,
+             lambda: check_golden_nearest_row(golden_dir))
+    assert ref.row_scores is orig_scores and ref.calibration_sample is orig_sample
