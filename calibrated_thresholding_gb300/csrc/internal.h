@@ -1,0 +1,32 @@
+// Internal launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "topt.h"
+
+namespace topt {
+
+// ------------------------------------------------------------------ decode
+size_t decode_workspace_bytes(const topt_decode_args& a);
+cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s);
+
+// ----------------------------------------------------------------- prefill
+size_t prefill_workspace_bytes(const topt_prefill_args& a);
+void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys);
+cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s);
+
+// --------------------------------------------------------------- calibrate
+size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);
+size_t calibrate_min_rows_per_pass();
+cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s);
+cudaError_t select_kth_launch(const float* x, int32_t rows, int32_t stride,
+                              const int32_t* row_len, int32_t k, float* out,
+                              int32_t* status, cudaStream_t s);
+
+// ------------------------------------------------------------------- vmean
+cudaError_t vmean_launch(const topt_vmean_args& a, cudaStream_t s);
+
+}  // namespace topt

@@ -1,0 +1,215 @@
+/*
+ * topt.h - C ABI of libtopt.so, Top-theta attention on one GB300 (sm_103a).
+ *
+ * Source of the method: "Top-Theta Attention: Sparsifying Transformers by
+ * Compensated Thresholding" (arXiv 2502.08363v2), cited below as [TopTheta].
+ *
+ *   scores      a_j = q . k_j / sqrt(d)                 [TopTheta §2.2 Eq. 1]
+ *   threshold   keep j iff x_j >= theta, x = a (pre-softmax) or
+ *               x = softmax(a) (post-softmax)            [TopTheta §3, Fig. 1]
+ *   calibration theta_r = mean + alpha*std of the per-sample k-th largest
+ *               element of row r                         [TopTheta §3.1 Alg. 1]
+ *   SDC         softmax over kept * R/(R + E~)           [TopTheta §3.2.1 Eq. 4]
+ *   VMC         p = s~ V~ + beta * mu                    [TopTheta §3.2.2 Eq. 5-7]
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a caller-owned DEVICE pointer to a dense,
+ *     row-major (C-contiguous) array in the layout stated beside it.  bf16 is
+ *     IEEE bfloat16 (2 bytes); fp32 is IEEE binary32.  16-byte alignment is
+ *     required for q, k and v tensors.
+ *   - A row with L visible keys uses theta table entry L-1; rows with
+ *     L > theta_len use entry theta_len-1.  Entries of -INFINITY keep the
+ *     whole row (dense attention).  Post-softmax entries <= 0 keep the row.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Arguments are validated on the host before anything
+ *     is launched; a failed validation returns an error and launches nothing.
+ *   - Data that lives on the device (sequence lengths, row lengths) is checked
+ *     by the kernels: a bad value makes the kernel store a nonzero
+ *     topt_status into *status (when status is not NULL) and skip that unit.
+ *     The caller zeroes *status and reads it after synchronising.
+ *   - The library allocates no device memory.  Scratch memory is the
+ *     caller's `workspace`; its size is returned by the *_workspace query.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef TOPT_H_
+#define TOPT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* topt_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  TOPT_OK = 0,
+  TOPT_EINVAL = 1,     /* bad argument value, NULL pointer, or bad device-side length */
+  TOPT_EDTYPE = 2,     /* unsupported dtype for this entry point */
+  TOPT_ESHAPE = 3,     /* unsupported or inconsistent shape */
+  TOPT_ECUDA = 4,      /* a CUDA launch or runtime call failed */
+  TOPT_ETIMEOUT = 5,   /* reserved: a bounded device-side wait gave up */
+  TOPT_EWORKSPACE = 6  /* workspace NULL or smaller than the query returned */
+} topt_status;
+
+typedef enum { TOPT_PRE = 0, TOPT_POST = 1 } topt_mode;
+
+/* Estimators of the discarded exponent sum E~ [TopTheta §3.2.1]:
+ *   EXACT  E~ = sum over discarded keys of exp(a_j - m)
+ *   EXPTH  E~ = gamma * (L - k~) * exp(theta - m)   (gamma: 0.05 in the paper)
+ * SDC applies to pre-softmax only; post-softmax ignores the field. */
+typedef enum { TOPT_SDC_NONE = 0, TOPT_SDC_EXACT = 1, TOPT_SDC_EXPTH = 2 } topt_sdc;
+
+typedef enum { TOPT_BF16 = 0, TOPT_F32 = 1 } topt_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Decode: one query token per sequence against its KV cache.               */
+/* [TopTheta §2.2 "generative decoding", Fig. 1, §3.2, §4.6 (GQA)]          */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t batch;        /* B >= 1 */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 8 */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t cache_len;    /* Nmax >= 1: token capacity of each cache */
+  int32_t theta_len;    /* Lmax >= 1: entries per head of `theta` */
+  int32_t mode;         /* topt_mode */
+  int32_t sdc;          /* topt_sdc */
+  int32_t vmc;          /* nonzero: add beta * mu  [Eq. 7] */
+  float gamma;          /* exp-threshold constant (TOPT_SDC_EXPTH) */
+  const void* q;        /* [B][Hq][d] bf16 */
+  const void* k_cache;  /* [B][Hkv][Nmax][d] bf16 */
+  const void* v_cache;  /* [B][Hkv][Nmax][d] bf16 */
+  const int32_t* seq_len; /* [B] keys per sequence incl. the current token, 1..Nmax */
+  const float* theta;   /* [Hq][Lmax] fp32, the layer's slice of the table */
+  const float* mu;      /* [B][Hkv][d] fp32 mean V row; required when vmc != 0 */
+  float* out;           /* [B][Hq][d] fp32 */
+  int32_t* kept;        /* [B][Hq] k~ per head, or NULL */
+  int32_t* vrows;       /* [B][Hkv] V rows read (union over the group), or NULL */
+  uint32_t* mask;       /* [B][Hq][ceil(Nmax/32)] kept bitmap (bit j%32 of word j/32), or NULL */
+  int32_t* status;      /* device-side error word, or NULL */
+  void* workspace;      /* scratch, >= topt_decode_workspace() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} topt_decode_args;
+
+/* Bytes of workspace topt_decode needs for these shapes (pointers unused). */
+topt_status topt_decode_workspace(const topt_decode_args* args, size_t* bytes);
+
+/* out[b][h] = Top-theta attention of q[b][h] over keys 0..seq_len[b]-1 of
+ * KV head h / (Hq/Hkv).  The whole K row range is read; only V rows kept by
+ * at least one head of the group are read.  Masked bits beyond seq_len[b]
+ * are written as 0. */
+topt_status topt_decode(const topt_decode_args* args, topt_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill: causal attention of S query rows; row i sees keys 0..i.         */
+/* [TopTheta §2.2 "prefill phase", §3, §3.2]                                 */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t batch;        /* B */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t seq;          /* S >= 1 */
+  int32_t theta_len;    /* Lmax */
+  int32_t dtype;        /* topt_dtype of q, k, v */
+  int32_t mode, sdc, vmc;
+  float gamma;
+  const void* q;        /* [B][Hq][S][d] */
+  const void* k;        /* [B][Hkv][S][d] */
+  const void* v;        /* [B][Hkv][S][d] */
+  const float* theta;   /* [Hq][Lmax] */
+  float* out;           /* [B][Hq][S][d] fp32; VMC uses the prefix mean of V rows 0..i */
+  int32_t* kept;        /* [B][Hq][S] k~ per row, or NULL */
+  uint32_t* mask;       /* [B][Hq][S][ceil(S/32)] kept bitmap, or NULL */
+  unsigned long long* tiles; /* [2] += (P.V tiles executed, causal tiles), or NULL */
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+} topt_prefill_args;
+
+topt_status topt_prefill_workspace(const topt_prefill_args* args, size_t* bytes);
+/* Row and key extent of the tiles counted in `tiles` for these arguments. */
+topt_status topt_prefill_tile_shape(const topt_prefill_args* args, int32_t* tile_rows,
+                                    int32_t* tile_keys);
+topt_status topt_prefill(const topt_prefill_args* args, topt_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Calibration [TopTheta §3.1, Algorithm 1], one layer per call.            */
+/* ------------------------------------------------------------------------ */
+enum { TOPT_CALIB_RESET = 1, TOPT_CALIB_FINALIZE = 2 };
+
+typedef struct {
+  int32_t n_seqs;       /* N >= 0 calibration sequences in this call */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t n_rows;       /* R query rows per sequence */
+  int32_t n_keys;       /* Nk keys per sequence */
+  int32_t theta_len;    /* Lmax */
+  int32_t dtype;        /* topt_dtype of q and keys */
+  int32_t mode;         /* topt_mode: quantile taken on a (PRE) or softmax(a) (POST) */
+  int32_t k;            /* target kept elements per row, >= 1 */
+  float alpha;          /* offset in standard deviations */
+  int32_t flags;        /* TOPT_CALIB_RESET: zero the accumulators first;
+                           TOPT_CALIB_FINALIZE: write theta after accumulating */
+  const void* q;        /* [N][Hq][R][d] */
+  const void* keys;     /* [N][Hkv][Nk][d] */
+  const int32_t* row_len; /* [R] keys seen by each query row, 1..Nk (causal prefill: r+1) */
+  double* acc;          /* [2][Hq][Lmax] running sum and sum of squares of samples */
+  int32_t* count;       /* [Hq][Lmax] number of samples */
+  float* theta;         /* [Hq][Lmax] written on FINALIZE */
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+} topt_calib_args;
+
+/* Minimum workspace is one row of scores per 8 rows; more lets a call process
+ * more rows per launch.  *bytes is the size that processes every row of the
+ * call at once, capped at 1 GiB. */
+topt_status topt_calibrate_workspace(const topt_calib_args* args, size_t* bytes);
+
+/* For every sequence, query head h and row i with L = row_len[i] > k: adds
+ * the k-th largest score of the row (PRE) or its softmax value (POST) to the
+ * accumulators at [h][L-1].  FINALIZE then writes, per head and L:
+ *   count > 0         mean + alpha * std (std with ddof 1; 0 for one sample)
+ *   L <= k            -INFINITY (the row is kept whole)
+ *   otherwise         the value of the nearest calibrated L (ties: smaller L);
+ *                     -INFINITY if the head has no calibrated row.          */
+topt_status topt_calibrate(const topt_calib_args* args, topt_stream stream);
+
+/* Building block of calibration, exposed for testing: out[r] = the k-th
+ * largest of x[r][0 .. row_len[r]-1] (x is [rows][row_stride] fp32 on the
+ * device; -0.0 counts as +0.0; -INFINITY if row_len[r] < k).  Exact: the
+ * result is one of the inputs, bit for bit. */
+topt_status topt_select_kth(const float* x, int32_t rows, int32_t row_stride,
+                            const int32_t* row_len, int32_t k, float* out,
+                            int32_t* status, topt_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Running mean of V rows [TopTheta §3.2.2: "mu can be maintained as a       */
+/* running mean during generative decoding"]                                 */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t batch, n_kv_heads, head_dim, cache_len;
+  int32_t dtype;        /* topt_dtype of v_cache */
+  int32_t n_new;        /* t >= 1 rows appended per sequence */
+  const void* v_cache;  /* [B][Hkv][Nmax][d] */
+  const int32_t* n_old; /* [B] rows already in mu; new rows are n_old..n_old+t-1 */
+  float* mu;            /* [B][Hkv][d] fp32, updated in place */
+  int32_t* status;
+} topt_vmean_args;
+
+/* mu <- (n_old * mu + sum of the t new rows) / (n_old + t).  t = 1 is the
+ * per-token decode update; n_old = 0, t = S initialises mu from a prefill. */
+topt_status topt_vmean_update(const topt_vmean_args* args, topt_stream stream);
+
+/* Library version (major*10000 + minor*100 + patch) and status names. */
+int32_t topt_version(void);
+const char* topt_status_string(topt_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TOPT_H_ */

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads, exports every function include/topt.h declares, and
+rejects bad arguments on the host before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from calibrated_thresholding_gb300 import build, topt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return topt.lib()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*(?:topt_status|int32_t|const char\*)\s+(topt_\w+)\s*\(",
+                                    text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("topt_calibrate", "topt_prefill", "topt_decode", "topt_vmean_update"):
+        assert n in names
+    assert set(topt.SYMBOLS) >= names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert L.topt_version() == 100
+    assert L.topt_status_string(3) == b"unsupported shape"
+
+
+def _decode_args(**kw):
+    a = topt.DecodeArgs()
+    a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim = 2, 8, 2, 128
+    a.cache_len, a.theta_len, a.mode, a.sdc, a.vmc, a.gamma = 64, 64, topt.POST, 0, 0, 0.05
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_decode_validation_rejects_on_host(L):
+    n = ctypes.c_size_t(0)
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args()), ctypes.byref(n)) == 0
+    assert n.value > 0
+    # workspace covers the fp32 score block of every head
+    assert n.value >= 2 * 8 * 64 * 4
+    bad = [dict(head_dim=96), dict(n_q_heads=6, n_kv_heads=4), dict(n_q_heads=32, n_kv_heads=2),
+           dict(batch=0), dict(cache_len=0)]
+    for kw in bad:
+        assert L.topt_decode_workspace(ctypes.byref(_decode_args(**kw)), ctypes.byref(n)) == 3, kw
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(mode=7)), ctypes.byref(n)) == 1
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=3)), ctypes.byref(n)) == 1
+    # NULL tensors: rejected before any launch
+    assert L.topt_decode(ctypes.byref(_decode_args()), None) == 1
+
+
+def test_prefill_and_calibrate_validation(L):
+    a = topt.PrefillArgs()
+    a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim, a.seq, a.theta_len = 1, 4, 2, 64, 100, 100
+    a.dtype, a.mode = topt.BF16, topt.PRE
+    r, c = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert L.topt_prefill_tile_shape(ctypes.byref(a), ctypes.byref(r), ctypes.byref(c)) == 0
+    assert r.value > 0 and c.value > 0
+    a.dtype = 9
+    assert L.topt_prefill(ctypes.byref(a), None) == 2
+    a.dtype = topt.F32
+    assert L.topt_prefill(ctypes.byref(a), None) == 1          # NULL tensors
+
+    c = topt.CalibArgs()
+    c.n_seqs, c.n_q_heads, c.n_kv_heads, c.head_dim, c.n_rows, c.n_keys = 2, 4, 2, 64, 10, 10
+    c.theta_len, c.dtype, c.mode, c.k, c.alpha = 10, topt.BF16, topt.PRE, 0, 0.0
+    assert L.topt_calibrate(ctypes.byref(c), None) == 1        # k < 1
+    c.k = 3
+    n = ctypes.c_size_t(0)
+    assert L.topt_calibrate_workspace(ctypes.byref(c), ctypes.byref(n)) == 0
+    assert n.value >= 2 * 4 * 10 * 10 * 4
+    c.flags = 8
+    assert L.topt_calibrate(ctypes.byref(c), None) == 1
+    assert L.topt_select_kth(None, 3, 4, None, 1, None, None, None) == 1
+
+    v = topt.VmeanArgs()
+    v.batch, v.n_kv_heads, v.head_dim, v.cache_len, v.dtype, v.n_new = 1, 1, 64, 8, topt.BF16, 9
+    assert L.topt_vmean_update(ctypes.byref(v), None) == 3     # t > capacity
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(topt, "_lib", None)
+    monkeypatch.setattr(topt, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        topt.lib()
