@@ -425,27 +425,34 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
   }
 }
 
+cudaError_t record(void* ev, cudaStream_t s) {
+  return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
+}
+
 template <int D, int G>
-cudaError_t launch_dg(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_dg(const DecodeParams& p, void* const* ev, cudaStream_t s) {
   const unsigned pairs = (unsigned)(p.B * p.Hkv);
+  cudaError_t e;
+  if ((e = record(ev[0], s)) != cudaSuccess) return e;
   decode_scores_kernel<D, G><<<dim3(p.nch1, pairs), kThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = record(ev[1], s)) != cudaSuccess) return e;
   decode_select_kernel<D, G><<<dim3(p.nch2, pairs), kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return record(ev[2], s);
 }
 
 template <int D>
-cudaError_t launch_d(const DecodeParams& p, int G, cudaStream_t s) {
+cudaError_t launch_d(const DecodeParams& p, int G, void* const* ev, cudaStream_t s) {
   switch (G) {
-    case 1: return launch_dg<D, 1>(p, s);
-    case 2: return launch_dg<D, 2>(p, s);
-    case 3: return launch_dg<D, 3>(p, s);
-    case 4: return launch_dg<D, 4>(p, s);
-    case 5: return launch_dg<D, 5>(p, s);
-    case 6: return launch_dg<D, 6>(p, s);
-    case 7: return launch_dg<D, 7>(p, s);
-    case 8: return launch_dg<D, 8>(p, s);
+    case 1: return launch_dg<D, 1>(p, ev, s);
+    case 2: return launch_dg<D, 2>(p, ev, s);
+    case 3: return launch_dg<D, 3>(p, ev, s);
+    case 4: return launch_dg<D, 4>(p, ev, s);
+    case 5: return launch_dg<D, 5>(p, ev, s);
+    case 6: return launch_dg<D, 6>(p, ev, s);
+    case 7: return launch_dg<D, 7>(p, ev, s);
+    case 8: return launch_dg<D, 8>(p, ev, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -490,8 +497,8 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
   p.counter = reinterpret_cast<unsigned*>(ws + l.counter);
   const int G = a.n_q_heads / a.n_kv_heads;
-  if (a.head_dim == 128) return launch_d<128>(p, G, s);
-  if (a.head_dim == 64) return launch_d<64>(p, G, s);
+  if (a.head_dim == 128) return launch_d<128>(p, G, a.events, s);
+  if (a.head_dim == 64) return launch_d<64>(p, G, a.events, s);
   return cudaErrorInvalidValue;
 }
 

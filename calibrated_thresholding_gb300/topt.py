@@ -39,7 +39,7 @@ class DecodeArgs(ctypes.Structure):
                 ("cache_len", i32), ("theta_len", i32), ("mode", i32), ("sdc", i32), ("vmc", i32),
                 ("gamma", f32), ("q", vp), ("k_cache", vp), ("v_cache", vp), ("seq_len", vp),
                 ("theta", vp), ("mu", vp), ("out", vp), ("kept", vp), ("vrows", vp), ("mask", vp),
-                ("status", vp), ("workspace", vp), ("workspace_bytes", sz)]
+                ("status", vp), ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 3)]
 
 
 class PrefillArgs(ctypes.Structure):

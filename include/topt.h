@@ -91,6 +91,10 @@ typedef struct {
   int32_t* status;      /* device-side error word, or NULL */
   void* workspace;      /* scratch, >= topt_decode_workspace() bytes, 256-byte aligned */
   size_t workspace_bytes;
+  /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
+   * `stream` before the score pass, between the passes and after the select
+   * pass, so a caller can time the two kernels of one call. */
+  void* events[3];
 } topt_decode_args;
 
 /* Bytes of workspace topt_decode needs for these shapes (pointers unused). */

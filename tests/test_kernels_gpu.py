@@ -148,7 +148,7 @@ def test_decode_dense_and_empty():
         assert torch.equal(res["vrows"].cpu(), torch.tensor([[777] * Hkv, [40] * Hkv], dtype=torch.int32))
         check_decode(q, K, V, seq_len, dense, mode, sdc, vmc, mu, res)
     # nothing survives: post + VMC and pre + SDC give mu, pre without SDC gives 0
-    for mode, th in ((ref.POST, 0.99), (ref.PRE, 1e4)):
+    for mode, th in ((ref.POST, 1.5), (ref.PRE, 1e4)):
         full = torch.full((Hq, Nmax), th, device="cuda")
         for sdc, vmc in ((ref.SDC_NONE, True), (ref.SDC_EXACT, True), (ref.SDC_NONE, False)):
             res = run_decode(q, K, V, seq_len, full, mode, sdc, vmc, mu)
