@@ -33,7 +33,8 @@ constexpr int kThreads = kWarps * kWarp;
 constexpr int kCh1 = 512;                       // keys per score CTA
 constexpr int kKeysPerWarp1 = kCh1 / kWarps;    // 128 = 8 MMA tiles of 16 keys
 constexpr int kCh2 = 1024;                      // keys per select CTA
-constexpr int kGatherUnroll = 8;                // V rows in flight per half-warp
+constexpr int kGatherUnroll = 8;                // V rows in flight per thread slot
+constexpr int kMaxDevices = 64;
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -216,28 +217,38 @@ __global__ void __launch_bounds__(kThreads) decode_scores_kernel(const DecodePar
 
 // ----------------------------------------------------------------------------
 // Pass 2: threshold, compaction of the group union, V gather, SDC/VMC.
+// Phase A: every warp loads the scores of its 8 groups of 32 keys at once,
+// ballots the per-head masks, ORs them into the group union and writes the
+// union's (key, weights) entries into a CTA-wide list at positions given by a
+// popcount prefix (deterministic order).  Phase B: all threads gather the
+// listed V rows, 16 bytes per lane, several rows in flight per thread.
 // ----------------------------------------------------------------------------
+constexpr int kGroupsPerWarp = kCh2 / (kWarps * kWarp);   // 8
+
+template <int D, int G>
+struct SelectSmem {
+  int j[kCh2];                       // union keys of the CTA, in key order
+  float w[kCh2][G];                  // exp(a - m) per head (0 if the head drops it)
+  float acc[kWarps][G][D];           // per-warp partial sums (phase B reduction)
+  float M[G], Z[G], T[G], th[G];
+  float r[kWarps][G];
+  int kt[kWarps][G];
+  int cnt[kWarps];
+  int last;
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodeParams p) {
-  constexpr int LPR = D / 8;        // lanes per V row (16 bytes each)
-  constexpr int RPW = kWarp / LPR;  // V rows per warp instruction
+  constexpr int LPR = D / 8;           // lanes per V row (16 bytes each)
+  constexpr int SLOTS = kThreads / LPR;  // V rows per CTA instruction
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
   const int pair = blockIdx.y;
   const int chunk = blockIdx.x;
   const int b = pair / p.Hkv;
   const int kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int sub = lane / LPR;       // which row of the warp instruction
-  const int dl = lane % LPR;        // which 8 d values
-
-  __shared__ float s_M[G], s_Z[G], s_T[G], s_th[G];
-  __shared__ float s_w[kWarps][32][G];
-  __shared__ int s_j[kWarps][32];
-  __shared__ float s_acc[kWarps][G][D];
-  __shared__ float s_r[kWarps][G];
-  __shared__ int s_kt[kWarps][G];
-  __shared__ int s_nu[kWarps];
-  __shared__ int s_last;
 
   const int L = p.seq_len[b];
   if (L < 1 || L > p.Nmax) return;  // reported by pass 1
@@ -252,88 +263,108 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
     ms_warp_merge(m, z, 1);
     if (lane == 0) {
       const float th = p.theta[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)];
-      s_M[h] = m;
-      s_Z[h] = z;
-      s_th[h] = th;
-      s_T[h] = score_bound(p.mode, th, m, z);
+      sm.M[h] = m;
+      sm.Z[h] = z;
+      sm.th[h] = th;
+      sm.T[h] = score_bound(p.mode, th, m, z);
     }
   }
   __syncthreads();
 
-  float T[G], M[G], Rl[G], acc[G][8];
+  // ---- phase A: thresholds and union list
+  const int c_begin = chunk * kCh2;
+  const int c_end = min(c_begin + kCh2, L);
+  const int w_begin = c_begin + warp * kGroupsPerWarp * kWarp;
+  const float* lbase = p.logits + (size_t)pair * G * p.Nmax;
+  const uint64_t pol = l2_evict_first_policy();
+  float wv[kGroupsPerWarp][G];
+#pragma unroll
+  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+    const int j = w_begin + gi * kWarp + lane;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      wv[gi][h] = j < c_end ? ld_hint_f32(lbase + (size_t)h * p.Nmax + j, pol) : -CUDART_INF_F;
+  }
+  float Rl[G];
   int kt[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    T[h] = s_T[h];
-    M[h] = s_M[h];
     Rl[h] = 0.f;
     kt[h] = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
   }
-  int nu = 0;
-
-  const int c_begin = chunk * kCh2;
-  const int c_end = min(c_begin + kCh2, L);
-  const int scan_end = min(c_begin + kCh2, p.mask_words * 32);
-  const float* lbase = p.logits + (size_t)pair * G * p.Nmax;
-  const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D;
-  const uint64_t pol = l2_evict_first_policy();
+  unsigned uni[kGroupsPerWarp];
+  int wcount = 0;
   uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
-
-  for (int j0 = c_begin + warp * kWarp; j0 < scan_end; j0 += kWarps * kWarp) {
-    if (j0 >= c_end) {
-      if (mrow && lane < G) mrow[(size_t)lane * p.mask_words + (j0 >> 5)] = 0u;
-      continue;
-    }
-    const int j = j0 + lane;
-    const bool valid = j < c_end;
-    float w[G];
-    unsigned uni = 0u;
+#pragma unroll
+  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+    const int j0 = w_begin + gi * kWarp;
+    const bool valid = j0 + lane < c_end;
+    unsigned u = 0u;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float a = valid ? ld_hint_f32(lbase + (size_t)h * p.Nmax + j, pol) : -CUDART_INF_F;
-      const bool keep = valid && (a >= T[h]);
-      w[h] = keep ? __expf(a - M[h]) : 0.f;
-      Rl[h] += w[h];
+      const float a = wv[gi][h];
+      const bool keep = valid && (a >= sm.T[h]);
+      wv[gi][h] = keep ? __expf(a - sm.M[h]) : 0.f;
+      Rl[h] += wv[gi][h];
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
       kt[h] += __popc(bal);
-      uni |= bal;
-      if (mrow && lane == 0) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      u |= bal;
+      if (mrow && lane == 0 && j0 < p.mask_words * 32)
+        mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
     }
-    const int nsel = __popc(uni);
-    if (nsel == 0) continue;
-    nu += nsel;
-    if ((uni >> lane) & 1u) {
-      const int pos = __popc(uni & ((1u << lane) - 1u));
-      s_j[warp][pos] = j;
+    uni[gi] = u;
+    wcount += __popc(u);
+  }
+  if (lane == 0) sm.cnt[warp] = wcount;
+  __syncthreads();
+  int base = 0, total = 0;
 #pragma unroll
-      for (int h = 0; h < G; ++h) s_w[warp][pos][h] = w[h];
+  for (int w = 0; w < kWarps; ++w) {
+    base += (w < warp) ? sm.cnt[w] : 0;
+    total += sm.cnt[w];
+  }
+#pragma unroll
+  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+    if ((uni[gi] >> lane) & 1u) {
+      const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
+      sm.j[pos] = w_begin + gi * kWarp + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h) sm.w[pos][h] = wv[gi][h];
     }
-    __syncwarp();
-    for (int base = 0; base < nsel; base += RPW * kGatherUnroll) {
-      uint4 vv[kGatherUnroll];
+    base += __popc(uni[gi]);
+  }
+  __syncthreads();
+
+  // ---- phase B: gather the listed V rows
+  const int slot = threadIdx.x / LPR;
+  const int dl = threadIdx.x % LPR;
+  const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * 8;
+  float acc[G][8];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int pos = base + RPW * u + sub;
-        if (pos < nsel) vv[u] = ld_nc16(vbase + (size_t)s_j[warp][pos] * D + dl * 8);
-      }
+  for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int pos = base + RPW * u + sub;
-        if (pos < nsel) {
-          const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
-                               bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+    for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
+  for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
+    uint4 vv[kGatherUnroll];
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float wh = s_w[warp][pos][h];
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int r = r0 + u * SLOTS + slot;
+      if (r < total) vv[u] = ld_nc16(vbase + (size_t)sm.j[r] * D);
+    }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
-          }
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int r = r0 + u * SLOTS + slot;
+      if (r < total) {
+        const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
+                             bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float wh = sm.w[r][h];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
         }
       }
     }
-    __syncwarp();
   }
 
   // Reduce over the rows of a warp instruction, then over warps.
@@ -350,27 +381,23 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s_acc[warp][h][dl * 8 + e] = acc[h][e];
+      for (int e = 0; e < 8; ++e) sm.acc[warp][h][dl * 8 + e] = acc[h][e];
   }
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      s_r[warp][h] = Rl[h];
-      s_kt[warp][h] = kt[h];
+      sm.r[warp][h] = Rl[h];
+      sm.kt[warp][h] = kt[h];
     }
-    s_nu[warp] = nu;
   }
   __syncthreads();
 
-  int nu_cta = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) nu_cta += s_nu[w];
   const size_t pc = (size_t)pair * p.nch2 + chunk;
-  if (nu_cta > 0) {
+  if (total > 0) {
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += s_acc[w][idx / D][idx % D];
+      for (int w = 0; w < kWarps; ++w) s += sm.acc[w][idx / D][idx % D];
       p.part_num[pc * G * D + idx] = s;
     }
   }
@@ -379,23 +406,23 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
     int k = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      r += s_r[w][threadIdx.x];
-      k += s_kt[w][threadIdx.x];
+      r += sm.r[w][threadIdx.x];
+      k += sm.kt[w][threadIdx.x];
     }
     p.part_r[pc * G + threadIdx.x] = r;
     p.part_kt[pc * G + threadIdx.x] = k;
   }
-  if (threadIdx.x == 0) p.part_nu[pc] = nu_cta;
+  if (threadIdx.x == 0) p.part_nu[pc] = total;
 
   // The last CTA of the pair to arrive combines (no CTA ever waits).
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(&p.counter[pair], 1u);
-    s_last = (prev == (unsigned)gridDim.x - 1u);
+    sm.last = (prev == (unsigned)gridDim.x - 1u);
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!sm.last) return;
   __threadfence();
 
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
@@ -410,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
       ktot += __ldcg(p.part_kt + q * G + h);
     }
     float sc, beta;
-    out_scale_beta(p.mode, p.sdc, p.gamma, s_th[h], s_M[h], s_Z[h], R, L, ktot, sc, beta);
+    out_scale_beta(p.mode, p.sdc, p.gamma, sm.th[h], sm.M[h], sm.Z[h], R, L, ktot, sc, beta);
     float o = num * sc;
     if (p.vmc) o = fmaf(beta, p.mu[(size_t)pair * D + dd], o);
     const size_t row = (size_t)b * p.Hq + kvh * G + h;
@@ -425,6 +452,11 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
   }
 }
 
+template <int D, int G>
+constexpr size_t select_smem_bytes() {
+  return sizeof(SelectSmem<D, G>);
+}
+
 cudaError_t record(void* ev, cudaStream_t s) {
   return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
 }
@@ -437,7 +469,18 @@ cudaError_t launch_dg(const DecodeParams& p, void* const* ev, cudaStream_t s) {
   decode_scores_kernel<D, G><<<dim3(p.nch1, pairs), kThreads, 0, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = record(ev[1], s)) != cudaSuccess) return e;
-  decode_select_kernel<D, G><<<dim3(p.nch2, pairs), kThreads, 0, s>>>(p);
+  constexpr size_t smem = select_smem_bytes<D, G>();
+  static bool attr_set[kMaxDevices] = {};  // per device, per (D, G) instantiation
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+      return e;
+    attr_set[dev] = true;
+  }
+  decode_select_kernel<D, G><<<dim3(p.nch2, pairs), kThreads, smem, s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return record(ev[2], s);
 }
