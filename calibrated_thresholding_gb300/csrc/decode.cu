@@ -3,25 +3,29 @@
 // [TopTheta] = "Top-Theta Attention: Sparsifying Transformers by Compensated
 // Thresholding" (arXiv 2502.08363v2).  Decode is bound by reading the K cache
 // ([TopTheta §2.2, generative decoding]); Top-theta's saving is that only the
-// V rows that survive the threshold are read ([TopTheta §1, §4.6]).
+// V rows that survive the threshold are read ([TopTheta §1, §4.6]).  A "pair"
+// is one (sequence, KV head) and its G = Hq/Hkv query heads ([TopTheta §2.2,
+// GQA]).
 //
-// Two kernels per call, one (batch, KV head) "pair" = the G = Hq/Hkv query
-// heads of a GQA group ([TopTheta §2.2, GQA]):
+// One persistent cooperative kernel per call, all CTAs co-resident:
 //
-//  1. decode_scores_kernel: streams the pair's K rows once with 16-byte
-//     loads (L2 evict-first) and computes the G x n score block
-//     a = q K^T / sqrt(d) [Eq. 1] with one m16n8k16 bf16 MMA per 16 keys and
-//     16 d (keys are the M side, the G query heads the N side).  Scores go
-//     to a workspace array that stays L2-resident (G x 4 bytes per key, vs
-//     2 d bytes of K), and each CTA writes per-head softmax partials (m, Z).
-//  2. decode_select_kernel: merges the (m, Z) partials of the pair, turns
-//     theta into a bound on the score (post-softmax: s >= theta <=>
-//     a >= m + ln theta + ln Z), thresholds 32 keys per warp in registers,
-//     ballots the per-head masks, ORs them into the group union, compacts
-//     the union with a popcount prefix into shared memory, gathers only those
-//     V rows and accumulates sum exp(a - m) V per head.  The last CTA of a
-//     pair (atomic ticket, no waiting) combines the partial sums and applies
-//     SDC [Eq. 4] and VMC [Eq. 5-7].
+//  Phase 1 (scores).  The valid keys of all pairs are cut into 128-key units
+//   and every warp of the grid takes an equal contiguous run of units.  Each
+//   warp streams its K rows through a private shared-memory ring with 1-D
+//   TMA bulk copies (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first,
+//   completion on an mbarrier), computes the G x 16 score block per tile with
+//   m16n8k16 bf16 MMAs (keys on the M side, query heads on the N side), writes
+//   a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4 bytes per
+//   key) and per-unit softmax partials (m, Z).
+//  Grid barrier (bounded spin; a timeout sets TOPT_ETIMEOUT, never hangs).
+//  Phase 2 (select).  Each CTA takes one slice of one pair: merges the pair's
+//   (m, Z) partials, turns theta into a bound on the score (post-softmax:
+//   s >= theta <=> a >= m + ln theta + ln Z), ballots the per-head masks of
+//   32 keys per warp, ORs them into the group union, compacts the union into
+//   a shared list by popcount prefix, gathers only those V rows (16-byte
+//   loads) and accumulates sum exp(a - m) V per head.  The last CTA of a pair
+//   to finish (atomic ticket, nothing waits) combines the slices and applies
+//   SDC [Eq. 4] and VMC [Eq. 5-7].
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,11 +34,17 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
-constexpr int kCh1 = 512;                       // keys per score CTA
-constexpr int kKeysPerWarp1 = kCh1 / kWarps;    // 128 = 8 MMA tiles of 16 keys
-constexpr int kCh2 = 1024;                      // keys per select CTA
-constexpr int kGatherUnroll = 8;                // V rows in flight per thread slot
+constexpr int kTile = 16;                          // keys per MMA tile / per bulk copy
+constexpr int kUnit = 128;                         // keys per softmax partial
+constexpr int kStages = 4;                         // ring slots per warp
+// Keys per select sub-chunk (the union list's capacity): smaller for large
+// groups so a warp's staged scores stay in registers.
+template <int G>
+__host__ __device__ constexpr int sub_keys() { return G > 4 ? 512 : 1024; }
+constexpr int kGatherUnroll = 4;                   // V rows in flight per thread slot
+constexpr int kMaxBatch = 1024;
 constexpr int kMaxDevices = 64;
+constexpr unsigned kSpinLimit = 1u << 22;          // x >= 256 ns sleep: ~1 s
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -50,37 +60,107 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  int mask_words, nch1, nch2;
+  int mask_words, upp, ipp;
   // workspace
   float* logits;      // [pairs][G][Nmax]
-  float2* stats;      // [pairs][nch1][G]
-  float* part_num;    // [pairs][nch2][G][D]
-  float* part_r;      // [pairs][nch2][G]
-  int* part_kt;       // [pairs][nch2][G]
-  int* part_nu;       // [pairs][nch2]
+  float2* stats;      // [pairs][upp][G]
+  float* part_num;    // [pairs][ipp][G][D]
+  float* part_r;      // [pairs][ipp][G]
+  int* part_kt;       // [pairs][ipp][G]
+  int* part_nu;       // [pairs][ipp]
   unsigned* counter;  // [pairs]
+  unsigned* barrier;  // [2]: arrivals, generation
 };
 
 struct DecodeLayout {
-  size_t logits, stats, part_num, part_r, part_kt, part_nu, counter, total;
+  size_t logits, stats, part_num, part_r, part_kt, part_nu, counter, barrier, total;
 };
 
-DecodeLayout decode_layout(const topt_decode_args& a) {
+DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
   const size_t pairs = (size_t)a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t nch1 = (a.cache_len + kCh1 - 1) / kCh1;
-  const size_t nch2 = (a.cache_len + kCh2 - 1) / kCh2;
+  const size_t upp = (a.cache_len + kUnit - 1) / kUnit;
   DecodeLayout l;
   size_t off = 0;
   l.logits = off;   off += align256(pairs * G * (size_t)a.cache_len * sizeof(float));
-  l.stats = off;    off += align256(pairs * nch1 * G * sizeof(float2));
-  l.part_num = off; off += align256(pairs * nch2 * G * (size_t)a.head_dim * sizeof(float));
-  l.part_r = off;   off += align256(pairs * nch2 * G * sizeof(float));
-  l.part_kt = off;  off += align256(pairs * nch2 * G * sizeof(int));
-  l.part_nu = off;  off += align256(pairs * nch2 * sizeof(int));
+  l.stats = off;    off += align256(pairs * upp * G * sizeof(float2));
+  l.part_num = off; off += align256(pairs * ipp * G * (size_t)a.head_dim * sizeof(float));
+  l.part_r = off;   off += align256(pairs * ipp * G * sizeof(float));
+  l.part_kt = off;  off += align256(pairs * ipp * G * sizeof(int));
+  l.part_nu = off;  off += align256(pairs * ipp * sizeof(int));
   l.counter = off;  off += align256(pairs * sizeof(unsigned));
+  l.barrier = off;  off += 256;
   l.total = off;
   return l;
+}
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  const uint32_t a = smem_u32(bar);
+  for (unsigned it = 0; it < (1u << 26); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ float ld_cg_hint_f32(const float* p, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+// Grid-wide barrier for a cooperative launch (all CTAs co-resident); its two
+// words are zeroed on the stream before each launch.  The spin is bounded; on
+// timeout the CTA records TOPT_ETIMEOUT and continues.
+__device__ void grid_sync(unsigned* bar, int32_t* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned* vgen = bar + 1;
+    const unsigned gen = *vgen;
+    __threadfence();
+    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
+    if (arrived == gridDim.x) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      unsigned spins = 0;
+      while (*vgen == gen) {
+        __nanosleep(256);
+        if (++spins > kSpinLimit) {
+          set_status(status, TOPT_ETIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
 }
 
 // Online (max, sum) update with two new scores (either may be -inf).
@@ -93,171 +173,232 @@ __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) 
 }
 
 // ----------------------------------------------------------------------------
-// Pass 1: scores and softmax partials.
-// MMA fragment mapping.  Thread (g = lane/4, t = lane%4) loads, for key rows
-// g and g+8 of a 16-key tile, the 16 bytes at d = 32p + 8t .. 32p + 8t + 7
-// (p = 0 .. D/32-1), i.e. words w0..w3 of two bf16 each.  Because a dot
-// product may visit d in any order, k-step s (0, 1) of slab p uses
-//   A row g:   {w[2s], w[2s+1]} of row g      (columns 2t,2t+1 and 2t+8,2t+9)
+// Shared memory: phase 1 rings and phase 2 lists share one buffer.
+// ----------------------------------------------------------------------------
+template <int D>
+struct Ring {
+  uint64_t bar[kWarps][kStages];
+  __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
+};
+
+template <int D, int G>
+struct Lists {
+  int j[sub_keys<G>()];       // union keys of the sub-chunk, in key order
+  float w[sub_keys<G>()][G];  // exp(a - m) per head (0 if the head drops the key)
+  float acc[kWarps][G][D];
+  float r[kWarps][G];
+  int kt[kWarps][G];
+  int cnt[kWarps];
+};
+
+template <int D, int G>
+struct DecodeSmem {
+  int ustart[kMaxBatch + 1];  // first unit of each sequence
+  int nunit[kMaxBatch];       // units per KV head of each sequence
+  float M[G], Z[G], T[G], th[G];
+  int last;
+  union {
+    Ring<D> ring;
+    Lists<D, G> lists;
+  } u;
+};
+
+// Unit index -> (pair, unit within the pair).
+template <int D, int G>
+__device__ __forceinline__ void unit_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int u, int& pair, int& c) {
+  int lo = 0, hi = B - 1;  // last b with ustart[b] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sm.ustart[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int b = lo;
+  const int nu = sm.nunit[b];
+  const int r = u - sm.ustart[b];
+  const int kvh = r / nu;
+  pair = b * Hkv + kvh;
+  c = r - kvh * nu;
+}
+
+// ----------------------------------------------------------------------------
+// Phase 1.  MMA fragment mapping: thread (g = lane/4, t = lane%4) uses, for
+// key rows g and g+8 of a tile, the 16 bytes at d = 32p + 8t .. +7
+// (p = 0 .. D/32-1) as words w0..w3 (two bf16 each).  A dot product may visit
+// d in any order, so k-step s (0, 1) of slab p uses
+//   A row g:   {w[2s], w[2s+1]} of row g      (k = 2t,2t+1 and 2t+8,2t+9)
 //   A row g+8: {w[2s], w[2s+1]} of row g+8
 //   B col g:   {w[2s], w[2s+1]} of the q row of head g
-// which assigns the same 4 d values to the same k slots of A and B, so each
-// MMA adds an exact partial dot product.  C then holds (key g, heads 2t, 2t+1)
-// and (key g+8, heads 2t, 2t+1).
+// so every MMA adds an exact partial dot product; C then holds (key g, heads
+// 2t, 2t+1) and (key g+8, heads 2t, 2t+1).
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_scores_kernel(const DecodeParams p) {
-  static_assert(D % 32 == 0 && G >= 1 && G <= 8, "shape");
+__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total_units) {
   constexpr int NP = D / 32;
-  const int pair = blockIdx.y;
-  const int chunk = blockIdx.x;
-  const int b = pair / p.Hkv;
-  const int kvh = pair - b * p.Hkv;
+  constexpr unsigned kTileBytes = kTile * D * 2;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  __shared__ float s_m[kWarps][8], s_z[kWarps][8];
+  const long TW = (long)gridDim.x * kWarps;
+  const long gw = (long)blockIdx.x * kWarps + warp;
+  const int u_begin = (int)((long)total_units * gw / TW);
+  const int u_end = (int)((long)total_units * (gw + 1) / TW);
+  if (u_begin >= u_end) return;
 
-  if (chunk == 0 && threadIdx.x == 0) p.counter[pair] = 0u;
-  float2* st = p.stats + ((size_t)pair * p.nch1 + chunk) * G;
-  const int L = p.seq_len[b];
-  const int key_begin = chunk * kCh1;
-  if (L < 1 || L > p.Nmax || key_begin >= L) {
-    if ((L < 1 || L > p.Nmax) && chunk == 0 && threadIdx.x == 0) set_status(p.status, TOPT_EINVAL);
-    if (threadIdx.x < G) st[threadIdx.x] = make_float2(-CUDART_INF_F, 0.f);
-    return;
-  }
-
-  uint32_t qf[NP][4];
-  if (g < G) {
-    const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + kvh * G + g) * D;
-#pragma unroll
-    for (int pp = 0; pp < NP; ++pp) {
-      const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
-      qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
-    }
-  } else {
-#pragma unroll
-    for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
-  }
-
-  const __nv_bfloat16* kbase = p.k + (size_t)pair * p.Nmax * D;
-  float* lbase = p.logits + (size_t)pair * G * p.Nmax;
+  uint64_t* bars = sm.u.ring.bar[warp];
+  unsigned char* slots = &sm.u.ring.slot[warp][0][0];
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep_pol = l2_evict_last_policy();
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // Producer iterator (lane 0 issues the copies; all lanes track it).
+  int pu = u_begin, pt = 0, ppair = 0, pc = 0, pL = 0, pnt = 0;
+  auto p_load_unit = [&]() {
+    unit_of(sm, p.B, p.Hkv, pu, ppair, pc);
+    pL = p.seq_len[ppair / p.Hkv];
+    pnt = (min(kUnit, pL - pc * kUnit) + kTile - 1) / kTile;
+  };
+  p_load_unit();
+  long issued = 0;
+  auto issue = [&]() {  // copy the producer's current tile into the next slot
+    const int key0 = pc * kUnit + pt * kTile;
+    const unsigned bytes = (unsigned)min(kTile, pL - key0) * D * 2;
+    const int s = (int)(issued % kStages);
+    if (lane == 0) {
+      mbar_expect_tx(&bars[s], bytes);
+      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)ppair * p.Nmax + key0) * D, bytes, &bars[s], pol);
+    }
+    ++issued;
+    if (++pt == pnt) {
+      pt = 0;
+      if (++pu < u_end) p_load_unit();
+    }
+  };
+  for (int s = 0; s < kStages && pu < u_end; ++s) issue();
+
   const float scale = p.sm_scale;
   const int h0 = 2 * t, h1 = 2 * t + 1;
-  float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
-
-  const int wbeg = key_begin + warp * kKeysPerWarp1;
-  const int wend = min(wbeg + kKeysPerWarp1, L);
-  for (int tile = wbeg; tile < wend; tile += 32) {
-    uint4 ka[2][NP], kb[2][NP];
+  uint32_t qf[NP][4];
+  int qpair = -1;
+  long consumed = 0;
+  for (int u = u_begin; u < u_end; ++u) {
+    int pair, c;
+    unit_of(sm, p.B, p.Hkv, u, pair, c);
+    const int b = pair / p.Hkv;
+    const int kvh = pair - b * p.Hkv;
+    const int L = p.seq_len[b];
+    const int ntile = (min(kUnit, L - c * kUnit) + kTile - 1) / kTile;
+    if (pair != qpair) {
+      qpair = pair;
+      if (g < G) {
+        const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + kvh * G + g) * D;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int r0 = min(tile + 16 * u + g, L - 1);
-      const int r1 = min(tile + 16 * u + g + 8, L - 1);
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
+          qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
+        }
+      } else {
 #pragma unroll
-      for (int pp = 0; pp < NP; ++pp) {
-        ka[u][pp] = ld_stream16(kbase + (size_t)r0 * D + 32 * pp + 8 * t, pol);
-        kb[u][pp] = ld_stream16(kbase + (size_t)r1 * D + 32 * pp + 8 * t, pol);
+        for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
       }
     }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int key0 = tile + 16 * u;
-      if (key0 >= wend) break;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float* lbase = p.logits + (size_t)pair * G * p.Nmax;
+    float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
+    for (int tt = 0; tt < ntile; ++tt) {
+      const int s = (int)(consumed % kStages);
+      const unsigned parity = (unsigned)((consumed / kStages) & 1);
+      if (!mbar_wait(&bars[s], parity)) set_status(p.status, TOPT_ETIMEOUT);
+      const unsigned char* tile = slots + (size_t)s * kTileBytes;
+      uint4 ka[NP], kb[NP];
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) {
-        const uint32_t wa[4] = {ka[u][pp].x, ka[u][pp].y, ka[u][pp].z, ka[u][pp].w};
-        const uint32_t wb[4] = {kb[u][pp].x, kb[u][pp].y, kb[u][pp].z, kb[u][pp].w};
+        ka[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)g * D * 2 + (32 * pp + 8 * t) * 2);
+        kb[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)(g + 8) * D * 2 + (32 * pp + 8 * t) * 2);
+      }
+      float cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const uint32_t af[4] = {wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1]};
-          const uint32_t bf[2] = {qf[pp][2 * s], qf[pp][2 * s + 1]};
-          mma_16816_bf16(c, af, bf);
+      for (int pp = 0; pp < NP; ++pp) {
+        const uint32_t wa[4] = {ka[pp].x, ka[pp].y, ka[pp].z, ka[pp].w};
+        const uint32_t wb[4] = {kb[pp].x, kb[pp].y, kb[pp].z, kb[pp].w};
+#pragma unroll
+        for (int ss = 0; ss < 2; ++ss) {
+          const uint32_t af[4] = {wa[2 * ss], wb[2 * ss], wa[2 * ss + 1], wb[2 * ss + 1]};
+          const uint32_t bf[2] = {qf[pp][2 * ss], qf[pp][2 * ss + 1]};
+          mma_16816_bf16(cc, af, bf);
         }
       }
+      ++consumed;
+      // The slot's data is consumed (the MMAs used it): refill it.
+      __syncwarp();
+      if (pu < u_end) {
+        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue();
+      }
+      const int key0 = c * kUnit + tt * kTile;
       const int j0 = key0 + g;
       const int j1 = key0 + g + 8;
-      const float a00 = j0 < wend ? c[0] * scale : -CUDART_INF_F;
-      const float a01 = j0 < wend ? c[1] * scale : -CUDART_INF_F;
-      const float a10 = j1 < wend ? c[2] * scale : -CUDART_INF_F;
-      const float a11 = j1 < wend ? c[3] * scale : -CUDART_INF_F;
+      const float a00 = j0 < L ? cc[0] * scale : -CUDART_INF_F;
+      const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
+      const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
+      const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
       if (h0 < G) {
-        if (j0 < wend) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j0, a00, keep_pol);
-        if (j1 < wend) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j1, a10, keep_pol);
+        if (j0 < L) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j0, a00, keep_pol);
+        if (j1 < L) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j1, a10, keep_pol);
         ms_add2(m0, z0, a00, a10);
       }
       if (h1 < G) {
-        if (j0 < wend) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j0, a01, keep_pol);
-        if (j1 < wend) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j1, a11, keep_pol);
+        if (j0 < L) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j0, a01, keep_pol);
+        if (j1 < L) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j1, a11, keep_pol);
         ms_add2(m1, z1, a01, a11);
       }
     }
+    // Partial of this unit: merge over the 8 key rows (lane bits 2..4).
+    ms_warp_merge(m0, z0, 4);
+    ms_warp_merge(m1, z1, 4);
+    if (g == 0) {
+      float2* st = p.stats + ((size_t)pair * p.upp + c) * G;
+      if (h0 < G) st[h0] = make_float2(m0, z0);
+      if (h1 < G) st[h1] = make_float2(m1, z1);
+    }
   }
-
-  // Merge over the 8 key rows (lane bits 2..4), then over warps.
-  ms_warp_merge(m0, z0, 4);
-  ms_warp_merge(m1, z1, 4);
-  if (g == 0) {
-    s_m[warp][h0] = m0; s_z[warp][h0] = z0;
-    s_m[warp][h1] = m1; s_z[warp][h1] = z1;
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    float m = -CUDART_INF_F, z = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) ms_merge(m, z, s_m[w][threadIdx.x], s_z[w][threadIdx.x]);
-    st[threadIdx.x] = make_float2(m, z);
-  }
+  // Every issued copy has been waited for; retire the barriers before the
+  // buffer is reused by phase 2.
+  __syncwarp();
+  if (lane == 0)
+    for (int s = 0; s < kStages; ++s)
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[s])) : "memory");
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------------------
-// Pass 2: threshold, compaction of the group union, V gather, SDC/VMC.
-// Phase A: every warp loads the scores of its 8 groups of 32 keys at once,
-// ballots the per-head masks, ORs them into the group union and writes the
-// union's (key, weights) entries into a CTA-wide list at positions given by a
-// popcount prefix (deterministic order).  Phase B: all threads gather the
-// listed V rows, 16 bytes per lane, several rows in flight per thread.
+// Phase 2: one slice (several 1024-key sub-chunks) of one pair per CTA.
 // ----------------------------------------------------------------------------
-constexpr int kGroupsPerWarp = kCh2 / (kWarps * kWarp);   // 8
-
 template <int D, int G>
-struct SelectSmem {
-  int j[kCh2];                       // union keys of the CTA, in key order
-  float w[kCh2][G];                  // exp(a - m) per head (0 if the head drops it)
-  float acc[kWarps][G][D];           // per-warp partial sums (phase B reduction)
-  float M[G], Z[G], T[G], th[G];
-  float r[kWarps][G];
-  int kt[kWarps][G];
-  int cnt[kWarps];
-  int last;
-};
-
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodeParams p) {
-  constexpr int LPR = D / 8;           // lanes per V row (16 bytes each)
-  constexpr int SLOTS = kThreads / LPR;  // V rows per CTA instruction
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
-  const int pair = blockIdx.y;
-  const int chunk = blockIdx.x;
+__device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int item) {
+  constexpr int LPR = D / 8;              // lanes per V row (16 bytes each)
+  constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
+  constexpr int kSub = sub_keys<G>();
+  constexpr int kGroupsPerWarp = kSub / (kWarps * kWarp);
+  Lists<D, G>& ls = sm.u.lists;
+  const int pair = item / p.ipp;
+  const int slice = item - pair * p.ipp;
   const int b = pair / p.Hkv;
   const int kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
   const int L = p.seq_len[b];
-  if (L < 1 || L > p.Nmax) return;  // reported by pass 1
+  if (L < 1 || L > p.Nmax) return;  // reported in phase 1
 
   // Softmax statistics of the whole row, per head of the group.
+  const int nu = (L + kUnit - 1) / kUnit;
   for (int h = warp; h < G; h += kWarps) {
     float m = -CUDART_INF_F, z = 0.f;
-    for (int c = lane; c < p.nch1; c += kWarp) {
-      const float2 v = p.stats[((size_t)pair * p.nch1 + c) * G + h];
+    for (int c = lane; c < nu; c += kWarp) {
+      const float2 v = __ldcg(p.stats + ((size_t)pair * p.upp + c) * G + h);
       ms_merge(m, z, v.x, v.y);
     }
     ms_warp_merge(m, z, 1);
@@ -271,97 +412,114 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
   }
   __syncthreads();
 
-  // ---- phase A: thresholds and union list
-  const int c_begin = chunk * kCh2;
-  const int c_end = min(c_begin + kCh2, L);
-  const int w_begin = c_begin + warp * kGroupsPerWarp * kWarp;
+  // This slice's sub-chunks; mask words past L are spread over the slices.
+  const int nsub = (L + kSub - 1) / kSub;
+  const int s_begin = (int)((long)nsub * slice / p.ipp);
+  const int s_end = (int)((long)nsub * (slice + 1) / p.ipp);
+  uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
+  if (mrow) {
+    const int w0 = (L + 31) >> 5;
+    const int span = p.mask_words - w0;
+    const int lo = w0 + (int)((long)span * slice / p.ipp);
+    const int hi = w0 + (int)((long)span * (slice + 1) / p.ipp);
+    for (int i = threadIdx.x; i < (hi - lo) * G; i += kThreads) {
+      const int h = i % G;
+      const int w = lo + i / G;
+      mrow[(size_t)h * p.mask_words + w] = 0u;
+    }
+  }
+
   const float* lbase = p.logits + (size_t)pair * G * p.Nmax;
   const uint64_t pol = l2_evict_first_policy();
-  float wv[kGroupsPerWarp][G];
-#pragma unroll
-  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-    const int j = w_begin + gi * kWarp + lane;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      wv[gi][h] = j < c_end ? ld_hint_f32(lbase + (size_t)h * p.Nmax + j, pol) : -CUDART_INF_F;
-  }
-  float Rl[G];
-  int kt[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    Rl[h] = 0.f;
-    kt[h] = 0;
-  }
-  unsigned uni[kGroupsPerWarp];
-  int wcount = 0;
-  uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
-#pragma unroll
-  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-    const int j0 = w_begin + gi * kWarp;
-    const bool valid = j0 + lane < c_end;
-    unsigned u = 0u;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float a = wv[gi][h];
-      const bool keep = valid && (a >= sm.T[h]);
-      wv[gi][h] = keep ? __expf(a - sm.M[h]) : 0.f;
-      Rl[h] += wv[gi][h];
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      kt[h] += __popc(bal);
-      u |= bal;
-      if (mrow && lane == 0 && j0 < p.mask_words * 32)
-        mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
-    }
-    uni[gi] = u;
-    wcount += __popc(u);
-  }
-  if (lane == 0) sm.cnt[warp] = wcount;
-  __syncthreads();
-  int base = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    base += (w < warp) ? sm.cnt[w] : 0;
-    total += sm.cnt[w];
-  }
-#pragma unroll
-  for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-    if ((uni[gi] >> lane) & 1u) {
-      const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
-      sm.j[pos] = w_begin + gi * kWarp + lane;
-#pragma unroll
-      for (int h = 0; h < G; ++h) sm.w[pos][h] = wv[gi][h];
-    }
-    base += __popc(uni[gi]);
-  }
-  __syncthreads();
-
-  // ---- phase B: gather the listed V rows
   const int slot = threadIdx.x / LPR;
   const int dl = threadIdx.x % LPR;
   const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * 8;
-  float acc[G][8];
+  float T[G], M[G], Rl[G], acc[G][8];
+  int kt[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int h = 0; h < G; ++h) {
+    T[h] = sm.T[h];
+    M[h] = sm.M[h];
+    Rl[h] = 0.f;
+    kt[h] = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-  for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
-    uint4 vv[kGatherUnroll];
+  }
+  int nsel_total = 0;
+
+  for (int sc = s_begin; sc < s_end; ++sc) {
+    const int c_begin = sc * kSub;
+    const int c_end = min(c_begin + kSub, L);
+    const int w_begin = c_begin + warp * kGroupsPerWarp * kWarp;
+    float wv[kGroupsPerWarp][G];
 #pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * SLOTS + slot;
-      if (r < total) vv[u] = ld_nc16(vbase + (size_t)sm.j[r] * D);
+    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+      const int j = w_begin + gi * kWarp + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        wv[gi][h] = j < c_end ? ld_cg_hint_f32(lbase + (size_t)h * p.Nmax + j, pol) : -CUDART_INF_F;
+    }
+    unsigned uni[kGroupsPerWarp];
+    int wcount = 0;
+#pragma unroll
+    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+      const int j0 = w_begin + gi * kWarp;
+      const bool valid = j0 + lane < c_end;
+      unsigned un = 0u;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float a = wv[gi][h];
+        const bool keep = valid && (a >= T[h]);
+        wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
+        Rl[h] += wv[gi][h];
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        kt[h] += __popc(bal);
+        un |= bal;
+        if (mrow && lane == 0 && j0 < c_end) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      }
+      uni[gi] = un;
+      wcount += __popc(un);
+    }
+    __syncthreads();  // previous sub-chunk's list is consumed
+    if (lane == 0) ls.cnt[warp] = wcount;
+    __syncthreads();
+    int base = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      base += (w < warp) ? ls.cnt[w] : 0;
+      total += ls.cnt[w];
     }
 #pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * SLOTS + slot;
-      if (r < total) {
-        const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
-                             bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+      if ((uni[gi] >> lane) & 1u) {
+        const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
+        ls.j[pos] = w_begin + gi * kWarp + lane;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float wh = sm.w[r][h];
+        for (int h = 0; h < G; ++h) ls.w[pos][h] = wv[gi][h];
+      }
+      base += __popc(uni[gi]);
+    }
+    __syncthreads();
+    nsel_total += total;
+    for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
+      uint4 vv[kGatherUnroll];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int r = r0 + u * SLOTS + slot;
+        if (r < total) vv[u] = ld_nc16(vbase + (size_t)ls.j[r] * D);
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int r = r0 + u * SLOTS + slot;
+        if (r < total) {
+          const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
+                               bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float wh = ls.w[r][h];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
+          }
         }
       }
     }
@@ -377,27 +535,28 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
     }
     Rl[h] = warp_sum(Rl[h]);
   }
+  __syncthreads();  // the list is no longer read
   if (lane < LPR) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sm.acc[warp][h][dl * 8 + e] = acc[h][e];
+      for (int e = 0; e < 8; ++e) ls.acc[warp][h][dl * 8 + e] = acc[h][e];
   }
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      sm.r[warp][h] = Rl[h];
-      sm.kt[warp][h] = kt[h];
+      ls.r[warp][h] = Rl[h];
+      ls.kt[warp][h] = kt[h];
     }
   }
   __syncthreads();
 
-  const size_t pc = (size_t)pair * p.nch2 + chunk;
-  if (total > 0) {
+  const size_t pc = (size_t)pair * p.ipp + slice;
+  if (nsel_total > 0) {
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += sm.acc[w][idx / D][idx % D];
+      for (int w = 0; w < kWarps; ++w) s += ls.acc[w][idx / D][idx % D];
       p.part_num[pc * G * D + idx] = s;
     }
   }
@@ -406,39 +565,38 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
     int k = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      r += sm.r[w][threadIdx.x];
-      k += sm.kt[w][threadIdx.x];
+      r += ls.r[w][threadIdx.x];
+      k += ls.kt[w][threadIdx.x];
     }
     p.part_r[pc * G + threadIdx.x] = r;
     p.part_kt[pc * G + threadIdx.x] = k;
   }
-  if (threadIdx.x == 0) p.part_nu[pc] = total;
+  if (threadIdx.x == 0) p.part_nu[pc] = nsel_total;
 
-  // The last CTA of the pair to arrive combines (no CTA ever waits).
+  // The last CTA of the pair to arrive combines (nothing waits).
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(&p.counter[pair], 1u);
-    sm.last = (prev == (unsigned)gridDim.x - 1u);
+    sm.last = (prev == (unsigned)p.ipp - 1u);
   }
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
     const int h = idx / D;
     const int dd = idx - h * D;
     float num = 0.f, R = 0.f;
     int ktot = 0;
-    for (int c = 0; c < p.nch2; ++c) {
-      const size_t q = (size_t)pair * p.nch2 + c;
+    for (int c = 0; c < p.ipp; ++c) {
+      const size_t q = (size_t)pair * p.ipp + c;
       if (__ldcg(p.part_nu + q) > 0) num += __ldcg(p.part_num + q * G * D + idx);
       R += __ldcg(p.part_r + q * G + h);
       ktot += __ldcg(p.part_kt + q * G + h);
     }
-    float sc, beta;
-    out_scale_beta(p.mode, p.sdc, p.gamma, sm.th[h], sm.M[h], sm.Z[h], R, L, ktot, sc, beta);
-    float o = num * sc;
+    float scl, beta;
+    out_scale_beta(p.mode, p.sdc, p.gamma, sm.th[h], sm.M[h], sm.Z[h], R, L, ktot, scl, beta);
+    float o = num * scl;
     if (p.vmc) o = fmaf(beta, p.mu[(size_t)pair * D + dd], o);
     const size_t row = (size_t)b * p.Hq + kvh * G + h;
     p.out[row * D + dd] = o;
@@ -446,67 +604,157 @@ __global__ void __launch_bounds__(kThreads) decode_select_kernel(const DecodePar
   }
   if (threadIdx.x == 0) {
     int tot = 0;
-    for (int c = 0; c < p.nch2; ++c) tot += __ldcg(p.part_nu + (size_t)pair * p.nch2 + c);
+    for (int c = 0; c < p.ipp; ++c) tot += __ldcg(p.part_nu + (size_t)pair * p.ipp + c);
     if (p.vrows) p.vrows[pair] = tot;
-    p.counter[pair] = 0u;
   }
 }
 
 template <int D, int G>
-constexpr size_t select_smem_bytes() {
-  return sizeof(SelectSmem<D, G>);
+__global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw);
+
+  // Units per sequence (every KV head of a sequence has the same length).
+  if (threadIdx.x < kWarp) {
+    const int lane = threadIdx.x;
+    const int per = (p.B + kWarp - 1) / kWarp;
+    int run = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = lane * per + i;
+      if (b < p.B) {
+        const int L = p.seq_len[b];
+        int nu = 0;
+        if (L >= 1 && L <= p.Nmax) nu = (L + kUnit - 1) / kUnit;
+        else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
+        sm.nunit[b] = nu > 0 ? nu : 1;
+        run += nu * p.Hkv;
+      }
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < kWarp; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int acc = incl - run;
+    for (int i = 0; i < per; ++i) {
+      const int b = lane * per + i;
+      if (b < p.B) {
+        sm.ustart[b] = acc;
+        const int L = p.seq_len[b];
+        if (L >= 1 && L <= p.Nmax) acc += ((L + kUnit - 1) / kUnit) * p.Hkv;
+      }
+    }
+    if (lane == kWarp - 1) sm.ustart[p.B] = incl;
+  }
+  const int pairs = p.B * p.Hkv;
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < pairs; i += gridDim.x * kThreads) p.counter[i] = 0u;
+  __syncthreads();
+
+  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
+  grid_sync(p.barrier, p.status);
+  for (int item = blockIdx.x; item < pairs * p.ipp; item += gridDim.x) {
+    phase_select<D, G>(p, sm, item);
+    __syncthreads();
+  }
 }
+
+// Co-resident CTAs of the cooperative grid, per device and instantiation.
+template <int D, int G>
+cudaError_t grid_of(int& grid) {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (cached[dev] == 0) {
+    const size_t smem = sizeof(DecodeSmem<D, G>);
+    if ((e = cudaFuncSetAttribute(decode_fused_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+      return e;
+    int per_sm = 0, sms = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel<D, G>, kThreads, smem)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cached[dev] = per_sm * sms;
+  }
+  grid = cached[dev];
+  return cudaSuccess;
+}
+
+// Select slices per pair: enough to give every CTA about one slice.
+int items_per_pair(int grid, int pairs, int cache_len, int G) {
+  const int sub = G > 4 ? sub_keys<8>() : sub_keys<4>();
+  const int nsub = (cache_len + sub - 1) / sub;
+  int ipp = grid / pairs;
+  if (ipp < 1) ipp = 1;
+  if (ipp > nsub) ipp = nsub;
+  return ipp;
+}
+
+// Upper bound of the cooperative grid on any supported GPU (for the
+// workspace query, which must not need a device).
+constexpr int kMaxGrid = 160 * 16;
 
 cudaError_t record(void* ev, cudaStream_t s) {
   return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const DecodeParams& p, void* const* ev, cudaStream_t s) {
-  const unsigned pairs = (unsigned)(p.B * p.Hkv);
+cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s) {
+  int grid = 0;
   cudaError_t e;
-  if ((e = record(ev[0], s)) != cudaSuccess) return e;
-  decode_scores_kernel<D, G><<<dim3(p.nch1, pairs), kThreads, 0, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = record(ev[1], s)) != cudaSuccess) return e;
-  constexpr size_t smem = select_smem_bytes<D, G>();
-  static bool attr_set[kMaxDevices] = {};  // per device, per (D, G) instantiation
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem)) != cudaSuccess)
-      return e;
-    attr_set[dev] = true;
-  }
-  decode_select_kernel<D, G><<<dim3(p.nch2, pairs), kThreads, smem, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return record(ev[2], s);
+  if ((e = grid_of<D, G>(grid)) != cudaSuccess) return e;
+  const int pairs = p.B * p.Hkv;
+  p.ipp = items_per_pair(grid, pairs, p.Nmax, G);
+  const DecodeLayout l = decode_layout(a, p.ipp);
+  if (a.workspace_bytes < l.total) return cudaErrorInvalidValue;
+  char* ws = static_cast<char*>(a.workspace);
+  p.logits = reinterpret_cast<float*>(ws + l.logits);
+  p.stats = reinterpret_cast<float2*>(ws + l.stats);
+  p.part_num = reinterpret_cast<float*>(ws + l.part_num);
+  p.part_r = reinterpret_cast<float*>(ws + l.part_r);
+  p.part_kt = reinterpret_cast<int*>(ws + l.part_kt);
+  p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
+  p.counter = reinterpret_cast<unsigned*>(ws + l.counter);
+  p.barrier = reinterpret_cast<unsigned*>(ws + l.barrier);
+  if ((e = record(a.events[0], s)) != cudaSuccess) return e;
+  // The grid barrier starts from zeroed words (the workspace may hold anything).
+  if ((e = cudaMemsetAsync(p.barrier, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
+  void* kargs[] = {&p};
+  e = cudaLaunchCooperativeKernel((const void*)decode_fused_kernel<D, G>, dim3(grid), dim3(kThreads), kargs,
+                                  sizeof(DecodeSmem<D, G>), s);
+  if (e != cudaSuccess) return e;
+  return record(a.events[1], s);
 }
 
 template <int D>
-cudaError_t launch_d(const DecodeParams& p, int G, void* const* ev, cudaStream_t s) {
+cudaError_t launch_d(const DecodeParams& p, int G, const topt_decode_args& a, cudaStream_t s) {
   switch (G) {
-    case 1: return launch_dg<D, 1>(p, ev, s);
-    case 2: return launch_dg<D, 2>(p, ev, s);
-    case 3: return launch_dg<D, 3>(p, ev, s);
-    case 4: return launch_dg<D, 4>(p, ev, s);
-    case 5: return launch_dg<D, 5>(p, ev, s);
-    case 6: return launch_dg<D, 6>(p, ev, s);
-    case 7: return launch_dg<D, 7>(p, ev, s);
-    case 8: return launch_dg<D, 8>(p, ev, s);
+    case 1: return launch_dg<D, 1>(p, a, s);
+    case 2: return launch_dg<D, 2>(p, a, s);
+    case 3: return launch_dg<D, 3>(p, a, s);
+    case 4: return launch_dg<D, 4>(p, a, s);
+    case 5: return launch_dg<D, 5>(p, a, s);
+    case 6: return launch_dg<D, 6>(p, a, s);
+    case 7: return launch_dg<D, 7>(p, a, s);
+    case 8: return launch_dg<D, 8>(p, a, s);
   }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-size_t decode_workspace_bytes(const topt_decode_args& a) { return decode_layout(a).total; }
+size_t decode_workspace_bytes(const topt_decode_args& a) {
+  const int pairs = a.batch * a.n_kv_heads;
+  const int G = a.n_q_heads / a.n_kv_heads;
+  return decode_layout(a, items_per_pair(kMaxGrid, pairs, a.cache_len, G)).total;
+}
 
 cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
-  const DecodeLayout l = decode_layout(a);
-  char* ws = static_cast<char*>(a.workspace);
+  if (a.batch > kMaxBatch) return cudaErrorInvalidValue;
   DecodeParams p;
   p.B = a.batch;
   p.Hq = a.n_q_heads;
@@ -530,18 +778,11 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.status = a.status;
   p.mask_words = (a.cache_len + 31) / 32;
-  p.nch1 = (a.cache_len + kCh1 - 1) / kCh1;
-  p.nch2 = (a.cache_len + kCh2 - 1) / kCh2;
-  p.logits = reinterpret_cast<float*>(ws + l.logits);
-  p.stats = reinterpret_cast<float2*>(ws + l.stats);
-  p.part_num = reinterpret_cast<float*>(ws + l.part_num);
-  p.part_r = reinterpret_cast<float*>(ws + l.part_r);
-  p.part_kt = reinterpret_cast<int*>(ws + l.part_kt);
-  p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
-  p.counter = reinterpret_cast<unsigned*>(ws + l.counter);
+  p.upp = (a.cache_len + kUnit - 1) / kUnit;
+  p.ipp = 1;
   const int G = a.n_q_heads / a.n_kv_heads;
-  if (a.head_dim == 128) return launch_d<128>(p, G, a.events, s);
-  if (a.head_dim == 64) return launch_d<64>(p, G, a.events, s);
+  if (a.head_dim == 128) return launch_d<128>(p, G, a, s);
+  if (a.head_dim == 64) return launch_d<64>(p, G, a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -92,8 +92,8 @@ typedef struct {
   void* workspace;      /* scratch, >= topt_decode_workspace() bytes, 256-byte aligned */
   size_t workspace_bytes;
   /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
-   * `stream` before the score pass, between the passes and after the select
-   * pass, so a caller can time the two kernels of one call. */
+   * `stream` right before [0] and right after [1] the decode kernel, so a
+   * caller can time it; [2] is reserved and must be NULL. */
   void* events[3];
 } topt_decode_args;
 
