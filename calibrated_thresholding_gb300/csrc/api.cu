@@ -28,6 +28,7 @@ topt_status check_decode_shape(const topt_decode_args* a) {
   if (!dim_ok(a->head_dim)) return TOPT_ESHAPE;
   if (a->n_q_heads % a->n_kv_heads != 0) return TOPT_ESHAPE;
   if (a->n_q_heads / a->n_kv_heads > 8) return TOPT_ESHAPE;
+  if (a->batch > decode_max_batch()) return TOPT_ESHAPE;
   return check_common_mode(a->mode, a->sdc);
 }
 

@@ -7,25 +7,32 @@
 // is one (sequence, KV head) and its G = Hq/Hkv query heads ([TopTheta §2.2,
 // GQA]).
 //
-// One persistent cooperative kernel per call, all CTAs co-resident:
+// One persistent kernel per call (one CTA slot per SM resource, no grid-wide
+// barrier), fed by two atomic work queues:
 //
-//  Phase 1 (scores).  The valid keys of all pairs are cut into 128-key units
-//   and every warp of the grid takes an equal contiguous run of units.  Each
-//   warp streams its K rows through a private shared-memory ring with 1-D
-//   TMA bulk copies (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first,
-//   completion on an mbarrier), computes the G x 16 score block per tile with
-//   m16n8k16 bf16 MMAs (keys on the M side, query heads on the N side), writes
+//  Scores.  The valid keys of every pair are cut into 128-key units, handed to
+//   warps in pair order by an atomic counter (each warp asks one unit ahead,
+//   so the atomic's latency is hidden).  A warp streams its units' K rows
+//   through a private shared-memory ring with 1-D TMA bulk copies
+//   (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first, completion on an
+//   mbarrier), computes each 16-key x G-head score block with m16n8k16 bf16
+//   MMAs (keys on the M side, query heads on the N side), writes
 //   a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4 bytes per
-//   key) and per-unit softmax partials (m, Z).
-//  Grid barrier (bounded spin; a timeout sets TOPT_ETIMEOUT, never hangs).
-//  Phase 2 (select).  Each CTA takes one slice of one pair: merges the pair's
-//   (m, Z) partials, turns theta into a bound on the score (post-softmax:
-//   s >= theta <=> a >= m + ln theta + ln Z), ballots the per-head masks of
-//   32 keys per warp, ORs them into the group union, compacts the union into
-//   a shared list by popcount prefix, gathers only those V rows (16-byte
-//   loads) and accumulates sum exp(a - m) V per head.  The last CTA of a pair
-//   to finish (atomic ticket, nothing waits) combines the slices and applies
-//   SDC [Eq. 4] and VMC [Eq. 5-7].
+//   key) and the unit's softmax partial (m, Z), then counts the unit as done
+//   for its pair.
+//  Select.  When a CTA's warps find the unit queue empty, the CTA takes
+//   (pair, slice) items in pair order from the second queue, waits (bounded)
+//   until the pair's units are all done, merges the (m, Z) partials, turns
+//   theta into a bound on the score (post-softmax: s >= theta <=>
+//   a >= m + ln theta + ln Z), ballots per-head masks of 32 keys per warp, ORs
+//   them into the group union, compacts the union into a shared list by
+//   popcount prefix, gathers only those V rows (16-byte loads) and accumulates
+//   sum exp(a - m) V per head.  The last CTA of a pair (atomic ticket, nothing
+//   waits) combines the slices and applies SDC [Eq. 4] and VMC [Eq. 5-7].
+//
+// No wait can deadlock: a CTA only waits for units that warps already took,
+// and a unit is only taken by a running warp.  Every wait is bounded and
+// reports TOPT_ETIMEOUT instead of hanging.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,16 +42,18 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
 constexpr int kTile = 16;                          // keys per MMA tile / per bulk copy
-constexpr int kUnit = 128;                         // keys per softmax partial
+constexpr int kUnit = 128;                         // keys per work unit and softmax partial
 constexpr int kStages = 4;                         // ring slots per warp
+constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
+constexpr int kGatherUnroll = 8;                   // V rows in flight per thread slot
+constexpr int kMaxBatch = 256;
+constexpr int kMaxDevices = 64;
+constexpr unsigned kSpinLimit = 1u << 24;          // bounded waits: x >= 32 ns sleep
+
 // Keys per select sub-chunk (the union list's capacity): smaller for large
 // groups so a warp's staged scores stay in registers.
 template <int G>
 __host__ __device__ constexpr int sub_keys() { return G > 4 ? 512 : 1024; }
-constexpr int kGatherUnroll = 4;                   // V rows in flight per thread slot
-constexpr int kMaxBatch = 1024;
-constexpr int kMaxDevices = 64;
-constexpr unsigned kSpinLimit = 1u << 22;          // x >= 256 ns sleep: ~1 s
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -68,12 +77,13 @@ struct DecodeParams {
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
   int* part_nu;       // [pairs][ipp]
-  unsigned* counter;  // [pairs]
-  unsigned* barrier;  // [2]: arrivals, generation
+  unsigned* queues;   // [2]: next unit, next select item       } zeroed before
+  unsigned* done;     // [pairs]: units finished                } every launch
+  unsigned* ticket;   // [pairs]: select slices finished        }
 };
 
 struct DecodeLayout {
-  size_t logits, stats, part_num, part_r, part_kt, part_nu, counter, barrier, total;
+  size_t logits, stats, part_num, part_r, part_kt, part_nu, counters, counters_bytes, total;
 };
 
 DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
@@ -88,8 +98,9 @@ DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
   l.part_r = off;   off += align256(pairs * ipp * G * sizeof(float));
   l.part_kt = off;  off += align256(pairs * ipp * G * sizeof(int));
   l.part_nu = off;  off += align256(pairs * ipp * sizeof(int));
-  l.counter = off;  off += align256(pairs * sizeof(unsigned));
-  l.barrier = off;  off += 256;
+  l.counters = off;
+  l.counters_bytes = align256((2 + 2 * pairs) * sizeof(unsigned));
+  off += l.counters_bytes;
   l.total = off;
   return l;
 }
@@ -133,34 +144,10 @@ __device__ __forceinline__ float ld_cg_hint_f32(const float* p, uint64_t pol) {
   asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
   return v;
 }
-
-// Grid-wide barrier for a cooperative launch (all CTAs co-resident); its two
-// words are zeroed on the stream before each launch.  The spin is bounded; on
-// timeout the CTA records TOPT_ETIMEOUT and continues.
-__device__ void grid_sync(unsigned* bar, int32_t* status) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    volatile unsigned* vgen = bar + 1;
-    const unsigned gen = *vgen;
-    __threadfence();
-    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
-      unsigned spins = 0;
-      while (*vgen == gen) {
-        __nanosleep(256);
-        if (++spins > kSpinLimit) {
-          set_status(status, TOPT_ETIMEOUT);
-          break;
-        }
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Online (max, sum) update with two new scores (either may be -inf).
@@ -173,11 +160,12 @@ __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) 
 }
 
 // ----------------------------------------------------------------------------
-// Shared memory: phase 1 rings and phase 2 lists share one buffer.
+// Shared memory: the score rings and the select lists share one buffer.
 // ----------------------------------------------------------------------------
 template <int D>
 struct Ring {
   uint64_t bar[kWarps][kStages];
+  int uq[kWarps][kQueue];  // units taken by each warp, in order
   __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
 };
 
@@ -195,7 +183,9 @@ template <int D, int G>
 struct DecodeSmem {
   int ustart[kMaxBatch + 1];  // first unit of each sequence
   int nunit[kMaxBatch];       // units per KV head of each sequence
+  int len[kMaxBatch];         // seq_len, staged once per CTA
   float M[G], Z[G], T[G], th[G];
+  int item;
   int last;
   union {
     Ring<D> ring;
@@ -221,7 +211,7 @@ __device__ __forceinline__ void unit_of(const DecodeSmem<D, G>& sm, int B, int H
 }
 
 // ----------------------------------------------------------------------------
-// Phase 1.  MMA fragment mapping: thread (g = lane/4, t = lane%4) uses, for
+// Scores.  MMA fragment mapping: thread (g = lane/4, t = lane%4) uses, for
 // key rows g and g+8 of a tile, the 16 bytes at d = 32p + 8t .. +7
 // (p = 0 .. D/32-1) as words w0..w3 (two bf16 each).  A dot product may visit
 // d in any order, so k-step s (0, 1) of slab p uses
@@ -239,13 +229,9 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  const long TW = (long)gridDim.x * kWarps;
-  const long gw = (long)blockIdx.x * kWarps + warp;
-  const int u_begin = (int)((long)total_units * gw / TW);
-  const int u_end = (int)((long)total_units * (gw + 1) / TW);
-  if (u_begin >= u_end) return;
 
   uint64_t* bars = sm.u.ring.bar[warp];
+  int* uq = sm.u.ring.uq[warp];
   unsigned char* slots = &sm.u.ring.slot[warp][0][0];
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep_pol = l2_evict_last_policy();
@@ -255,14 +241,26 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   }
   __syncwarp();
 
-  // Producer iterator (lane 0 issues the copies; all lanes track it).
-  int pu = u_begin, pt = 0, ppair = 0, pc = 0, pL = 0, pnt = 0;
-  auto p_load_unit = [&]() {
-    unit_of(sm, p.B, p.Hkv, pu, ppair, pc);
-    pL = p.seq_len[ppair / p.Hkv];
-    pnt = (min(kUnit, pL - pc * kUnit) + kTile - 1) / kTile;
+  // Unit queue: lane 0 keeps one request in flight.
+  unsigned pending = 0;
+  if (lane == 0) pending = atomicAdd(&p.queues[0], 1u);
+  auto take = [&]() -> int {
+    const int u = (int)__shfl_sync(0xffffffffu, pending, 0);
+    if (lane == 0 && u < total_units) pending = atomicAdd(&p.queues[0], 1u);
+    return u;
   };
-  p_load_unit();
+
+  // Producer: the unit being issued and its tile cursor.
+  int pu = take(), pt = 0, ppair = 0, pc = 0, pL = 0, pnt = 0;
+  int qh = 0, qt = 0;  // unit queue head (pushes) / tail (pops)
+  auto start_unit = [&]() {
+    unit_of(sm, p.B, p.Hkv, pu, ppair, pc);
+    pL = sm.len[ppair / p.Hkv];
+    pnt = (min(kUnit, pL - pc * kUnit) + kTile - 1) / kTile;
+    if (lane == 0) uq[qh % kQueue] = pu;
+    ++qh;
+  };
+  if (pu < total_units) start_unit();
   long issued = 0;
   auto issue = [&]() {  // copy the producer's current tile into the next slot
     const int key0 = pc * kUnit + pt * kTile;
@@ -275,22 +273,26 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
     ++issued;
     if (++pt == pnt) {
       pt = 0;
-      if (++pu < u_end) p_load_unit();
+      pu = take();
+      if (pu < total_units) start_unit();
     }
   };
-  for (int s = 0; s < kStages && pu < u_end; ++s) issue();
+  while (pu < total_units && issued < kStages) issue();
+  __syncwarp();
 
   const float scale = p.sm_scale;
   const int h0 = 2 * t, h1 = 2 * t + 1;
   uint32_t qf[NP][4];
   int qpair = -1;
   long consumed = 0;
-  for (int u = u_begin; u < u_end; ++u) {
+  while (qt < qh) {
+    const int u = uq[qt % kQueue];
+    ++qt;
     int pair, c;
     unit_of(sm, p.B, p.Hkv, u, pair, c);
     const int b = pair / p.Hkv;
     const int kvh = pair - b * p.Hkv;
-    const int L = p.seq_len[b];
+    const int L = sm.len[b];
     const int ntile = (min(kUnit, L - c * kUnit) + kTile - 1) / kTile;
     if (pair != qpair) {
       qpair = pair;
@@ -334,9 +336,10 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
       ++consumed;
       // The slot's data is consumed (the MMAs used it): refill it.
       __syncwarp();
-      if (pu < u_end) {
+      if (pu < total_units) {
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue();
+        __syncwarp();
       }
       const int key0 = c * kUnit + tt * kTile;
       const int j0 = key0 + g;
@@ -364,9 +367,13 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
       if (h0 < G) st[h0] = make_float2(m0, z0);
       if (h1 < G) st[h1] = make_float2(m1, z1);
     }
+    // Publish: this unit's scores and partial are visible before it counts.
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(&p.done[pair], 1u);
   }
   // Every issued copy has been waited for; retire the barriers before the
-  // buffer is reused by phase 2.
+  // buffer is reused by the select phase.
   __syncwarp();
   if (lane == 0)
     for (int s = 0; s < kStages; ++s)
@@ -375,7 +382,7 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
 }
 
 // ----------------------------------------------------------------------------
-// Phase 2: one slice (several 1024-key sub-chunks) of one pair per CTA.
+// Select: one slice (one or more sub-chunks of keys) of one pair per item.
 // ----------------------------------------------------------------------------
 template <int D, int G>
 __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int item) {
@@ -390,8 +397,23 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   const int kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int L = p.seq_len[b];
-  if (L < 1 || L > p.Nmax) return;  // reported in phase 1
+  const int L = sm.len[b];
+  if (L < 1 || L > p.Nmax) return;  // reported at kernel start
+
+  // Wait (bounded) until every unit of the pair has been scored.
+  if (threadIdx.x == 0) {
+    const unsigned want = (unsigned)sm.nunit[b];
+    unsigned spins = 0;
+    while (ld_acquire_u32(&p.done[pair]) < want) {
+      __nanosleep(32);
+      if (++spins > kSpinLimit) {
+        set_status(p.status, TOPT_ETIMEOUT);
+        break;
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
 
   // Softmax statistics of the whole row, per head of the group.
   const int nu = (L + kUnit - 1) / kUnit;
@@ -577,7 +599,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(&p.counter[pair], 1u);
+    const unsigned prev = atomicAdd(&p.ticket[pair], 1u);
     sm.last = (prev == (unsigned)p.ipp - 1u);
   }
   __syncthreads();
@@ -623,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
       const int b = lane * per + i;
       if (b < p.B) {
         const int L = p.seq_len[b];
+        sm.len[b] = L;
         int nu = 0;
         if (L >= 1 && L <= p.Nmax) nu = (L + kUnit - 1) / kUnit;
         else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
@@ -641,25 +664,29 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
       const int b = lane * per + i;
       if (b < p.B) {
         sm.ustart[b] = acc;
-        const int L = p.seq_len[b];
+        const int L = sm.len[b];
         if (L >= 1 && L <= p.Nmax) acc += ((L + kUnit - 1) / kUnit) * p.Hkv;
       }
     }
     if (lane == kWarp - 1) sm.ustart[p.B] = incl;
   }
-  const int pairs = p.B * p.Hkv;
-  for (int i = blockIdx.x * kThreads + threadIdx.x; i < pairs; i += gridDim.x * kThreads) p.counter[i] = 0u;
   __syncthreads();
 
   phase_scores<D, G>(p, sm, sm.ustart[p.B]);
-  grid_sync(p.barrier, p.status);
-  for (int item = blockIdx.x; item < pairs * p.ipp; item += gridDim.x) {
+  __syncthreads();
+
+  const int items = p.B * p.Hkv * p.ipp;
+  for (;;) {
+    if (threadIdx.x == 0) sm.item = (int)atomicAdd(&p.queues[1], 1u);
+    __syncthreads();
+    const int item = sm.item;
+    if (item >= items) break;
     phase_select<D, G>(p, sm, item);
     __syncthreads();
   }
 }
 
-// Co-resident CTAs of the cooperative grid, per device and instantiation.
+// Resident CTAs of the persistent grid, per device and instantiation.
 template <int D, int G>
 cudaError_t grid_of(int& grid) {
   static int cached[kMaxDevices] = {};
@@ -694,8 +721,8 @@ int items_per_pair(int grid, int pairs, int cache_len, int G) {
   return ipp;
 }
 
-// Upper bound of the cooperative grid on any supported GPU (for the
-// workspace query, which must not need a device).
+// Upper bound of the persistent grid on any supported GPU (for the workspace
+// query, which must not need a device).
 constexpr int kMaxGrid = 160 * 16;
 
 cudaError_t record(void* ev, cudaStream_t s) {
@@ -718,15 +745,15 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   p.part_r = reinterpret_cast<float*>(ws + l.part_r);
   p.part_kt = reinterpret_cast<int*>(ws + l.part_kt);
   p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
-  p.counter = reinterpret_cast<unsigned*>(ws + l.counter);
-  p.barrier = reinterpret_cast<unsigned*>(ws + l.barrier);
+  unsigned* counters = reinterpret_cast<unsigned*>(ws + l.counters);
+  p.queues = counters;
+  p.done = counters + 2;
+  p.ticket = counters + 2 + pairs;
   if ((e = record(a.events[0], s)) != cudaSuccess) return e;
-  // The grid barrier starts from zeroed words (the workspace may hold anything).
-  if ((e = cudaMemsetAsync(p.barrier, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
-  void* kargs[] = {&p};
-  e = cudaLaunchCooperativeKernel((const void*)decode_fused_kernel<D, G>, dim3(grid), dim3(kThreads), kargs,
-                                  sizeof(DecodeSmem<D, G>), s);
-  if (e != cudaSuccess) return e;
+  // Queues and counters start from zero (the workspace may hold anything).
+  if ((e = cudaMemsetAsync(counters, 0, l.counters_bytes, s)) != cudaSuccess) return e;
+  decode_fused_kernel<D, G><<<grid, kThreads, sizeof(DecodeSmem<D, G>), s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return record(a.events[1], s);
 }
 
@@ -746,6 +773,8 @@ cudaError_t launch_d(const DecodeParams& p, int G, const topt_decode_args& a, cu
 }
 
 }  // namespace
+
+int decode_max_batch() { return kMaxBatch; }
 
 size_t decode_workspace_bytes(const topt_decode_args& a) {
   const int pairs = a.batch * a.n_kv_heads;

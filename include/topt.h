@@ -68,7 +68,7 @@ typedef enum { TOPT_BF16 = 0, TOPT_F32 = 1 } topt_dtype;
 /* [TopTheta §2.2 "generative decoding", Fig. 1, §3.2, §4.6 (GQA)]          */
 /* ------------------------------------------------------------------------ */
 typedef struct {
-  int32_t batch;        /* B >= 1 */
+  int32_t batch;        /* B, 1 .. 256 */
   int32_t n_q_heads;    /* Hq */
   int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 8 */
   int32_t head_dim;     /* d: 64 or 128 */
