@@ -169,7 +169,7 @@ class DecodeState:
             self.kept.append(torch.empty((B, Hq), device=dev, dtype=torch.int32))
             self.vrows.append(torch.empty((B, Hkv), device=dev, dtype=torch.int32))
         a0 = self.args(0)
-        self.ws = torch.empty(topt.decode_workspace_bytes(a0), device=dev, dtype=torch.uint8)
+        self.ws = topt.decode_workspace(a0, dev)
         self.dargs = []
         self.vargs = []
         for l in range(layers):

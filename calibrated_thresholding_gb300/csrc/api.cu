@@ -29,6 +29,7 @@ topt_status check_decode_shape(const topt_decode_args* a) {
   if (a->n_q_heads % a->n_kv_heads != 0) return TOPT_ESHAPE;
   if (a->n_q_heads / a->n_kv_heads > 8) return TOPT_ESHAPE;
   if (a->batch > decode_max_batch()) return TOPT_ESHAPE;
+  if (a->batch * a->n_kv_heads > decode_max_pairs()) return TOPT_ESHAPE;
   return check_common_mode(a->mode, a->sdc);
 }
 
@@ -93,7 +94,6 @@ topt_status topt_decode(const topt_decode_args* a, topt_stream stream) {
   if (a->vmc && !a->mu) return TOPT_EINVAL;
   if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache)) return TOPT_EINVAL;
   if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
-  if ((size_t)a->batch * a->n_kv_heads > 65535u) return TOPT_ESHAPE;
   const size_t need = decode_workspace_bytes(*a);
   if (!a->workspace || a->workspace_bytes < need || (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
     return TOPT_EWORKSPACE;

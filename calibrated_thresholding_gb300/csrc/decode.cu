@@ -7,31 +7,37 @@
 // is one (sequence, KV head) and its G = Hq/Hkv query heads ([TopTheta §2.2,
 // GQA]).
 //
-// One persistent kernel per call (one CTA slot per SM resource, no grid-wide
+// One persistent kernel per call (as many CTAs as fit on the GPU, no grid-wide
 // barrier), fed by two atomic work queues:
 //
-//  Scores.  The valid keys of every pair are cut into 128-key units, handed to
-//   warps in pair order by an atomic counter (each warp asks one unit ahead,
-//   so the atomic's latency is hidden).  A warp streams its units' K rows
-//   through a private shared-memory ring with 1-D TMA bulk copies
-//   (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first, completion on an
+//  Scores.  Every pair's valid keys form 16-key tiles, numbered pair after
+//   pair.  Warps take runs of tiles from an atomic counter (guided: runs of up
+//   to 8 tiles shrink to 1 as the queue drains; each warp asks one run
+//   ahead, so the atomic's latency is hidden).  A warp streams its tiles'
+//   K rows through a private shared-memory ring with 1-D TMA bulk copies
+//   (cp.async.bulk, 4 KB per tile, L2 evict-first, completion on an
 //   mbarrier), computes each 16-key x G-head score block with m16n8k16 bf16
 //   MMAs (keys on the M side, query heads on the N side), writes
 //   a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4 bytes per
-//   key) and the unit's softmax partial (m, Z), then counts the unit as done
-//   for its pair.
-//  Select.  When a CTA's warps find the unit queue empty, the CTA takes
-//   (pair, slice) items in pair order from the second queue, waits (bounded)
-//   until the pair's units are all done, merges the (m, Z) partials, turns
-//   theta into a bound on the score (post-softmax: s >= theta <=>
-//   a >= m + ln theta + ln Z), ballots per-head masks of 32 keys per warp, ORs
-//   them into the group union, compacts the union into a shared list by
-//   popcount prefix, gathers only those V rows (16-byte loads) and accumulates
-//   sum exp(a - m) V per head.  The last CTA of a pair (atomic ticket, nothing
-//   waits) combines the slices and applies SDC [Eq. 4] and VMC [Eq. 5-7].
+//   key) and the tile's softmax partial (m, Z) per head, and counts finished
+//   tiles per pair.
+//  Select.  When a CTA's warps find the tile queue empty, the CTA takes
+//   (pair, slice) items in pair order from the second queue and waits
+//   (bounded) until all tiles of the pair are done.  It loads the slice's
+//   scores into registers in one go (8192 values per CTA) while it merges the
+//   pair's (m, Z) partials, turns theta into a bound on the score
+//   (post-softmax: s >= theta <=> a >= m + ln theta + ln Z), ballots per-head
+//   masks of 32 keys per warp, ORs them into the group union, compacts the
+//   union into a shared list by popcount prefix, gathers only those V rows
+//   (16-byte loads, 64 rows in flight per CTA) and accumulates
+//   sum exp(a - m) V per head.  The last slice of a pair to finish (atomic
+//   ticket, nothing waits) combines the slices and applies SDC [Eq. 4] and
+//   VMC [Eq. 5-7].
+//  Exit.  The last CTA to leave zeroes the queues and counters, so the
+//   workspace is ready for the next call without a memset.
 //
-// No wait can deadlock: a CTA only waits for units that warps already took,
-// and a unit is only taken by a running warp.  Every wait is bounded and
+// No wait can deadlock: a CTA only waits for tiles that warps already took,
+// and a tile is only taken by a running warp.  Every wait is bounded and
 // reports TOPT_ETIMEOUT instead of hanging.
 #include "common.cuh"
 #include "internal.h"
@@ -41,19 +47,19 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
-constexpr int kTile = 16;                          // keys per MMA tile / per bulk copy
-constexpr int kUnit = 128;                         // keys per work unit and softmax partial
+constexpr int kTile = 16;                          // keys per MMA tile / bulk copy
 constexpr int kStages = 4;                         // ring slots per warp
-constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
+constexpr int kQueue = 8;                          // per-warp queue of taken runs (>= kStages + 1)
+constexpr int kMaxRun = 8;                         // tiles per run while the queue is long
 constexpr int kGatherUnroll = 8;                   // V rows in flight per thread slot
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDevices = 64;
 constexpr unsigned kSpinLimit = 1u << 24;          // bounded waits: x >= 32 ns sleep
 
-// Keys per select sub-chunk (the union list's capacity): smaller for large
-// groups so a warp's staged scores stay in registers.
+// Keys per select slice: the CTA holds the slice's G x keys scores in
+// registers, at most 64 per thread and 32 groups of 32 keys per warp.
 template <int G>
-__host__ __device__ constexpr int sub_keys() { return G > 4 ? 512 : 1024; }
+__host__ __device__ constexpr int slice_keys() { return kThreads * (64 / G < 32 ? 64 / G : 32); }
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -69,38 +75,44 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  int mask_words, upp, ipp;
+  int mask_words, tpp, ipp, lstride;
   // workspace
-  float* logits;      // [pairs][G][Nmax]
-  float2* stats;      // [pairs][upp][G]
+  float* logits;      // [pairs][G][lstride]
+  float2* stats;      // [pairs][tpp][G]
   float* part_num;    // [pairs][ipp][G][D]
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
   int* part_nu;       // [pairs][ipp]
-  unsigned* queues;   // [2]: next unit, next select item       } zeroed before
-  unsigned* done;     // [pairs]: units finished                } every launch
-  unsigned* ticket;   // [pairs]: select slices finished        }
+  unsigned* queues;   // [3]: next tile, next select item, CTAs finished   } zero between
+  unsigned* done;     // [pairs]: tiles scored                              } calls (the last
+  unsigned* ticket;   // [pairs]: select slices finished                    } CTA resets them)
 };
 
+// The workspace starts with a fixed-size block of counters, so a workspace
+// reused across shapes keeps them in one place: zero before the first call,
+// and every call leaves the ones it used at zero again.
+constexpr size_t kCounterBytes = 128 * 1024;
+constexpr int kMaxPairs = (int)(kCounterBytes / sizeof(unsigned) - 4) / 2;
+
 struct DecodeLayout {
-  size_t logits, stats, part_num, part_r, part_kt, part_nu, counters, counters_bytes, total;
+  size_t counters, logits, stats, part_num, part_r, part_kt, part_nu, total;
 };
+
+int logit_stride(int cache_len) { return (cache_len + 31) / 32 * 32; }
 
 DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
   const size_t pairs = (size_t)a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t upp = (a.cache_len + kUnit - 1) / kUnit;
+  const size_t tpp = (a.cache_len + kTile - 1) / kTile;
   DecodeLayout l;
   size_t off = 0;
-  l.logits = off;   off += align256(pairs * G * (size_t)a.cache_len * sizeof(float));
-  l.stats = off;    off += align256(pairs * upp * G * sizeof(float2));
+  l.counters = off; off += kCounterBytes;
+  l.logits = off;   off += align256(pairs * G * (size_t)logit_stride(a.cache_len) * sizeof(float));
+  l.stats = off;    off += align256(pairs * tpp * G * sizeof(float2));
   l.part_num = off; off += align256(pairs * ipp * G * (size_t)a.head_dim * sizeof(float));
   l.part_r = off;   off += align256(pairs * ipp * G * sizeof(float));
   l.part_kt = off;  off += align256(pairs * ipp * G * sizeof(int));
   l.part_nu = off;  off += align256(pairs * ipp * sizeof(int));
-  l.counters = off;
-  l.counters_bytes = align256((2 + 2 * pairs) * sizeof(unsigned));
-  off += l.counters_bytes;
   l.total = off;
   return l;
 }
@@ -150,39 +162,31 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Online (max, sum) update with two new scores (either may be -inf).
-__device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) {
-  const float mt = fmaxf(x0, x1);
-  if (mt == -CUDART_INF_F) return;
-  const float mn = fmaxf(m, mt);
-  z = z * __expf(m - mn) + __expf(x0 - mn) + __expf(x1 - mn);
-  m = mn;
-}
-
 // ----------------------------------------------------------------------------
 // Shared memory: the score rings and the select lists share one buffer.
 // ----------------------------------------------------------------------------
 template <int D>
 struct Ring {
   uint64_t bar[kWarps][kStages];
-  int uq[kWarps][kQueue];  // units taken by each warp, in order
+  int2 rq[kWarps][kQueue];  // runs of tiles taken by each warp, in order
   __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
 };
 
 template <int D, int G>
 struct Lists {
-  int j[sub_keys<G>()];       // union keys of the sub-chunk, in key order
-  float w[sub_keys<G>()][G];  // exp(a - m) per head (0 if the head drops the key)
+  int j[slice_keys<G>()];       // union keys of the slice
+  float w[slice_keys<G>()][G];  // exp(a - m) per head (0 if the head drops the key)
   float acc[kWarps][G][D];
   float r[kWarps][G];
   int kt[kWarps][G];
   int cnt[kWarps];
+  float m[kWarps][G], z[kWarps][G];
 };
 
 template <int D, int G>
 struct DecodeSmem {
-  int ustart[kMaxBatch + 1];  // first unit of each sequence
-  int nunit[kMaxBatch];       // units per KV head of each sequence
+  int tstart[kMaxBatch + 1];  // first tile of each sequence
+  int ntile[kMaxBatch];       // tiles per KV head of each sequence
   int len[kMaxBatch];         // seq_len, staged once per CTA
   float M[G], Z[G], T[G], th[G];
   int item;
@@ -193,21 +197,28 @@ struct DecodeSmem {
   } u;
 };
 
-// Unit index -> (pair, unit within the pair).
+struct TileRef {
+  int pair, b, kvh, tile, L;
+};
+
+// Global tile index -> (pair, tile within the pair).
 template <int D, int G>
-__device__ __forceinline__ void unit_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int u, int& pair, int& c) {
-  int lo = 0, hi = B - 1;  // last b with ustart[b] <= u
+__device__ __forceinline__ TileRef tile_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int tau) {
+  int lo = 0, hi = B - 1;  // last b with tstart[b] <= tau
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (sm.ustart[mid] <= u) lo = mid;
+    if (sm.tstart[mid] <= tau) lo = mid;
     else hi = mid - 1;
   }
-  const int b = lo;
-  const int nu = sm.nunit[b];
-  const int r = u - sm.ustart[b];
-  const int kvh = r / nu;
-  pair = b * Hkv + kvh;
-  c = r - kvh * nu;
+  TileRef r;
+  r.b = lo;
+  const int nt = sm.ntile[lo];
+  const int rem = tau - sm.tstart[lo];
+  r.kvh = rem / nt;
+  r.tile = rem - r.kvh * nt;
+  r.pair = lo * Hkv + r.kvh;
+  r.L = sm.len[lo];
+  return r;
 }
 
 // ----------------------------------------------------------------------------
@@ -222,16 +233,17 @@ __device__ __forceinline__ void unit_of(const DecodeSmem<D, G>& sm, int B, int H
 // 2t, 2t+1) and (key g+8, heads 2t, 2t+1).
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total_units) {
+__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total) {
   constexpr int NP = D / 32;
   constexpr unsigned kTileBytes = kTile * D * 2;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
+  const int workers = gridDim.x * kWarps;
 
   uint64_t* bars = sm.u.ring.bar[warp];
-  int* uq = sm.u.ring.uq[warp];
+  int2* rq = sm.u.ring.rq[warp];
   unsigned char* slots = &sm.u.ring.slot[warp][0][0];
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep_pol = l2_evict_last_policy();
@@ -241,76 +253,92 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   }
   __syncwarp();
 
-  // Unit queue: lane 0 keeps one request in flight.
-  unsigned pending = 0;
-  if (lane == 0) pending = atomicAdd(&p.queues[0], 1u);
-  auto take = [&]() -> int {
-    const int u = (int)__shfl_sync(0xffffffffu, pending, 0);
-    if (lane == 0 && u < total_units) pending = atomicAdd(&p.queues[0], 1u);
-    return u;
+  // Tile queue: lane 0 keeps one request in flight; run length shrinks as
+  // the queue drains (guided self-scheduling).
+  unsigned pend_start = 0, pend_len = 0;
+  auto request = [&](unsigned seen) {
+    if (lane == 0) {
+      const unsigned left = seen < (unsigned)total ? (unsigned)total - seen : 0u;
+      unsigned n = left / (2u * (unsigned)workers);
+      n = n < 1u ? 1u : (n > (unsigned)kMaxRun ? (unsigned)kMaxRun : n);
+      pend_len = n;
+      pend_start = atomicAdd(&p.queues[0], n);
+    }
+  };
+  request(0);
+  auto take = [&](int& s, int& e) {
+    s = (int)__shfl_sync(0xffffffffu, pend_start, 0);
+    const int n = (int)__shfl_sync(0xffffffffu, pend_len, 0);
+    e = min(s + n, total);
+    if (s < total) request((unsigned)s + n);
   };
 
-  // Producer: the unit being issued and its tile cursor.
-  int pu = take(), pt = 0, ppair = 0, pc = 0, pL = 0, pnt = 0;
-  int qh = 0, qt = 0;  // unit queue head (pushes) / tail (pops)
-  auto start_unit = [&]() {
-    unit_of(sm, p.B, p.Hkv, pu, ppair, pc);
-    pL = sm.len[ppair / p.Hkv];
-    pnt = (min(kUnit, pL - pc * kUnit) + kTile - 1) / kTile;
-    if (lane == 0) uq[qh % kQueue] = pu;
+  // Producer: the run being issued.
+  int ps = 0, pe = 0, qh = 0, qt = 0;
+  take(ps, pe);
+  if (ps < total) {
+    if (lane == 0) rq[qh % kQueue] = make_int2(ps, pe);
     ++qh;
-  };
-  if (pu < total_units) start_unit();
+  }
   long issued = 0;
-  auto issue = [&]() {  // copy the producer's current tile into the next slot
-    const int key0 = pc * kUnit + pt * kTile;
-    const unsigned bytes = (unsigned)min(kTile, pL - key0) * D * 2;
+  auto issue = [&]() {  // copy tile ps into the next slot
+    const TileRef r = tile_of(sm, p.B, p.Hkv, ps);
+    const int key0 = r.tile * kTile;
+    const unsigned bytes = (unsigned)min(kTile, r.L - key0) * D * 2;
     const int s = (int)(issued % kStages);
     if (lane == 0) {
       mbar_expect_tx(&bars[s], bytes);
-      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)ppair * p.Nmax + key0) * D, bytes, &bars[s], pol);
+      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)r.pair * p.Nmax + key0) * D, bytes, &bars[s], pol);
     }
     ++issued;
-    if (++pt == pnt) {
-      pt = 0;
-      pu = take();
-      if (pu < total_units) start_unit();
+    if (++ps == pe) {
+      take(ps, pe);
+      if (ps < total) {
+        if (lane == 0) rq[qh % kQueue] = make_int2(ps, pe);
+        ++qh;
+      }
     }
   };
-  while (pu < total_units && issued < kStages) issue();
+  while (ps < total && issued < kStages) issue();
   __syncwarp();
 
   const float scale = p.sm_scale;
   const int h0 = 2 * t, h1 = 2 * t + 1;
   uint32_t qf[NP][4];
   int qpair = -1;
+  int run_pair = -1, run_cnt = 0;
   long consumed = 0;
-  while (qt < qh) {
-    const int u = uq[qt % kQueue];
-    ++qt;
-    int pair, c;
-    unit_of(sm, p.B, p.Hkv, u, pair, c);
-    const int b = pair / p.Hkv;
-    const int kvh = pair - b * p.Hkv;
-    const int L = sm.len[b];
-    const int ntile = (min(kUnit, L - c * kUnit) + kTile - 1) / kTile;
-    if (pair != qpair) {
-      qpair = pair;
-      if (g < G) {
-        const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + kvh * G + g) * D;
-#pragma unroll
-        for (int pp = 0; pp < NP; ++pp) {
-          const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
-          qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
-        }
-      } else {
-#pragma unroll
-        for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
-      }
+  auto publish = [&]() {  // this warp's scores of run_pair are visible, then counted
+    if (run_cnt > 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(&p.done[run_pair], (unsigned)run_cnt);
+      run_cnt = 0;
     }
-    float* lbase = p.logits + (size_t)pair * G * p.Nmax;
-    float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
-    for (int tt = 0; tt < ntile; ++tt) {
+  };
+  while (qt < qh) {
+    const int2 run = rq[qt % kQueue];
+    ++qt;
+    for (int tau = run.x; tau < run.y; ++tau) {
+      const TileRef r = tile_of(sm, p.B, p.Hkv, tau);
+      if (r.pair != run_pair) {
+        publish();
+        run_pair = r.pair;
+      }
+      if (r.pair != qpair) {
+        qpair = r.pair;
+        if (g < G) {
+          const __nv_bfloat16* qrow = p.q + ((size_t)r.b * p.Hq + r.kvh * G + g) * D;
+#pragma unroll
+          for (int pp = 0; pp < NP; ++pp) {
+            const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
+            qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
+          }
+        } else {
+#pragma unroll
+          for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
+        }
+      }
       const int s = (int)(consumed % kStages);
       const unsigned parity = (unsigned)((consumed / kStages) & 1);
       if (!mbar_wait(&bars[s], parity)) set_status(p.status, TOPT_ETIMEOUT);
@@ -336,41 +364,48 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
       ++consumed;
       // The slot's data is consumed (the MMAs used it): refill it.
       __syncwarp();
-      if (pu < total_units) {
+      if (ps < total) {
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue();
         __syncwarp();
       }
-      const int key0 = c * kUnit + tt * kTile;
+      const int key0 = r.tile * kTile;
       const int j0 = key0 + g;
       const int j1 = key0 + g + 8;
+      const int L = r.L;
       const float a00 = j0 < L ? cc[0] * scale : -CUDART_INF_F;
       const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
       const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
       const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
+      float* lrow = p.logits + (size_t)r.pair * G * p.lstride;
+      // Per-tile softmax partial of each head: max, then sum over the 16 keys.
+      float m0 = fmaxf(a00, a10), m1 = fmaxf(a01, a11);
+#pragma unroll
+      for (int off = 4; off < kWarp; off <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+      }
+      float z0 = __expf(a00 - m0) + __expf(a10 - m0);
+      float z1 = __expf(a01 - m1) + __expf(a11 - m1);
+#pragma unroll
+      for (int off = 4; off < kWarp; off <<= 1) {
+        z0 += __shfl_xor_sync(0xffffffffu, z0, off);
+        z1 += __shfl_xor_sync(0xffffffffu, z1, off);
+      }
+      float2* st = p.stats + ((size_t)r.pair * p.tpp + r.tile) * G;
       if (h0 < G) {
-        if (j0 < L) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j0, a00, keep_pol);
-        if (j1 < L) st_hint_f32(lbase + (size_t)h0 * p.Nmax + j1, a10, keep_pol);
-        ms_add2(m0, z0, a00, a10);
+        if (j0 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j0, a00, keep_pol);
+        if (j1 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j1, a10, keep_pol);
+        if (g == 0) st[h0] = make_float2(m0, z0);
       }
       if (h1 < G) {
-        if (j0 < L) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j0, a01, keep_pol);
-        if (j1 < L) st_hint_f32(lbase + (size_t)h1 * p.Nmax + j1, a11, keep_pol);
-        ms_add2(m1, z1, a01, a11);
+        if (j0 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j0, a01, keep_pol);
+        if (j1 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j1, a11, keep_pol);
+        if (g == 0) st[h1] = make_float2(m1, z1);
       }
+      ++run_cnt;
     }
-    // Partial of this unit: merge over the 8 key rows (lane bits 2..4).
-    ms_warp_merge(m0, z0, 4);
-    ms_warp_merge(m1, z1, 4);
-    if (g == 0) {
-      float2* st = p.stats + ((size_t)pair * p.upp + c) * G;
-      if (h0 < G) st[h0] = make_float2(m0, z0);
-      if (h1 < G) st[h1] = make_float2(m1, z1);
-    }
-    // Publish: this unit's scores and partial are visible before it counts.
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) atomicAdd(&p.done[pair], 1u);
+    publish();
   }
   // Every issued copy has been waited for; retire the barriers before the
   // buffer is reused by the select phase.
@@ -382,14 +417,14 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
 }
 
 // ----------------------------------------------------------------------------
-// Select: one slice (one or more sub-chunks of keys) of one pair per item.
+// Select: one slice of one pair per item.
 // ----------------------------------------------------------------------------
 template <int D, int G>
 __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int item) {
   constexpr int LPR = D / 8;              // lanes per V row (16 bytes each)
   constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
-  constexpr int kSub = sub_keys<G>();
-  constexpr int kGroupsPerWarp = kSub / (kWarps * kWarp);
+  constexpr int SK = slice_keys<G>();
+  constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
   Lists<D, G>& ls = sm.u.lists;
   const int pair = item / p.ipp;
   const int slice = item - pair * p.ipp;
@@ -399,12 +434,12 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   const int lane = threadIdx.x & 31;
   const int L = sm.len[b];
   if (L < 1 || L > p.Nmax) return;  // reported at kernel start
+  const int nt = sm.ntile[b];
 
-  // Wait (bounded) until every unit of the pair has been scored.
+  // Wait (bounded) until every tile of the pair has been scored.
   if (threadIdx.x == 0) {
-    const unsigned want = (unsigned)sm.nunit[b];
     unsigned spins = 0;
-    while (ld_acquire_u32(&p.done[pair]) < want) {
+    while (ld_acquire_u32(&p.done[pair]) < (unsigned)nt) {
       __nanosleep(32);
       if (++spins > kSpinLimit) {
         set_status(p.status, TOPT_ETIMEOUT);
@@ -415,133 +450,135 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   }
   __syncthreads();
 
-  // Softmax statistics of the whole row, per head of the group.
-  const int nu = (L + kUnit - 1) / kUnit;
-  for (int h = warp; h < G; h += kWarps) {
-    float m = -CUDART_INF_F, z = 0.f;
-    for (int c = lane; c < nu; c += kWarp) {
-      const float2 v = __ldcg(p.stats + ((size_t)pair * p.upp + c) * G + h);
-      ms_merge(m, z, v.x, v.y);
-    }
-    ms_warp_merge(m, z, 1);
-    if (lane == 0) {
-      const float th = p.theta[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)];
-      sm.M[h] = m;
-      sm.Z[h] = z;
-      sm.th[h] = th;
-      sm.T[h] = score_bound(p.mode, th, m, z);
-    }
-  }
-  __syncthreads();
-
-  // This slice's sub-chunks; mask words past L are spread over the slices.
-  const int nsub = (L + kSub - 1) / kSub;
-  const int s_begin = (int)((long)nsub * slice / p.ipp);
-  const int s_end = (int)((long)nsub * (slice + 1) / p.ipp);
-  uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
-  if (mrow) {
-    const int w0 = (L + 31) >> 5;
-    const int span = p.mask_words - w0;
-    const int lo = w0 + (int)((long)span * slice / p.ipp);
-    const int hi = w0 + (int)((long)span * (slice + 1) / p.ipp);
-    for (int i = threadIdx.x; i < (hi - lo) * G; i += kThreads) {
-      const int h = i % G;
-      const int w = lo + i / G;
-      mrow[(size_t)h * p.mask_words + w] = 0u;
-    }
-  }
-
-  const float* lbase = p.logits + (size_t)pair * G * p.Nmax;
+  // The slice's scores, all loads in flight at once: group gi of warp w is
+  // keys s0 + gi*128 + w*32 + lane.
+  const int s0 = slice * SK;
+  const float* lrow = p.logits + (size_t)pair * G * p.lstride;
   const uint64_t pol = l2_evict_first_policy();
-  const int slot = threadIdx.x / LPR;
-  const int dl = threadIdx.x % LPR;
-  const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * 8;
-  float T[G], M[G], Rl[G], acc[G][8];
+  float wv[NGRP][G];
+#pragma unroll
+  for (int gi = 0; gi < NGRP; ++gi) {
+    const int j = s0 + gi * kThreads + warp * kWarp + lane;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      wv[gi][h] = j < L ? ld_cg_hint_f32(lrow + (size_t)h * p.lstride + j, pol) : -CUDART_INF_F;
+  }
+
+  // Softmax statistics of the whole row, per head, from the tile partials.
+  {
+    float m[G], z[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -CUDART_INF_F;
+      z[h] = 0.f;
+    }
+    for (int c = threadIdx.x; c < nt; c += kThreads) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float2 v = __ldcg(p.stats + ((size_t)pair * p.tpp + c) * G + h);
+        ms_merge(m[h], z[h], v.x, v.y);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      ms_warp_merge(m[h], z[h], 1);
+      if (lane == 0) {
+        ls.m[warp][h] = m[h];
+        ls.z[warp][h] = z[h];
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+      const int h = threadIdx.x;
+      float mm = -CUDART_INF_F, zz = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) ms_merge(mm, zz, ls.m[w][h], ls.z[w][h]);
+      const float th = p.theta[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)];
+      sm.M[h] = mm;
+      sm.Z[h] = zz;
+      sm.th[h] = th;
+      sm.T[h] = score_bound(p.mode, th, mm, zz);
+    }
+    __syncthreads();
+  }
+
+  // Thresholds, masks and the union of the group.
+  uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
+  float Rl[G];
   int kt[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    T[h] = sm.T[h];
-    M[h] = sm.M[h];
     Rl[h] = 0.f;
     kt[h] = 0;
+  }
+  unsigned uni[NGRP];
+  int wcount = 0;
+#pragma unroll
+  for (int gi = 0; gi < NGRP; ++gi) {
+    const int j0 = s0 + gi * kThreads + warp * kWarp;
+    const bool valid = j0 + lane < L;
+    unsigned un = 0u;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float a = wv[gi][h];
+      const bool keep = valid && (a >= sm.T[h]);
+      wv[gi][h] = keep ? __expf(a - sm.M[h]) : 0.f;
+      Rl[h] += wv[gi][h];
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      kt[h] += __popc(bal);
+      un |= bal;
+      if (mrow && lane == 0 && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+    }
+    uni[gi] = un;
+    wcount += __popc(un);
+  }
+  if (lane == 0) ls.cnt[warp] = wcount;
+  __syncthreads();
+  int base = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    base += (w < warp) ? ls.cnt[w] : 0;
+    total += ls.cnt[w];
+  }
+#pragma unroll
+  for (int gi = 0; gi < NGRP; ++gi) {
+    if ((uni[gi] >> lane) & 1u) {
+      const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
+      ls.j[pos] = s0 + gi * kThreads + warp * kWarp + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h) ls.w[pos][h] = wv[gi][h];
+    }
+    base += __popc(uni[gi]);
+  }
+  __syncthreads();
+
+  // Gather the union's V rows.
+  const int slot = threadIdx.x / LPR;
+  const int dl = threadIdx.x % LPR;
+  const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * 8;
+  float acc[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-  }
-  int nsel_total = 0;
-
-  for (int sc = s_begin; sc < s_end; ++sc) {
-    const int c_begin = sc * kSub;
-    const int c_end = min(c_begin + kSub, L);
-    const int w_begin = c_begin + warp * kGroupsPerWarp * kWarp;
-    float wv[kGroupsPerWarp][G];
+  for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
+    uint4 vv[kGatherUnroll];
 #pragma unroll
-    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-      const int j = w_begin + gi * kWarp + lane;
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        wv[gi][h] = j < c_end ? ld_cg_hint_f32(lbase + (size_t)h * p.Nmax + j, pol) : -CUDART_INF_F;
-    }
-    unsigned uni[kGroupsPerWarp];
-    int wcount = 0;
-#pragma unroll
-    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-      const int j0 = w_begin + gi * kWarp;
-      const bool valid = j0 + lane < c_end;
-      unsigned un = 0u;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float a = wv[gi][h];
-        const bool keep = valid && (a >= T[h]);
-        wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
-        Rl[h] += wv[gi][h];
-        const unsigned bal = __ballot_sync(0xffffffffu, keep);
-        kt[h] += __popc(bal);
-        un |= bal;
-        if (mrow && lane == 0 && j0 < c_end) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
-      }
-      uni[gi] = un;
-      wcount += __popc(un);
-    }
-    __syncthreads();  // previous sub-chunk's list is consumed
-    if (lane == 0) ls.cnt[warp] = wcount;
-    __syncthreads();
-    int base = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      base += (w < warp) ? ls.cnt[w] : 0;
-      total += ls.cnt[w];
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int r = r0 + u * SLOTS + slot;
+      if (r < total) vv[u] = ld_nc16(vbase + (size_t)ls.j[r] * D);
     }
 #pragma unroll
-    for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
-      if ((uni[gi] >> lane) & 1u) {
-        const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
-        ls.j[pos] = w_begin + gi * kWarp + lane;
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      const int r = r0 + u * SLOTS + slot;
+      if (r < total) {
+        const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
+                             bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
 #pragma unroll
-        for (int h = 0; h < G; ++h) ls.w[pos][h] = wv[gi][h];
-      }
-      base += __popc(uni[gi]);
-    }
-    __syncthreads();
-    nsel_total += total;
-    for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
-      uint4 vv[kGatherUnroll];
+        for (int h = 0; h < G; ++h) {
+          const float wh = ls.w[r][h];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int r = r0 + u * SLOTS + slot;
-        if (r < total) vv[u] = ld_nc16(vbase + (size_t)ls.j[r] * D);
-      }
-#pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int r = r0 + u * SLOTS + slot;
-        if (r < total) {
-          const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
-                               bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float wh = ls.w[r][h];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
-          }
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
         }
       }
     }
@@ -557,7 +594,6 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
     }
     Rl[h] = warp_sum(Rl[h]);
   }
-  __syncthreads();  // the list is no longer read
   if (lane < LPR) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -574,7 +610,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   __syncthreads();
 
   const size_t pc = (size_t)pair * p.ipp + slice;
-  if (nsel_total > 0) {
+  if (total > 0) {
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
       float s = 0.f;
 #pragma unroll
@@ -593,9 +629,9 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
     p.part_r[pc * G + threadIdx.x] = r;
     p.part_kt[pc * G + threadIdx.x] = k;
   }
-  if (threadIdx.x == 0) p.part_nu[pc] = nsel_total;
+  if (threadIdx.x == 0) p.part_nu[pc] = total;
 
-  // The last CTA of the pair to arrive combines (nothing waits).
+  // The last slice of the pair to arrive combines (nothing waits).
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -636,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw);
 
-  // Units per sequence (every KV head of a sequence has the same length).
+  // Tiles per sequence (every KV head of a sequence has the same length).
   if (threadIdx.x < kWarp) {
     const int lane = threadIdx.x;
     const int per = (p.B + kWarp - 1) / kWarp;
@@ -646,11 +682,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
       if (b < p.B) {
         const int L = p.seq_len[b];
         sm.len[b] = L;
-        int nu = 0;
-        if (L >= 1 && L <= p.Nmax) nu = (L + kUnit - 1) / kUnit;
+        int nt = 0;
+        if (L >= 1 && L <= p.Nmax) nt = (L + kTile - 1) / kTile;
         else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
-        sm.nunit[b] = nu > 0 ? nu : 1;
-        run += nu * p.Hkv;
+        sm.ntile[b] = nt > 0 ? nt : 1;
+        run += nt * p.Hkv;
       }
     }
     int incl = run;
@@ -663,18 +699,19 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
     for (int i = 0; i < per; ++i) {
       const int b = lane * per + i;
       if (b < p.B) {
-        sm.ustart[b] = acc;
+        sm.tstart[b] = acc;
         const int L = sm.len[b];
-        if (L >= 1 && L <= p.Nmax) acc += ((L + kUnit - 1) / kUnit) * p.Hkv;
+        if (L >= 1 && L <= p.Nmax) acc += ((L + kTile - 1) / kTile) * p.Hkv;
       }
     }
-    if (lane == kWarp - 1) sm.ustart[p.B] = incl;
+    if (lane == kWarp - 1) sm.tstart[p.B] = incl;
   }
   __syncthreads();
 
-  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
+  phase_scores<D, G>(p, sm, sm.tstart[p.B]);
   __syncthreads();
 
+  // Select slices past a sequence's length only zero their mask words.
   const int items = p.B * p.Hkv * p.ipp;
   for (;;) {
     if (threadIdx.x == 0) sm.item = (int)atomicAdd(&p.queues[1], 1u);
@@ -683,6 +720,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
     if (item >= items) break;
     phase_select<D, G>(p, sm, item);
     __syncthreads();
+  }
+
+  // The last CTA out leaves the queues and counters zeroed for the next call.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sm.last = (atomicAdd(&p.queues[2], 1u) == gridDim.x - 1u);
+  __syncthreads();
+  if (sm.last) {
+    __threadfence();
+    const int pairs = p.B * p.Hkv;
+    for (int i = threadIdx.x; i < pairs; i += kThreads) {
+      p.done[i] = 0u;
+      p.ticket[i] = 0u;
+    }
+    if (threadIdx.x == 0) {
+      p.queues[0] = 0u;
+      p.queues[1] = 0u;
+      p.queues[2] = 0u;
+    }
   }
 }
 
@@ -711,19 +767,20 @@ cudaError_t grid_of(int& grid) {
   return cudaSuccess;
 }
 
-// Select slices per pair: enough to give every CTA about one slice.
-int items_per_pair(int grid, int pairs, int cache_len, int G) {
-  const int sub = G > 4 ? sub_keys<8>() : sub_keys<4>();
-  const int nsub = (cache_len + sub - 1) / sub;
-  int ipp = grid / pairs;
-  if (ipp < 1) ipp = 1;
-  if (ipp > nsub) ipp = nsub;
-  return ipp;
+int slices_per_pair(int cache_len, int G) {
+  int sk = 0;
+  switch (G) {
+    case 1: sk = slice_keys<1>(); break;
+    case 2: sk = slice_keys<2>(); break;
+    case 3: sk = slice_keys<3>(); break;
+    case 4: sk = slice_keys<4>(); break;
+    case 5: sk = slice_keys<5>(); break;
+    case 6: sk = slice_keys<6>(); break;
+    case 7: sk = slice_keys<7>(); break;
+    default: sk = slice_keys<8>(); break;
+  }
+  return (cache_len + sk - 1) / sk;
 }
-
-// Upper bound of the persistent grid on any supported GPU (for the workspace
-// query, which must not need a device).
-constexpr int kMaxGrid = 160 * 16;
 
 cudaError_t record(void* ev, cudaStream_t s) {
   return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
@@ -735,7 +792,7 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   cudaError_t e;
   if ((e = grid_of<D, G>(grid)) != cudaSuccess) return e;
   const int pairs = p.B * p.Hkv;
-  p.ipp = items_per_pair(grid, pairs, p.Nmax, G);
+  p.ipp = slices_per_pair(p.Nmax, G);
   const DecodeLayout l = decode_layout(a, p.ipp);
   if (a.workspace_bytes < l.total) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.workspace);
@@ -747,11 +804,9 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
   unsigned* counters = reinterpret_cast<unsigned*>(ws + l.counters);
   p.queues = counters;
-  p.done = counters + 2;
-  p.ticket = counters + 2 + pairs;
+  p.done = counters + 4;
+  p.ticket = counters + 4 + pairs;
   if ((e = record(a.events[0], s)) != cudaSuccess) return e;
-  // Queues and counters start from zero (the workspace may hold anything).
-  if ((e = cudaMemsetAsync(counters, 0, l.counters_bytes, s)) != cudaSuccess) return e;
   decode_fused_kernel<D, G><<<grid, kThreads, sizeof(DecodeSmem<D, G>), s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return record(a.events[1], s);
@@ -775,15 +830,15 @@ cudaError_t launch_d(const DecodeParams& p, int G, const topt_decode_args& a, cu
 }  // namespace
 
 int decode_max_batch() { return kMaxBatch; }
+int decode_max_pairs() { return kMaxPairs; }
 
 size_t decode_workspace_bytes(const topt_decode_args& a) {
-  const int pairs = a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
-  return decode_layout(a, items_per_pair(kMaxGrid, pairs, a.cache_len, G)).total;
+  return decode_layout(a, slices_per_pair(a.cache_len, G)).total;
 }
 
 cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
-  if (a.batch > kMaxBatch) return cudaErrorInvalidValue;
+  if (a.batch > kMaxBatch || a.batch * a.n_kv_heads > kMaxPairs) return cudaErrorInvalidValue;
   DecodeParams p;
   p.B = a.batch;
   p.Hq = a.n_q_heads;
@@ -807,7 +862,8 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.status = a.status;
   p.mask_words = (a.cache_len + 31) / 32;
-  p.upp = (a.cache_len + kUnit - 1) / kUnit;
+  p.tpp = (a.cache_len + kTile - 1) / kTile;
+  p.lstride = logit_stride(a.cache_len);
   p.ipp = 1;
   const int G = a.n_q_heads / a.n_kv_heads;
   if (a.head_dim == 128) return launch_d<128>(p, G, a, s);

@@ -175,6 +175,11 @@ def decode_workspace_bytes(a: DecodeArgs) -> int:
     return n.value
 
 
+def decode_workspace(a: DecodeArgs, device) -> torch.Tensor:
+    """A zero-filled workspace for topt_decode (its counters start at zero)."""
+    return torch.zeros(decode_workspace_bytes(a), device=device, dtype=torch.uint8)
+
+
 def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
            gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
            workspace=None, stream=None):
@@ -195,7 +200,7 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
     a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
                     gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status)
     if workspace is None:
-        workspace = torch.empty(decode_workspace_bytes(a), device=dev, dtype=torch.uint8)
+        workspace = decode_workspace(a, dev)
     a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
     a.workspace_bytes = workspace.numel()
     _check("topt_decode", lib().topt_decode(ctypes.byref(a), _stream(stream)))

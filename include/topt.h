@@ -70,7 +70,7 @@ typedef enum { TOPT_BF16 = 0, TOPT_F32 = 1 } topt_dtype;
 typedef struct {
   int32_t batch;        /* B, 1 .. 256 */
   int32_t n_q_heads;    /* Hq */
-  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 8 */
+  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 8, B * Hkv <= 16382 */
   int32_t head_dim;     /* d: 64 or 128 */
   int32_t cache_len;    /* Nmax >= 1: token capacity of each cache */
   int32_t theta_len;    /* Lmax >= 1: entries per head of `theta` */
@@ -89,7 +89,11 @@ typedef struct {
   int32_t* vrows;       /* [B][Hkv] V rows read (union over the group), or NULL */
   uint32_t* mask;       /* [B][Hq][ceil(Nmax/32)] kept bitmap (bit j%32 of word j/32), or NULL */
   int32_t* status;      /* device-side error word, or NULL */
-  void* workspace;      /* scratch, >= topt_decode_workspace() bytes, 256-byte aligned */
+  /* Scratch, >= topt_decode_workspace() bytes, 256-byte aligned.  Its first
+   * 128 KiB hold work counters that must be zero before the first call; every
+   * call that runs to completion leaves them zero again, so one zero-filled
+   * workspace serves any number of calls and shapes. */
+  void* workspace;
   size_t workspace_bytes;
   /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
    * `stream` right before [0] and right after [1] the decode kernel, so a

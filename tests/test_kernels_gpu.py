@@ -178,7 +178,7 @@ def test_decode_reuses_workspace():
     seq_len = torch.tensor([2048, 1500], device="cuda", dtype=torch.int32)
     theta, _ = calibrate_prefill_rows(52, 2, Hq, Hkv, d, 512, 32, ref.POST, Nmax)
     args = topt.decode_args(q, K, V, seq_len, theta, mode=ref.POST)
-    ws = torch.empty(topt.decode_workspace_bytes(args), device="cuda", dtype=torch.uint8)
+    ws = topt.decode_workspace(args, "cuda")
     a = topt.decode(q, K, V, seq_len, theta, mode=ref.POST, workspace=ws)
     first = a["out"].clone()
     for _ in range(3):
