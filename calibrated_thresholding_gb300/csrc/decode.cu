@@ -10,20 +10,19 @@
 // One persistent kernel per call (as many CTAs as fit on the GPU, no grid-wide
 // barrier), fed by two atomic work queues:
 //
-//  Scores.  Every pair's valid keys form 16-key tiles, numbered pair after
-//   pair.  Warps take runs of tiles from an atomic counter (guided: runs of up
-//   to 8 tiles shrink to 1 as the queue drains; each warp asks one run
-//   ahead, so the atomic's latency is hidden).  A warp streams its tiles'
+//  Scores.  Every pair's valid keys form 64-key units, numbered pair after
+//   pair.  Warps take units from an atomic counter (each warp asks one unit
+//   ahead, so the atomic's latency is hidden).  A warp streams its units'
 //   K rows through a private shared-memory ring with 1-D TMA bulk copies
-//   (cp.async.bulk, 4 KB per tile, L2 evict-first, completion on an
-//   mbarrier), computes each 16-key x G-head score block with m16n8k16 bf16
-//   MMAs (keys on the M side, query heads on the N side), writes
+//   (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first, completion on
+//   an mbarrier), computes each 16-key x G-head score block with m16n8k16
+//   bf16 MMAs (keys on the M side, query heads on the N side), writes
 //   a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4 bytes per
-//   key) and the tile's softmax partial (m, Z) per head, and counts finished
-//   tiles per pair.
+//   key) and the unit's softmax partial (m, Z) per head, then counts the unit
+//   as done for its pair (release atomic).
 //  Select.  When a CTA's warps find the tile queue empty, the CTA takes
 //   (pair, slice) items in pair order from the second queue and waits
-//   (bounded) until all tiles of the pair are done.  It loads the slice's
+//   (bounded) until all units of the pair are done.  It loads the slice's
 //   scores into registers in one go (8192 values per CTA) while it merges the
 //   pair's (m, Z) partials, turns theta into a bound on the score
 //   (post-softmax: s >= theta <=> a >= m + ln theta + ln Z), ballots per-head
@@ -36,8 +35,8 @@
 //  Exit.  The last CTA to leave zeroes the queues and counters, so the
 //   workspace is ready for the next call without a memset.
 //
-// No wait can deadlock: a CTA only waits for tiles that warps already took,
-// and a tile is only taken by a running warp.  Every wait is bounded and
+// No wait can deadlock: a CTA only waits for units that warps already took,
+// and a unit is only taken by a running warp.  Every wait is bounded and
 // reports TOPT_ETIMEOUT instead of hanging.
 #include "common.cuh"
 #include "internal.h"
@@ -48,16 +47,20 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
 constexpr int kTile = 16;                          // keys per MMA tile / bulk copy
+constexpr int kUnit = 64;                          // keys per work unit and softmax partial
+constexpr int kTilesPerUnit = kUnit / kTile;
 constexpr int kStages = 4;                         // ring slots per warp
-constexpr int kQueue = 8;                          // per-warp queue of taken runs (>= kStages + 1)
-constexpr int kMaxRun = 8;                         // tiles per run while the queue is long
-constexpr int kGatherUnroll = 8;                   // V rows in flight per thread slot
+constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDevices = 64;
 constexpr unsigned kSpinLimit = 1u << 24;          // bounded waits: x >= 32 ns sleep
 
 // Keys per select slice: the CTA holds the slice's G x keys scores in
 // registers, at most 64 per thread and 32 groups of 32 keys per warp.
+// V rows in flight per thread slot of the gather (register budget).
+template <int G>
+__host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 16 : (G <= 4 ? 10 : 6); }
+
 template <int G>
 __host__ __device__ constexpr int slice_keys() { return kThreads * (64 / G < 32 ? 64 / G : 32); }
 
@@ -75,16 +78,16 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  int mask_words, tpp, ipp, lstride;
+  int mask_words, upp, ipp, lstride;
   // workspace
   float* logits;      // [pairs][G][lstride]
-  float2* stats;      // [pairs][tpp][G]
+  float2* stats;      // [pairs][upp][G]
   float* part_num;    // [pairs][ipp][G][D]
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
   int* part_nu;       // [pairs][ipp]
-  unsigned* queues;   // [3]: next tile, next select item, CTAs finished   } zero between
-  unsigned* done;     // [pairs]: tiles scored                              } calls (the last
+  unsigned* queues;   // [3]: next unit, next select item, CTAs finished   } zero between
+  unsigned* done;     // [pairs]: units scored                              } calls (the last
   unsigned* ticket;   // [pairs]: select slices finished                    } CTA resets them)
 };
 
@@ -103,12 +106,12 @@ int logit_stride(int cache_len) { return (cache_len + 31) / 32 * 32; }
 DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
   const size_t pairs = (size_t)a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t tpp = (a.cache_len + kTile - 1) / kTile;
+  const size_t upp = (a.cache_len + kUnit - 1) / kUnit;
   DecodeLayout l;
   size_t off = 0;
   l.counters = off; off += kCounterBytes;
   l.logits = off;   off += align256(pairs * G * (size_t)logit_stride(a.cache_len) * sizeof(float));
-  l.stats = off;    off += align256(pairs * tpp * G * sizeof(float2));
+  l.stats = off;    off += align256(pairs * upp * G * sizeof(float2));
   l.part_num = off; off += align256(pairs * ipp * G * (size_t)a.head_dim * sizeof(float));
   l.part_r = off;   off += align256(pairs * ipp * G * sizeof(float));
   l.part_kt = off;  off += align256(pairs * ipp * G * sizeof(int));
@@ -156,6 +159,17 @@ __device__ __forceinline__ float ld_cg_hint_f32(const float* p, uint64_t pol) {
   asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
   return v;
 }
+// Online (max, sum) update with two new scores (either may be -inf).
+__device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) {
+  const float mt = fmaxf(x0, x1);
+  if (mt == -CUDART_INF_F) return;
+  const float mn = fmaxf(m, mt);
+  z = z * __expf(m - mn) + __expf(x0 - mn) + __expf(x1 - mn);
+  m = mn;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -168,7 +182,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 template <int D>
 struct Ring {
   uint64_t bar[kWarps][kStages];
-  int2 rq[kWarps][kQueue];  // runs of tiles taken by each warp, in order
+  int uq[kWarps][kQueue];  // units taken by each warp, in order
   __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
 };
 
@@ -185,8 +199,8 @@ struct Lists {
 
 template <int D, int G>
 struct DecodeSmem {
-  int tstart[kMaxBatch + 1];  // first tile of each sequence
-  int ntile[kMaxBatch];       // tiles per KV head of each sequence
+  int ustart[kMaxBatch + 1];  // first unit of each sequence
+  int nunit[kMaxBatch];       // units per KV head of each sequence
   int len[kMaxBatch];         // seq_len, staged once per CTA
   float M[G], Z[G], T[G], th[G];
   int item;
@@ -197,25 +211,25 @@ struct DecodeSmem {
   } u;
 };
 
-struct TileRef {
-  int pair, b, kvh, tile, L;
+struct UnitRef {
+  int pair, b, kvh, unit, L;
 };
 
-// Global tile index -> (pair, tile within the pair).
+// Global unit index -> (pair, unit within the pair).
 template <int D, int G>
-__device__ __forceinline__ TileRef tile_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int tau) {
-  int lo = 0, hi = B - 1;  // last b with tstart[b] <= tau
+__device__ __forceinline__ UnitRef unit_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int u) {
+  int lo = 0, hi = B - 1;  // last b with ustart[b] <= u
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (sm.tstart[mid] <= tau) lo = mid;
+    if (sm.ustart[mid] <= u) lo = mid;
     else hi = mid - 1;
   }
-  TileRef r;
+  UnitRef r;
   r.b = lo;
-  const int nt = sm.ntile[lo];
-  const int rem = tau - sm.tstart[lo];
-  r.kvh = rem / nt;
-  r.tile = rem - r.kvh * nt;
+  const int nu = sm.nunit[lo];
+  const int rem = u - sm.ustart[lo];
+  r.kvh = rem / nu;
+  r.unit = rem - r.kvh * nu;
   r.pair = lo * Hkv + r.kvh;
   r.L = sm.len[lo];
   return r;
@@ -240,10 +254,9 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
-  const int workers = gridDim.x * kWarps;
 
   uint64_t* bars = sm.u.ring.bar[warp];
-  int2* rq = sm.u.ring.rq[warp];
+  int* uq = sm.u.ring.uq[warp];
   unsigned char* slots = &sm.u.ring.slot[warp][0][0];
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep_pol = l2_evict_last_policy();
@@ -253,92 +266,71 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   }
   __syncwarp();
 
-  // Tile queue: lane 0 keeps one request in flight; run length shrinks as
-  // the queue drains (guided self-scheduling).
-  unsigned pend_start = 0, pend_len = 0;
-  auto request = [&](unsigned seen) {
-    if (lane == 0) {
-      const unsigned left = seen < (unsigned)total ? (unsigned)total - seen : 0u;
-      unsigned n = left / (2u * (unsigned)workers);
-      n = n < 1u ? 1u : (n > (unsigned)kMaxRun ? (unsigned)kMaxRun : n);
-      pend_len = n;
-      pend_start = atomicAdd(&p.queues[0], n);
-    }
-  };
-  request(0);
-  auto take = [&](int& s, int& e) {
-    s = (int)__shfl_sync(0xffffffffu, pend_start, 0);
-    const int n = (int)__shfl_sync(0xffffffffu, pend_len, 0);
-    e = min(s + n, total);
-    if (s < total) request((unsigned)s + n);
+  // Unit queue: lane 0 keeps one request in flight.
+  unsigned pending = 0;
+  if (lane == 0) pending = atomicAdd(&p.queues[0], 1u);
+  auto take = [&]() -> int {
+    const int u = (int)__shfl_sync(0xffffffffu, pending, 0);
+    if (lane == 0 && u < total) pending = atomicAdd(&p.queues[0], 1u);
+    return u;
   };
 
-  // Producer: the run being issued.
-  int ps = 0, pe = 0, qh = 0, qt = 0;
-  take(ps, pe);
-  if (ps < total) {
-    if (lane == 0) rq[qh % kQueue] = make_int2(ps, pe);
+  // Producer: the unit being issued and its tile cursor.
+  int pu = take(), pt = 0, pnt = 0, qh = 0, qt = 0;
+  UnitRef pr;
+  auto start_unit = [&]() {
+    pr = unit_of(sm, p.B, p.Hkv, pu);
+    pnt = (min(kUnit, pr.L - pr.unit * kUnit) + kTile - 1) / kTile;
+    if (lane == 0) uq[qh % kQueue] = pu;
     ++qh;
-  }
+  };
+  if (pu < total) start_unit();
   long issued = 0;
-  auto issue = [&]() {  // copy tile ps into the next slot
-    const TileRef r = tile_of(sm, p.B, p.Hkv, ps);
-    const int key0 = r.tile * kTile;
-    const unsigned bytes = (unsigned)min(kTile, r.L - key0) * D * 2;
+  auto issue = [&]() {  // copy the producer's current tile into the next slot
+    const int key0 = pr.unit * kUnit + pt * kTile;
+    const unsigned bytes = (unsigned)min(kTile, pr.L - key0) * D * 2;
     const int s = (int)(issued % kStages);
     if (lane == 0) {
       mbar_expect_tx(&bars[s], bytes);
-      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)r.pair * p.Nmax + key0) * D, bytes, &bars[s], pol);
+      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)pr.pair * p.Nmax + key0) * D, bytes, &bars[s], pol);
     }
     ++issued;
-    if (++ps == pe) {
-      take(ps, pe);
-      if (ps < total) {
-        if (lane == 0) rq[qh % kQueue] = make_int2(ps, pe);
-        ++qh;
-      }
+    if (++pt == pnt) {
+      pt = 0;
+      pu = take();
+      if (pu < total) start_unit();
     }
   };
-  while (ps < total && issued < kStages) issue();
+  while (pu < total && issued < kStages) issue();
   __syncwarp();
 
   const float scale = p.sm_scale;
   const int h0 = 2 * t, h1 = 2 * t + 1;
   uint32_t qf[NP][4];
   int qpair = -1;
-  int run_pair = -1, run_cnt = 0;
   long consumed = 0;
-  auto publish = [&]() {  // this warp's scores of run_pair are visible, then counted
-    if (run_cnt > 0) {
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) atomicAdd(&p.done[run_pair], (unsigned)run_cnt);
-      run_cnt = 0;
-    }
-  };
   while (qt < qh) {
-    const int2 run = rq[qt % kQueue];
+    const UnitRef r = unit_of(sm, p.B, p.Hkv, uq[qt % kQueue]);
     ++qt;
-    for (int tau = run.x; tau < run.y; ++tau) {
-      const TileRef r = tile_of(sm, p.B, p.Hkv, tau);
-      if (r.pair != run_pair) {
-        publish();
-        run_pair = r.pair;
-      }
-      if (r.pair != qpair) {
-        qpair = r.pair;
-        if (g < G) {
-          const __nv_bfloat16* qrow = p.q + ((size_t)r.b * p.Hq + r.kvh * G + g) * D;
+    const int ntile = (min(kUnit, r.L - r.unit * kUnit) + kTile - 1) / kTile;
+    if (r.pair != qpair) {
+      qpair = r.pair;
+      if (g < G) {
+        const __nv_bfloat16* qrow = p.q + ((size_t)r.b * p.Hq + r.kvh * G + g) * D;
 #pragma unroll
-          for (int pp = 0; pp < NP; ++pp) {
-            const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
-            qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
-          }
-        } else {
-#pragma unroll
-          for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
+        for (int pp = 0; pp < NP; ++pp) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
+          qf[pp][0] = w.x; qf[pp][1] = w.y; qf[pp][2] = w.z; qf[pp][3] = w.w;
         }
+      } else {
+#pragma unroll
+        for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
       }
+    }
+    float* lrow = p.logits + (size_t)r.pair * G * p.lstride;
+    const int L = r.L;
+    float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
+    for (int tt = 0; tt < ntile; ++tt) {
       const int s = (int)(consumed % kStages);
       const unsigned parity = (unsigned)((consumed / kStages) & 1);
       if (!mbar_wait(&bars[s], parity)) set_status(p.status, TOPT_ETIMEOUT);
@@ -364,48 +356,40 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
       ++consumed;
       // The slot's data is consumed (the MMAs used it): refill it.
       __syncwarp();
-      if (ps < total) {
+      if (pu < total) {
         if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         issue();
         __syncwarp();
       }
-      const int key0 = r.tile * kTile;
+      const int key0 = r.unit * kUnit + tt * kTile;
       const int j0 = key0 + g;
       const int j1 = key0 + g + 8;
-      const int L = r.L;
       const float a00 = j0 < L ? cc[0] * scale : -CUDART_INF_F;
       const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
       const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
       const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
-      float* lrow = p.logits + (size_t)r.pair * G * p.lstride;
-      // Per-tile softmax partial of each head: max, then sum over the 16 keys.
-      float m0 = fmaxf(a00, a10), m1 = fmaxf(a01, a11);
-#pragma unroll
-      for (int off = 4; off < kWarp; off <<= 1) {
-        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-      }
-      float z0 = __expf(a00 - m0) + __expf(a10 - m0);
-      float z1 = __expf(a01 - m1) + __expf(a11 - m1);
-#pragma unroll
-      for (int off = 4; off < kWarp; off <<= 1) {
-        z0 += __shfl_xor_sync(0xffffffffu, z0, off);
-        z1 += __shfl_xor_sync(0xffffffffu, z1, off);
-      }
-      float2* st = p.stats + ((size_t)r.pair * p.tpp + r.tile) * G;
       if (h0 < G) {
         if (j0 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j0, a00, keep_pol);
         if (j1 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j1, a10, keep_pol);
-        if (g == 0) st[h0] = make_float2(m0, z0);
+        ms_add2(m0, z0, a00, a10);
       }
       if (h1 < G) {
         if (j0 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j0, a01, keep_pol);
         if (j1 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j1, a11, keep_pol);
-        if (g == 0) st[h1] = make_float2(m1, z1);
+        ms_add2(m1, z1, a01, a11);
       }
-      ++run_cnt;
     }
-    publish();
+    // Partial of this unit: merge over the 8 key rows (lane bits 2..4).
+    ms_warp_merge(m0, z0, 4);
+    ms_warp_merge(m1, z1, 4);
+    if (g == 0) {
+      float2* st = p.stats + ((size_t)r.pair * p.upp + r.unit) * G;
+      if (h0 < G) st[h0] = make_float2(m0, z0);
+      if (h1 < G) st[h1] = make_float2(m1, z1);
+    }
+    // Publish: the warp's writes are ordered before the release increment.
+    __syncwarp();
+    if (lane == 0) red_release_add(&p.done[r.pair], 1u);
   }
   // Every issued copy has been waited for; retire the barriers before the
   // buffer is reused by the select phase.
@@ -425,6 +409,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
+  constexpr int kGatherUnroll = gather_unroll<G>();
   Lists<D, G>& ls = sm.u.lists;
   const int pair = item / p.ipp;
   const int slice = item - pair * p.ipp;
@@ -434,12 +419,12 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   const int lane = threadIdx.x & 31;
   const int L = sm.len[b];
   if (L < 1 || L > p.Nmax) return;  // reported at kernel start
-  const int nt = sm.ntile[b];
+  const int nu = sm.nunit[b];
 
-  // Wait (bounded) until every tile of the pair has been scored.
+  // Wait (bounded) until every unit of the pair has been scored.
   if (threadIdx.x == 0) {
     unsigned spins = 0;
-    while (ld_acquire_u32(&p.done[pair]) < (unsigned)nt) {
+    while (ld_acquire_u32(&p.done[pair]) < (unsigned)nu) {
       __nanosleep(32);
       if (++spins > kSpinLimit) {
         set_status(p.status, TOPT_ETIMEOUT);
@@ -464,7 +449,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
       wv[gi][h] = j < L ? ld_cg_hint_f32(lrow + (size_t)h * p.lstride + j, pol) : -CUDART_INF_F;
   }
 
-  // Softmax statistics of the whole row, per head, from the tile partials.
+  // Softmax statistics of the whole row, per head, from the unit partials.
   {
     float m[G], z[G];
 #pragma unroll
@@ -472,10 +457,10 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
       m[h] = -CUDART_INF_F;
       z[h] = 0.f;
     }
-    for (int c = threadIdx.x; c < nt; c += kThreads) {
+    for (int c = threadIdx.x; c < nu; c += kThreads) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float2 v = __ldcg(p.stats + ((size_t)pair * p.tpp + c) * G + h);
+        const float2 v = __ldcg(p.stats + ((size_t)pair * p.upp + c) * G + h);
         ms_merge(m[h], z[h], v.x, v.y);
       }
     }
@@ -672,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw);
 
-  // Tiles per sequence (every KV head of a sequence has the same length).
+  // Units per sequence (every KV head of a sequence has the same length).
   if (threadIdx.x < kWarp) {
     const int lane = threadIdx.x;
     const int per = (p.B + kWarp - 1) / kWarp;
@@ -682,11 +667,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
       if (b < p.B) {
         const int L = p.seq_len[b];
         sm.len[b] = L;
-        int nt = 0;
-        if (L >= 1 && L <= p.Nmax) nt = (L + kTile - 1) / kTile;
+        int nu = 0;
+        if (L >= 1 && L <= p.Nmax) nu = (L + kUnit - 1) / kUnit;
         else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
-        sm.ntile[b] = nt > 0 ? nt : 1;
-        run += nt * p.Hkv;
+        sm.nunit[b] = nu > 0 ? nu : 1;
+        run += nu * p.Hkv;
       }
     }
     int incl = run;
@@ -699,16 +684,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
     for (int i = 0; i < per; ++i) {
       const int b = lane * per + i;
       if (b < p.B) {
-        sm.tstart[b] = acc;
+        sm.ustart[b] = acc;
         const int L = sm.len[b];
-        if (L >= 1 && L <= p.Nmax) acc += ((L + kTile - 1) / kTile) * p.Hkv;
+        if (L >= 1 && L <= p.Nmax) acc += ((L + kUnit - 1) / kUnit) * p.Hkv;
       }
     }
-    if (lane == kWarp - 1) sm.tstart[p.B] = incl;
+    if (lane == kWarp - 1) sm.ustart[p.B] = incl;
   }
   __syncthreads();
 
-  phase_scores<D, G>(p, sm, sm.tstart[p.B]);
+  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
   __syncthreads();
 
   // Select slices past a sequence's length only zero their mask words.
@@ -862,7 +847,7 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.status = a.status;
   p.mask_words = (a.cache_len + 31) / 32;
-  p.tpp = (a.cache_len + kTile - 1) / kTile;
+  p.upp = (a.cache_len + kUnit - 1) / kUnit;
   p.lstride = logit_stride(a.cache_len);
   p.ipp = 1;
   const int G = a.n_q_heads / a.n_kv_heads;
