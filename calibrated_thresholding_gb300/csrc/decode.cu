@@ -7,8 +7,9 @@
 // is one (sequence, KV head) and its G = Hq/Hkv query heads ([TopTheta §2.2,
 // GQA]).
 //
-// One persistent kernel per call (as many CTAs as fit on the GPU, no grid-wide
-// barrier), fed by two atomic work queues:
+// One persistent cooperative kernel per call (as many CTAs as fit on the GPU;
+// two in three stream K, the rest select from the start), fed by two atomic
+// work queues:
 //
 //  Scores.  Every pair's valid keys form 64-key units, numbered pair after
 //   pair.  Warps take units from an atomic counter (each warp asks one unit
@@ -79,6 +80,7 @@ struct DecodeParams {
   uint32_t* mask;
   int32_t* status;
   int mask_words, upp, ipp, lstride;
+  int streamers;      // CTAs [0, streamers) score K first; the rest only select
   // workspace
   float* logits;      // [pairs][G][lstride]
   float2* stats;      // [pairs][upp][G]
@@ -247,7 +249,7 @@ __device__ __forceinline__ UnitRef unit_of(const DecodeSmem<D, G>& sm, int B, in
 // 2t, 2t+1) and (key g+8, heads 2t, 2t+1).
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total) {
+__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total, int ctas) {
   constexpr int NP = D / 32;
   constexpr unsigned kTileBytes = kTile * D * 2;
   const int warp = threadIdx.x >> 5;
@@ -449,7 +451,10 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
       wv[gi][h] = j < L ? ld_cg_hint_f32(lrow + (size_t)h * p.lstride + j, pol) : -CUDART_INF_F;
   }
 
-  // Softmax statistics of the whole row, per head, from the unit partials.
+  // Softmax statistics of the whole row, per head, from the unit partials
+  // (the thresholds are fetched alongside).
+  float th_pre = 0.f;
+  if (threadIdx.x < G) th_pre = p.theta[(size_t)(kvh * G + threadIdx.x) * p.Lmax + (min(L, p.Lmax) - 1)];
   {
     float m[G], z[G];
 #pragma unroll
@@ -478,7 +483,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
       float mm = -CUDART_INF_F, zz = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) ms_merge(mm, zz, ls.m[w][h], ls.z[w][h]);
-      const float th = p.theta[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)];
+      const float th = th_pre;
       sm.M[h] = mm;
       sm.Z[h] = zz;
       sm.th[h] = th;
@@ -693,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
   }
   __syncthreads();
 
-  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
+  if ((int)blockIdx.x < p.streamers) phase_scores<D, G>(p, sm, sm.ustart[p.B], p.streamers);
   __syncthreads();
 
   // Select slices past a sequence's length only zero their mask words.
@@ -791,9 +796,15 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   p.queues = counters;
   p.done = counters + 4;
   p.ticket = counters + 4 + pairs;
+  // Two CTAs in three stream K; the third starts selecting as soon as its
+  // pair is ready.  Co-residency (cooperative launch) guarantees that every
+  // unit a selecting CTA waits for is being processed by a running warp.
+  p.streamers = grid - grid / 3;
   if ((e = record(a.events[0], s)) != cudaSuccess) return e;
-  decode_fused_kernel<D, G><<<grid, kThreads, sizeof(DecodeSmem<D, G>), s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  void* kargs[] = {&p};
+  e = cudaLaunchCooperativeKernel((const void*)decode_fused_kernel<D, G>, dim3(grid), dim3(kThreads), kargs,
+                                  sizeof(DecodeSmem<D, G>), s);
+  if (e != cudaSuccess) return e;
   return record(a.events[1], s);
 }
 
