@@ -343,25 +343,32 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
         ka[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)g * D * 2 + (32 * pp + 8 * t) * 2);
         kb[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)(g + 8) * D * 2 + (32 * pp + 8 * t) * 2);
       }
-      float cc[4] = {0.f, 0.f, 0.f, 0.f};
+      // One accumulator per slab: NP independent MMA chains of two.
+      float cs[NP][4];
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) {
+        cs[pp][0] = cs[pp][1] = cs[pp][2] = cs[pp][3] = 0.f;
         const uint32_t wa[4] = {ka[pp].x, ka[pp].y, ka[pp].z, ka[pp].w};
         const uint32_t wb[4] = {kb[pp].x, kb[pp].y, kb[pp].z, kb[pp].w};
 #pragma unroll
         for (int ss = 0; ss < 2; ++ss) {
           const uint32_t af[4] = {wa[2 * ss], wb[2 * ss], wa[2 * ss + 1], wb[2 * ss + 1]};
           const uint32_t bf[2] = {qf[pp][2 * ss], qf[pp][2 * ss + 1]};
-          mma_16816_bf16(cc, af, bf);
+          mma_16816_bf16(cs[pp], af, bf);
         }
       }
       ++consumed;
-      // The slot's data is consumed (the MMAs used it): refill it.
+      // Every lane's shared-memory reads of the slot have completed (their
+      // values fed the MMAs above); refill the slot.
       __syncwarp();
-      if (pu < total) {
-        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue();
-        __syncwarp();
+      if (pu < total) issue();
+      float cc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = cs[0][e];
+#pragma unroll
+        for (int pp = 1; pp < NP; ++pp) v += cs[pp][e];
+        cc[e] = v;
       }
       const int key0 = r.unit * kUnit + tt * kTile;
       const int j0 = key0 + g;
