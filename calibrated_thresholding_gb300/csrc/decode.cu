@@ -7,38 +7,32 @@
 // is one (sequence, KV head) and its G = Hq/Hkv query heads ([TopTheta §2.2,
 // GQA]).
 //
-// One persistent cooperative kernel per call (as many CTAs as fit on the GPU;
-// two in three stream K, the rest select from the start), fed by two atomic
-// work queues:
+// Two kernels per call, the second launched as a programmatic dependent of
+// the first (it is scheduled while the first drains and waits for its data):
 //
-//  Scores.  Every pair's valid keys form 64-key units, numbered pair after
-//   pair.  Warps take units from an atomic counter (each warp asks one unit
-//   ahead, so the atomic's latency is hidden).  A warp streams its units'
-//   K rows through a private shared-memory ring with 1-D TMA bulk copies
-//   (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first, completion on
-//   an mbarrier), computes each 16-key x G-head score block with m16n8k16
-//   bf16 MMAs (keys on the M side, query heads on the N side), writes
-//   a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4 bytes per
-//   key) and the unit's softmax partial (m, Z) per head, then counts the unit
-//   as done for its pair (release atomic).
-//  Select.  When a CTA's warps find the tile queue empty, the CTA takes
-//   (pair, slice) items in pair order from the second queue and waits
-//   (bounded) until all units of the pair are done.  It loads the slice's
-//   scores into registers in one go (8192 values per CTA) while it merges the
-//   pair's (m, Z) partials, turns theta into a bound on the score
-//   (post-softmax: s >= theta <=> a >= m + ln theta + ln Z), ballots per-head
-//   masks of 32 keys per warp, ORs them into the group union, compacts the
-//   union into a shared list by popcount prefix, gathers only those V rows
-//   (16-byte loads, 64 rows in flight per CTA) and accumulates
-//   sum exp(a - m) V per head.  The last slice of a pair to finish (atomic
-//   ticket, nothing waits) combines the slices and applies SDC [Eq. 4] and
-//   VMC [Eq. 5-7].
-//  Exit.  The last CTA to leave zeroes the queues and counters, so the
-//   workspace is ready for the next call without a memset.
+//  decode_scores_kernel (persistent, as many CTAs as fit, ~85 registers so
+//   24 warps share each SM).  Every pair's valid keys form 64-key units,
+//   numbered pair after pair and handed to warps by an atomic counter (each
+//   warp asks one unit ahead, so the atomic's latency is hidden).  A warp
+//   streams its units' K rows through a private shared-memory ring with 1-D
+//   TMA bulk copies (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first,
+//   completion on an mbarrier), computes each 16-key x G-head score block
+//   with m16n8k16 bf16 MMAs (keys on the M side, query heads on the N side),
+//   writes a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4
+//   bytes per key) and the unit's softmax partial (m, Z) per head.
+//  decode_select_kernel (one CTA per (pair, slice)).  Loads the slice's
+//   scores into registers in one go while it merges the pair's (m, Z)
+//   partials, turns theta into a bound on the score (post-softmax:
+//   s >= theta <=> a >= m + ln theta + ln Z), ballots per-head masks of 32
+//   keys per warp, ORs them into the group union, compacts the union into a
+//   shared list by popcount prefix, gathers only those V rows (16-byte loads,
+//   many rows in flight) and accumulates sum exp(a - m) V per head.  The last
+//   slice of a pair to finish (atomic ticket, nothing waits) combines the
+//   slices and applies SDC [Eq. 4] and VMC [Eq. 5-7].
 //
-// No wait can deadlock: a CTA only waits for units that warps already took,
-// and a unit is only taken by a running warp.  Every wait is bounded and
-// reports TOPT_ETIMEOUT instead of hanging.
+// Counters live at the start of the workspace; the last CTA to use one puts
+// it back to zero, so the workspace is ready for the next call without a
+// memset.
 #include "common.cuh"
 #include "internal.h"
 
@@ -49,12 +43,10 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
 constexpr int kTile = 16;                          // keys per MMA tile / bulk copy
 constexpr int kUnit = 64;                          // keys per work unit and softmax partial
-constexpr int kTilesPerUnit = kUnit / kTile;
-constexpr int kStages = 4;                         // ring slots per warp
+constexpr int kStages = 2;                         // ring slots per warp
 constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDevices = 64;
-constexpr unsigned kSpinLimit = 1u << 24;          // bounded waits: x >= 32 ns sleep
 
 // Keys per select slice: the CTA holds the slice's G x keys scores in
 // registers, at most 64 per thread and 32 groups of 32 keys per warp.
@@ -80,7 +72,6 @@ struct DecodeParams {
   uint32_t* mask;
   int32_t* status;
   int mask_words, upp, ipp, lstride;
-  int streamers;      // CTAs [0, streamers) score K first; the rest only select
   // workspace
   float* logits;      // [pairs][G][lstride]
   float2* stats;      // [pairs][upp][G]
@@ -88,16 +79,15 @@ struct DecodeParams {
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
   int* part_nu;       // [pairs][ipp]
-  unsigned* queues;   // [3]: next unit, next select item, CTAs finished   } zero between
-  unsigned* done;     // [pairs]: units scored                              } calls (the last
-  unsigned* ticket;   // [pairs]: select slices finished                    } CTA resets them)
+  unsigned* queues;   // [2]: next unit, score CTAs finished      } zero between calls
+  unsigned* ticket;   // [pairs]: select slices finished          } (reset by their last user)
 };
 
 // The workspace starts with a fixed-size block of counters, so a workspace
 // reused across shapes keeps them in one place: zero before the first call,
 // and every call leaves the ones it used at zero again.
 constexpr size_t kCounterBytes = 128 * 1024;
-constexpr int kMaxPairs = (int)(kCounterBytes / sizeof(unsigned) - 4) / 2;
+constexpr int kMaxPairs = (int)(kCounterBytes / sizeof(unsigned) - 4);
 
 struct DecodeLayout {
   size_t counters, logits, stats, part_num, part_r, part_kt, part_nu, total;
@@ -169,27 +159,24 @@ __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) 
   z = z * __expf(m - mn) + __expf(x0 - mn) + __expf(x1 - mn);
   m = mn;
 }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // ----------------------------------------------------------------------------
 // Shared memory: the score rings and the select lists share one buffer.
 // ----------------------------------------------------------------------------
 template <int D>
-struct Ring {
+struct ScoreSmem {
+  int ustart[kMaxBatch + 1];  // first unit of each sequence
+  int nunit[kMaxBatch];       // units per KV head of each sequence
+  int len[kMaxBatch];         // seq_len, staged once per CTA
+  int last;
   uint64_t bar[kWarps][kStages];
-  int uq[kWarps][kQueue];  // units taken by each warp, in order
+  int uq[kWarps][kQueue];     // units taken by each warp, in order
   __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
 };
 
 template <int D, int G>
-struct Lists {
+struct SelectSmem {
+  float M[G], Z[G], T[G], th[G];
+  int last;
   int j[slice_keys<G>()];       // union keys of the slice
   float w[slice_keys<G>()][G];  // exp(a - m) per head (0 if the head drops the key)
   float acc[kWarps][G][D];
@@ -199,27 +186,13 @@ struct Lists {
   float m[kWarps][G], z[kWarps][G];
 };
 
-template <int D, int G>
-struct DecodeSmem {
-  int ustart[kMaxBatch + 1];  // first unit of each sequence
-  int nunit[kMaxBatch];       // units per KV head of each sequence
-  int len[kMaxBatch];         // seq_len, staged once per CTA
-  float M[G], Z[G], T[G], th[G];
-  int item;
-  int last;
-  union {
-    Ring<D> ring;
-    Lists<D, G> lists;
-  } u;
-};
-
 struct UnitRef {
   int pair, b, kvh, unit, L;
 };
 
 // Global unit index -> (pair, unit within the pair).
-template <int D, int G>
-__device__ __forceinline__ UnitRef unit_of(const DecodeSmem<D, G>& sm, int B, int Hkv, int u) {
+template <int D>
+__device__ __forceinline__ UnitRef unit_of(const ScoreSmem<D>& sm, int B, int Hkv, int u) {
   int lo = 0, hi = B - 1;  // last b with ustart[b] <= u
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -249,7 +222,7 @@ __device__ __forceinline__ UnitRef unit_of(const DecodeSmem<D, G>& sm, int B, in
 // 2t, 2t+1) and (key g+8, heads 2t, 2t+1).
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int total, int ctas) {
+__device__ void phase_scores(const DecodeParams& p, ScoreSmem<D>& sm, int total) {
   constexpr int NP = D / 32;
   constexpr unsigned kTileBytes = kTile * D * 2;
   const int warp = threadIdx.x >> 5;
@@ -257,9 +230,9 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
   const int g = lane >> 2;
   const int t = lane & 3;
 
-  uint64_t* bars = sm.u.ring.bar[warp];
-  int* uq = sm.u.ring.uq[warp];
-  unsigned char* slots = &sm.u.ring.slot[warp][0][0];
+  uint64_t* bars = sm.bar[warp];
+  int* uq = sm.uq[warp];
+  unsigned char* slots = &sm.slot[warp][0][0];
   const uint64_t pol = l2_evict_first_policy();
   const uint64_t keep_pol = l2_evict_last_policy();
   if (lane == 0) {
@@ -396,12 +369,8 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
       if (h0 < G) st[h0] = make_float2(m0, z0);
       if (h1 < G) st[h1] = make_float2(m1, z1);
     }
-    // Publish: the warp's writes are ordered before the release increment.
-    __syncwarp();
-    if (lane == 0) red_release_add(&p.done[r.pair], 1u);
   }
-  // Every issued copy has been waited for; retire the barriers before the
-  // buffer is reused by the select phase.
+  // Every issued copy has been waited for; retire the barriers.
   __syncwarp();
   if (lane == 0)
     for (int s = 0; s < kStages; ++s)
@@ -413,36 +382,22 @@ __device__ void phase_scores(const DecodeParams& p, DecodeSmem<D, G>& sm, int to
 // Select: one slice of one pair per item.
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int item) {
+__device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int item) {
   constexpr int LPR = D / 8;              // lanes per V row (16 bytes each)
   constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
   constexpr int kGatherUnroll = gather_unroll<G>();
-  Lists<D, G>& ls = sm.u.lists;
+  SelectSmem<D, G>& ls = sm;
   const int pair = item / p.ipp;
   const int slice = item - pair * p.ipp;
   const int b = pair / p.Hkv;
   const int kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int L = sm.len[b];
-  if (L < 1 || L > p.Nmax) return;  // reported at kernel start
-  const int nu = sm.nunit[b];
-
-  // Wait (bounded) until every unit of the pair has been scored.
-  if (threadIdx.x == 0) {
-    unsigned spins = 0;
-    while (ld_acquire_u32(&p.done[pair]) < (unsigned)nu) {
-      __nanosleep(32);
-      if (++spins > kSpinLimit) {
-        set_status(p.status, TOPT_ETIMEOUT);
-        break;
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
+  const int L = p.seq_len[b];
+  if (L < 1 || L > p.Nmax) return;  // reported by the score kernel
+  const int nu = (L + kUnit - 1) / kUnit;
 
   // The slice's scores, all loads in flight at once: group gi of warp w is
   // keys s0 + gi*128 + w*32 + lane.
@@ -638,6 +593,7 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
+  if (threadIdx.x == 0) p.ticket[pair] = 0u;  // every slice has arrived
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
     const int h = idx / D;
     const int dd = idx - h * D;
@@ -665,9 +621,11 @@ __device__ void phase_select(const DecodeParams& p, DecodeSmem<D, G>& sm, int it
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 6) decode_scores_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw);
+  ScoreSmem<D>& sm = *reinterpret_cast<ScoreSmem<D>*>(smem_raw);
+  // The select kernel may be scheduled now; it waits for this grid's data.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Units per sequence (every KV head of a sequence has the same length).
   if (threadIdx.x < kWarp) {
@@ -705,41 +663,30 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fused_kernel(const DecodeP
   }
   __syncthreads();
 
-  if ((int)blockIdx.x < p.streamers) phase_scores<D, G>(p, sm, sm.ustart[p.B], p.streamers);
-  __syncthreads();
+  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
 
-  // Select slices past a sequence's length only zero their mask words.
-  const int items = p.B * p.Hkv * p.ipp;
-  for (;;) {
-    if (threadIdx.x == 0) sm.item = (int)atomicAdd(&p.queues[1], 1u);
-    __syncthreads();
-    const int item = sm.item;
-    if (item >= items) break;
-    phase_select<D, G>(p, sm, item);
-    __syncthreads();
-  }
-
-  // The last CTA out leaves the queues and counters zeroed for the next call.
-  __threadfence();
+  // The last CTA out leaves the unit queue zeroed for the next call.
   __syncthreads();
-  if (threadIdx.x == 0) sm.last = (atomicAdd(&p.queues[2], 1u) == gridDim.x - 1u);
-  __syncthreads();
-  if (sm.last) {
+  if (threadIdx.x == 0) {
     __threadfence();
-    const int pairs = p.B * p.Hkv;
-    for (int i = threadIdx.x; i < pairs; i += kThreads) {
-      p.done[i] = 0u;
-      p.ticket[i] = 0u;
-    }
-    if (threadIdx.x == 0) {
+    if (atomicAdd(&p.queues[1], 1u) == gridDim.x - 1u) {
       p.queues[0] = 0u;
       p.queues[1] = 0u;
-      p.queues[2] = 0u;
     }
   }
 }
 
-// Resident CTAs of the persistent grid, per device and instantiation.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 3) decode_select_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
+  // Wait until the score kernel has finished and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  phase_select<D, G>(p, sm, blockIdx.x);
+}
+
+// Resident CTAs of the persistent score grid, per device and instantiation
+// (also sets both kernels' shared-memory limits once).
 template <int D, int G>
 cudaError_t grid_of(int& grid) {
   static int cached[kMaxDevices] = {};
@@ -748,12 +695,15 @@ cudaError_t grid_of(int& grid) {
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (cached[dev] == 0) {
-    const size_t smem = sizeof(DecodeSmem<D, G>);
-    if ((e = cudaFuncSetAttribute(decode_fused_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = sizeof(ScoreSmem<D>);
+    if ((e = cudaFuncSetAttribute(decode_scores_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)) != cudaSuccess)
       return e;
+    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sizeof(SelectSmem<D, G>))) != cudaSuccess)
+      return e;
     int per_sm = 0, sms = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_kernel<D, G>, kThreads, smem)) !=
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_scores_kernel<D, G>, kThreads, smem)) !=
         cudaSuccess)
       return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -801,17 +751,21 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
   unsigned* counters = reinterpret_cast<unsigned*>(ws + l.counters);
   p.queues = counters;
-  p.done = counters + 4;
-  p.ticket = counters + 4 + pairs;
-  // Two CTAs in three stream K; the third starts selecting as soon as its
-  // pair is ready.  Co-residency (cooperative launch) guarantees that every
-  // unit a selecting CTA waits for is being processed by a running warp.
-  p.streamers = grid - grid / 3;
+  p.ticket = counters + 4;
   if ((e = record(a.events[0], s)) != cudaSuccess) return e;
-  void* kargs[] = {&p};
-  e = cudaLaunchCooperativeKernel((const void*)decode_fused_kernel<D, G>, dim3(grid), dim3(kThreads), kargs,
-                                  sizeof(DecodeSmem<D, G>), s);
-  if (e != cudaSuccess) return e;
+  decode_scores_kernel<D, G><<<grid, kThreads, sizeof(ScoreSmem<D>), s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pairs * p.ipp));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(SelectSmem<D, G>);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G>, p)) != cudaSuccess) return e;
   return record(a.events[1], s);
 }
 
