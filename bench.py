@@ -47,7 +47,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_fused_kernel
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_scores_kernel
 # (one layer call of the default workload), with the hash of the kernel source
 # those counters were taken on.  Reported as null when the source differs.
 DECODE_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
@@ -226,6 +226,7 @@ class DecodeState:
             if events is not None:
                 a.events[0] = events[l][0]
                 a.events[1] = events[l][1]
+                a.events[2] = events[l][2]
             rc = L.topt_decode(ctypes.byref(a), stream)
             if rc:
                 raise topt.ToptError("topt_decode", rc)
@@ -234,6 +235,7 @@ class DecodeState:
         for a in self.dargs:
             a.events[0] = None
             a.events[1] = None
+            a.events[2] = None
 
 
 def algorithmic_bytes(state):
@@ -404,7 +406,7 @@ def main():
     for _ in range(args.warmup):
         state.run_step(L, sh)
     # events around the decode kernel of every layer call of the timed region
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
           for _ in range(args.steps)]
     for s in ev:
         for l in s:
@@ -430,16 +432,20 @@ def main():
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    kern_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(args.steps) for l in range(layers)]
+    score_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(args.steps) for l in range(layers)]
+    kern_ms = [ev[s][l][0].elapsed_time(ev[s][l][2]) for s in range(args.steps) for l in range(layers)]
     ms_per_step = ms / args.steps
     tokens = wl.B * args.steps * world
     value = tokens / (ms / 1e3)
 
     k_bytes, per_layer = algorithmic_bytes(state)
     kern_avg = float(np.mean(kern_ms)) / 1e3
+    score_avg = float(np.mean(score_ms)) / 1e3
     peak, peak_kind = hbm_peak()
     alg_bytes = float(np.mean(per_layer))
-    achieved = alg_bytes / kern_avg / 1e9
+    q_bytes = wl.B * wl.Hq * wl.d * 2
+    achieved = (k_bytes + q_bytes) / score_avg / 1e9
+    call_gbs = alg_bytes / kern_avg / 1e9
     traffic = None
     src = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc", "decode.cu")
     if DECODE_TRAFFIC["source_sha256"] == source_sha(src):
@@ -462,15 +468,20 @@ def main():
                    "l2": "inputs larger than L2: each layer call streams a distinct "
                          f"{k_bytes / 1e6:.0f} MB K cache",
                    "parallelism": f"replicas x{world} (independent sequences per GPU)"},
-        "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "decode_scores_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic,
-                     "algorithmic_bytes_per_launch": alg_bytes,
-                     "bytes": "whole K cache + union V rows + theta entries + q, mu, out",
-                     "avg_launch_ms": kern_avg * 1e3},
+                     "algorithmic_bytes_per_launch": k_bytes + q_bytes,
+                     "bytes": "whole K cache + q",
+                     "avg_launch_ms": score_avg * 1e3},
+        "decode_call": {"gbs": call_gbs, "frac_of_measured": call_gbs / peak,
+                        "frac_of_8tbs": call_gbs / NOMINAL_HBM_GBS, "avg_ms": kern_avg * 1e3,
+                        "select_avg_ms": (kern_avg - score_avg) * 1e3,
+                        "bytes_per_call": alg_bytes,
+                        "bytes": "whole K cache + union V rows + theta entries + q, mu, out"},
         "vrows_per_group": vrows_per_group,
         "kept_over_k": kept_ratio_by_bucket(state),
         "gpu_launches": args.steps * layers * 2,

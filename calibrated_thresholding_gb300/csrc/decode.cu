@@ -765,8 +765,9 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if ((e = record(a.events[1], s)) != cudaSuccess) return e;
   if ((e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G>, p)) != cudaSuccess) return e;
-  return record(a.events[1], s);
+  return record(a.events[2], s);
 }
 
 template <int D>

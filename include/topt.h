@@ -96,8 +96,10 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
-   * `stream` right before [0] and right after [1] the decode kernel, so a
-   * caller can time it; [2] is reserved and must be NULL. */
+   * `stream` before the score kernel [0], between the score and the select
+   * kernel [1] and after the select kernel [2].  An event between the two
+   * kernels keeps the select kernel from being scheduled early, so leave [1]
+   * NULL unless the split is wanted. */
   void* events[3];
 } topt_decode_args;
 
