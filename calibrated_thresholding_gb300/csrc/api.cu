@@ -100,6 +100,17 @@ topt_status topt_decode(const topt_decode_args* a, topt_stream stream) {
   return cuda_status(decode_launch(*a, (cudaStream_t)stream));
 }
 
+topt_status topt_decode_noalloc(const topt_decode_args* a, topt_stream stream) {
+  topt_status st = check_decode_shape(a);
+  if (st != TOPT_OK) return st;
+  if (!a->q || !a->k_cache || !a->v_cache || !a->seq_len || !a->theta || !a->out) return TOPT_EINVAL;
+  if (a->vmc && !a->mu) return TOPT_EINVAL;
+  if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache)) return TOPT_EINVAL;
+  if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
+  if (decode_workspace_bytes(*a) > decode_noalloc_capacity()) return TOPT_EWORKSPACE;
+  return cuda_status(decode_noalloc_launch(*a, (cudaStream_t)stream));
+}
+
 // ----------------------------------------------------------------- prefill
 topt_status topt_prefill_workspace(const topt_prefill_args* a, size_t* bytes) {
   topt_status st = check_prefill_shape(a);

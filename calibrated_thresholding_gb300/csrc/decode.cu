@@ -33,6 +33,8 @@
 // Counters live at the start of the workspace; the last CTA to use one puts
 // it back to zero, so the workspace is ready for the next call without a
 // memset.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -785,7 +787,40 @@ cudaError_t launch_d(const DecodeParams& p, int G, const topt_decode_args& a, cu
   return cudaErrorInvalidValue;
 }
 
+// Fixed scratch for topt_decode_noalloc: one file-scope device array (every
+// GPU that loads the library holds it until exit).  Host code must not use the
+// symbol as a device address; the address comes from cudaGetSymbolAddress.
+constexpr size_t kNoAllocBytes = size_t(32) << 20;
+__device__ __align__(256) unsigned char g_decode_scratch[kNoAllocBytes];
+
 }  // namespace
+
+size_t decode_noalloc_capacity() { return kNoAllocBytes; }
+
+cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {  // once per device, with that device current
+      void* ptr = nullptr;
+      if ((e = cudaGetSymbolAddress(&ptr, g_decode_scratch)) != cudaSuccess) return e;
+      addr[dev] = ptr;
+    }
+    base = addr[dev];
+  }
+  // The array keeps the previous call's contents: the counters must start at 0.
+  if ((e = cudaMemsetAsync(base, 0, kCounterBytes, s)) != cudaSuccess) return e;
+  topt_decode_args b = a;
+  b.workspace = base;
+  b.workspace_bytes = kNoAllocBytes;
+  return decode_launch(b, s);
+}
 
 int decode_max_batch() { return kMaxBatch; }
 int decode_max_pairs() { return kMaxPairs; }

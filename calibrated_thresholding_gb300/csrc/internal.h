@@ -14,6 +14,8 @@ size_t decode_workspace_bytes(const topt_decode_args& a);
 int decode_max_batch();
 int decode_max_pairs();
 cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s);
+size_t decode_noalloc_capacity();
+cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s);
 
 // ----------------------------------------------------------------- prefill
 size_t prefill_workspace_bytes(const topt_prefill_args& a);

@@ -67,7 +67,7 @@ class VmeanArgs(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 
-SYMBOLS = ["topt_decode_workspace", "topt_decode", "topt_prefill_workspace",
+SYMBOLS = ["topt_decode_workspace", "topt_decode", "topt_decode_noalloc", "topt_prefill_workspace",
            "topt_prefill_tile_shape", "topt_prefill", "topt_calibrate_workspace",
            "topt_calibrate", "topt_select_kth", "topt_vmean_update", "topt_version",
            "topt_status_string"]
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             P = ctypes.POINTER
             L.topt_decode_workspace.argtypes = [P(DecodeArgs), P(sz)]
             L.topt_decode.argtypes = [P(DecodeArgs), vp]
+            L.topt_decode_noalloc.argtypes = [P(DecodeArgs), vp]
             L.topt_prefill_workspace.argtypes = [P(PrefillArgs), P(sz)]
             L.topt_prefill_tile_shape.argtypes = [P(PrefillArgs), P(i32), P(i32)]
             L.topt_prefill.argtypes = [P(PrefillArgs), vp]
@@ -204,6 +205,30 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
     a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
     a.workspace_bytes = workspace.numel()
     _check("topt_decode", lib().topt_decode(ctypes.byref(a), _stream(stream)))
+    return dict(out=out, kept=kept, vrows=vrows, mask=mask)
+
+
+def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
+                   gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
+                   stream=None):
+    """Top-theta decode through ``topt_decode_noalloc`` (library-held scratch).
+
+    For callers that must not allocate device scratch; see include/topt.h for
+    the limit and the rule that calls must not overlap.  Outputs that are not
+    given are allocated here with torch (the C entry point allocates nothing).
+    """
+    B, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Hq, d), device=dev, dtype=torch.float32)
+    if kept is None:
+        kept = torch.empty((B, Hq), device=dev, dtype=torch.int32)
+    if vrows is None:
+        vrows = torch.empty((B, Hkv), device=dev, dtype=torch.int32)
+    a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
+                    gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status)
+    _check("topt_decode_noalloc", lib().topt_decode_noalloc(ctypes.byref(a), _stream(stream)))
     return dict(out=out, kept=kept, vrows=vrows, mask=mask)
 
 

@@ -112,6 +112,24 @@ topt_status topt_decode_workspace(const topt_decode_args* args, size_t* bytes);
  * are written as 0. */
 topt_status topt_decode(const topt_decode_args* args, topt_stream stream);
 
+/* Same operation as topt_decode, for callers that cannot allocate device
+ * memory themselves (for example an application whose memory budget is fixed
+ * at start-up, or code embedded in a framework whose allocator owns all device
+ * memory).  This entry point has no counterpart in the paper; it only changes
+ * where the scratch memory comes from.
+ *   - args->workspace and args->workspace_bytes are ignored.  The scratch is
+ *     one 32 MiB array that the library holds in device memory of every GPU
+ *     that loads it, until the process exits.  Shapes that need more than
+ *     32 MiB (topt_decode_workspace) return TOPT_EWORKSPACE and launch nothing.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
+ *     call.  The first call on a device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.  Each call clears the array's counters on `stream` first.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (other streams, other threads) race and corrupt each other's
+ *     results.  Serialise them. */
+topt_status topt_decode_noalloc(const topt_decode_args* args, topt_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill: causal attention of S query rows; row i sees keys 0..i.         */
 /* [TopTheta §2.2 "prefill phase", §3, §3.2]                                 */
