@@ -47,17 +47,18 @@ constexpr int kTile = 16;                          // keys per MMA tile / bulk c
 constexpr int kUnit = 64;                          // keys per work unit and softmax partial
 constexpr int kStages = 2;                         // ring slots per warp
 constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
+constexpr int kGrab = 4;                           // consecutive units per queue request
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDevices = 64;
 
 // Keys per select slice: the CTA holds the slice's G x keys scores in
-// registers, at most 64 per thread and 32 groups of 32 keys per warp.
+// registers, at most 32 per thread.
 // V rows in flight per thread slot of the gather (register budget).
 template <int G>
-__host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 16 : (G <= 4 ? 10 : 6); }
+__host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 16 : (G <= 4 ? 8 : 6); }
 
 template <int G>
-__host__ __device__ constexpr int slice_keys() { return kThreads * (64 / G < 32 ? 64 / G : 32); }
+__host__ __device__ constexpr int slice_keys() { return kThreads * (32 / G > 0 ? 32 / G : 1); }
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -243,13 +244,20 @@ __device__ void phase_scores(const DecodeParams& p, ScoreSmem<D>& sm, int total)
   }
   __syncwarp();
 
-  // Unit queue: lane 0 keeps one request in flight.
+  // Unit queue: lane 0 keeps one request of kGrab consecutive units in
+  // flight (consecutive units mostly share a pair, so q is reloaded rarely).
   unsigned pending = 0;
-  if (lane == 0) pending = atomicAdd(&p.queues[0], 1u);
+  if (lane == 0) pending = atomicAdd(&p.queues[0], (unsigned)kGrab);
+  int grab = 0, grab_left = 0;
   auto take = [&]() -> int {
-    const int u = (int)__shfl_sync(0xffffffffu, pending, 0);
-    if (lane == 0 && u < total) pending = atomicAdd(&p.queues[0], 1u);
-    return u;
+    if (grab_left == 0) {
+      grab = (int)__shfl_sync(0xffffffffu, pending, 0);
+      grab_left = kGrab;
+      if (lane == 0 && grab < total) pending = atomicAdd(&p.queues[0], (unsigned)kGrab);
+    }
+    const int u = grab++;
+    --grab_left;
+    return u < total ? u : total;
   };
 
   // Producer: the unit being issued and its tile cursor.
@@ -679,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 6) decode_scores_kernel(const Decode
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 3) decode_select_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
   // Wait until the score kernel has finished and its writes are visible.
