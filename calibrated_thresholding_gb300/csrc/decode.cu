@@ -739,8 +739,15 @@ int slices_per_pair(int cache_len, int G) {
   return (cache_len + sk - 1) / sk;
 }
 
+// Profiling events; under stream capture they become timing nodes of the graph.
 cudaError_t record(void* ev, cudaStream_t s) {
-  return ev ? cudaEventRecord(static_cast<cudaEvent_t>(ev), s) : cudaSuccess;
+  if (!ev) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal)
+             : cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
 }
 
 template <int D, int G>
