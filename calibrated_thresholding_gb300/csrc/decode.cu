@@ -10,18 +10,19 @@
 // Two kernels per call, the second launched as a programmatic dependent of
 // the first (it is scheduled while the first drains and waits for its data):
 //
-//  decode_scores_kernel (persistent, as many CTAs as fit, ~85 registers so
-//   24 warps share each SM).  Every pair's valid keys form 64-key units,
-//   numbered pair after pair and handed to warps by an atomic counter (each
-//   warp asks one unit ahead, so the atomic's latency is hidden).  A warp
-//   streams its units' K rows through a private shared-memory ring with 1-D
-//   TMA bulk copies (cp.async.bulk, 4 KB = 16 keys per copy, L2 evict-first,
-//   completion on an mbarrier), computes each 16-key x G-head score block
-//   with m16n8k16 bf16 MMAs (keys on the M side, query heads on the N side),
-//   writes a = q K^T / sqrt(d) [Eq. 1] to an L2-resident workspace (G x 4
-//   bytes per key) and the unit's softmax partial (m, Z) per head.
+//  decode_scores_kernel (one resident wave, 4 warps per CTA).  Every pair's
+//   valid keys form 16-key tiles, numbered pair after pair; warp w of the W
+//   warps takes the contiguous tile range [T*w/W, T*(w+1)/W), so every warp
+//   streams the same number of bytes.  Each warp stages its tiles in a
+//   private shared-memory ring with cp.async (16 bytes per lane, 3 tiles in
+//   flight), computes each 16-key x G-head score block with m16n8k16 bf16
+//   MMAs (keys on the M side, query heads on the N side, one accumulator
+//   chain per 32-wide d slab), writes a = q K^T / sqrt(d) [Eq. 1] to an
+//   L2-resident workspace laid out [key][head] (one 8-byte store per lane and
+//   key), and keeps a running softmax partial (m, Z) per head that it writes
+//   once per run of tiles of one pair.
 //  decode_select_kernel (one CTA per (pair, slice)).  Loads the slice's
-//   scores into registers in one go while it merges the pair's (m, Z)
+//   scores (one vector load per key) while it merges the pair's (m, Z)
 //   partials, turns theta into a bound on the score (post-softmax:
 //   s >= theta <=> a >= m + ln theta + ln Z), ballots per-head masks of 32
 //   keys per warp, ORs them into the group union, compacts the union into a
@@ -30,9 +31,8 @@
 //   slice of a pair to finish (atomic ticket, nothing waits) combines the
 //   slices and applies SDC [Eq. 4] and VMC [Eq. 5-7].
 //
-// Counters live at the start of the workspace; the last CTA to use one puts
-// it back to zero, so the workspace is ready for the next call without a
-// memset.
+// The workspace starts with a block of counters; the last user of a counter
+// puts it back to zero, so a zero-filled workspace serves every later call.
 #include <mutex>
 
 #include "common.cuh"
@@ -43,22 +43,22 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * kWarp;
-constexpr int kTile = 16;                          // keys per MMA tile / bulk copy
-constexpr int kUnit = 64;                          // keys per work unit and softmax partial
-constexpr int kStages = 2;                         // ring slots per warp
-constexpr int kQueue = 8;                          // per-warp queue of taken units (>= kStages + 1)
-constexpr int kGrab = 4;                           // consecutive units per queue request
+constexpr int kTile = 16;                          // keys per MMA tile
+constexpr int kStages = 3;                         // cp.async ring slots per warp
 constexpr int kMaxBatch = 256;
 constexpr int kMaxDevices = 64;
 
-// Keys per select slice: the CTA holds the slice's G x keys scores in
-// registers, at most 32 per thread.
 // V rows in flight per thread slot of the gather (register budget).
 template <int G>
 __host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 16 : (G <= 4 ? 8 : 6); }
 
+// Keys per select slice: the CTA holds the slice's G x keys scores in
+// registers, at most 32 per thread.
 template <int G>
 __host__ __device__ constexpr int slice_keys() { return kThreads * (32 / G > 0 ? 32 / G : 1); }
+
+// Score columns per key in the workspace: G rounded up to even (8-byte stores).
+__host__ __device__ constexpr int score_cols(int G) { return G == 1 ? 1 : (G + 1) / 2 * 2; }
 
 struct DecodeParams {
   int B, Hq, Hkv, Nmax, Lmax, mode, sdc, vmc;
@@ -74,23 +74,23 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  int mask_words, upp, ipp, lstride;
+  int mask_words, spp, ipp, lstride, score_warps;
   // workspace
-  float* logits;      // [pairs][G][lstride]
-  float2* stats;      // [pairs][upp][G]
+  float* logits;      // [pairs][lstride][score_cols(G)]
+  float2* stats;      // [pairs][spp][G]: one partial per warp run, spp = tiles/pair + 1
   float* part_num;    // [pairs][ipp][G][D]
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
   int* part_nu;       // [pairs][ipp]
-  unsigned* queues;   // [2]: next unit, score CTAs finished      } zero between calls
-  unsigned* ticket;   // [pairs]: select slices finished          } (reset by their last user)
+  unsigned* ticket;   // [pairs]: select slices finished (zero between calls)
+  int* tstart;        // [B + 1]: first tile of each sequence, total (written each call)
 };
 
 // The workspace starts with a fixed-size block of counters, so a workspace
 // reused across shapes keeps them in one place: zero before the first call,
 // and every call leaves the ones it used at zero again.
 constexpr size_t kCounterBytes = 128 * 1024;
-constexpr int kMaxPairs = (int)(kCounterBytes / sizeof(unsigned) - 4);
+constexpr int kMaxPairs = (int)(kCounterBytes / sizeof(unsigned)) - 2 * (kMaxBatch + 1);
 
 struct DecodeLayout {
   size_t counters, logits, stats, part_num, part_r, part_kt, part_nu, total;
@@ -101,12 +101,12 @@ int logit_stride(int cache_len) { return (cache_len + 31) / 32 * 32; }
 DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
   const size_t pairs = (size_t)a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
-  const size_t upp = (a.cache_len + kUnit - 1) / kUnit;
+  const size_t spp = (a.cache_len + kTile - 1) / kTile + 1;
   DecodeLayout l;
   size_t off = 0;
   l.counters = off; off += kCounterBytes;
-  l.logits = off;   off += align256(pairs * G * (size_t)logit_stride(a.cache_len) * sizeof(float));
-  l.stats = off;    off += align256(pairs * upp * G * sizeof(float2));
+  l.logits = off;   off += align256(pairs * score_cols(G) * (size_t)logit_stride(a.cache_len) * sizeof(float));
+  l.stats = off;    off += align256(pairs * spp * G * sizeof(float2));
   l.part_num = off; off += align256(pairs * ipp * G * (size_t)a.head_dim * sizeof(float));
   l.part_r = off;   off += align256(pairs * ipp * G * sizeof(float));
   l.part_kt = off;  off += align256(pairs * ipp * G * sizeof(int));
@@ -119,41 +119,20 @@ DecodeLayout decode_layout(const topt_decode_args& a, int ipp) {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+// 16-byte async copy global -> shared; src_bytes = 0 fills zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, unsigned src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-  const uint32_t a = smem_u32(bar);
-  for (unsigned it = 0; it < (1u << 26); ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar,
-                                         uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-__device__ __forceinline__ float ld_cg_hint_f32(const float* p, uint64_t pol) {
-  float v;
-  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float2 ld_cg_f2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
   return v;
 }
+
 // Online (max, sum) update with two new scores (either may be -inf).
 __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) {
   const float mt = fmaxf(x0, x1);
@@ -162,17 +141,20 @@ __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) 
   z = z * __expf(m - mn) + __expf(x0 - mn) + __expf(x1 - mn);
   m = mn;
 }
+
+// Warp w's first tile in a split of T tiles over W warps, and the warp that
+// owns tile tau in that split.
+__device__ __forceinline__ int split_start(long T, long W, long w) { return (int)(T * w / W); }
+__device__ __forceinline__ int split_owner(long T, long W, long tau) { return (int)(((tau + 1) * W - 1) / T); }
+
 // ----------------------------------------------------------------------------
-// Shared memory: the score rings and the select lists share one buffer.
+// Shared memory
 // ----------------------------------------------------------------------------
 template <int D>
 struct ScoreSmem {
-  int ustart[kMaxBatch + 1];  // first unit of each sequence
-  int nunit[kMaxBatch];       // units per KV head of each sequence
-  int len[kMaxBatch];         // seq_len, staged once per CTA
-  int last;
-  uint64_t bar[kWarps][kStages];
-  int uq[kWarps][kQueue];     // units taken by each warp, in order
+  int tstart[kMaxBatch + 1];  // first tile of each sequence; [B] = total
+  int ntile[kMaxBatch];       // tiles per KV head of each sequence (0: invalid)
+  int len[kMaxBatch];
   __align__(128) unsigned char slot[kWarps][kStages][kTile * D * 2];
 };
 
@@ -189,28 +171,44 @@ struct SelectSmem {
   float m[kWarps][G], z[kWarps][G];
 };
 
-struct UnitRef {
-  int pair, b, kvh, unit, L;
+// Tile bookkeeping shared by the producer and consumer of a warp's run.
+struct TileCursor {
+  int b, kvh, tile, nt, L;
+  __device__ __forceinline__ int pair(int Hkv) const { return b * Hkv + kvh; }
 };
 
-// Global unit index -> (pair, unit within the pair).
 template <int D>
-__device__ __forceinline__ UnitRef unit_of(const ScoreSmem<D>& sm, int B, int Hkv, int u) {
-  int lo = 0, hi = B - 1;  // last b with ustart[b] <= u
+__device__ __forceinline__ TileCursor cursor_at(const ScoreSmem<D>& sm, int B, int Hkv, int tau) {
+  int lo = 0, hi = B - 1;  // last b with tstart[b] <= tau and tiles
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (sm.ustart[mid] <= u) lo = mid;
+    if (sm.tstart[mid] <= tau) lo = mid;
     else hi = mid - 1;
   }
-  UnitRef r;
-  r.b = lo;
-  const int nu = sm.nunit[lo];
-  const int rem = u - sm.ustart[lo];
-  r.kvh = rem / nu;
-  r.unit = rem - r.kvh * nu;
-  r.pair = lo * Hkv + r.kvh;
-  r.L = sm.len[lo];
-  return r;
+  while (lo < B - 1 && sm.ntile[lo] == 0) ++lo;  // sequences without tiles share tstart
+  TileCursor c;
+  c.b = lo;
+  c.nt = sm.ntile[lo];
+  const int rem = tau - sm.tstart[lo];
+  c.kvh = rem / c.nt;
+  c.tile = rem - c.kvh * c.nt;
+  c.L = sm.len[lo];
+  return c;
+}
+
+template <int D>
+__device__ __forceinline__ void cursor_next(const ScoreSmem<D>& sm, int B, int Hkv, TileCursor& c) {
+  if (++c.tile < c.nt) return;
+  c.tile = 0;
+  if (++c.kvh < Hkv) return;
+  c.kvh = 0;
+  do {
+    ++c.b;
+  } while (c.b < B && sm.ntile[c.b] == 0);
+  if (c.b < B) {
+    c.nt = sm.ntile[c.b];
+    c.L = sm.len[c.b];
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -225,83 +223,132 @@ __device__ __forceinline__ UnitRef unit_of(const ScoreSmem<D>& sm, int B, int Hk
 // 2t, 2t+1) and (key g+8, heads 2t, 2t+1).
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_scores(const DecodeParams& p, ScoreSmem<D>& sm, int total) {
+__global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const DecodeParams p) {
   constexpr int NP = D / 32;
+  constexpr int GC = score_cols(G);
   constexpr unsigned kTileBytes = kTile * D * 2;
+  constexpr int kChunks = kTileBytes / 16 / kWarp;  // 16-byte copies per lane per tile
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ScoreSmem<D>& sm = *reinterpret_cast<ScoreSmem<D>*>(smem_raw);
+  // The select kernel may be scheduled now; it waits for this grid's data.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // Tiles per sequence (every KV head of a sequence has the same length).
+  if (threadIdx.x < kWarp) {
+    const int lane = threadIdx.x;
+    const int per = (p.B + kWarp - 1) / kWarp;
+    int run = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = lane * per + i;
+      if (b < p.B) {
+        const int L = p.seq_len[b];
+        sm.len[b] = L;
+        int nt = 0;
+        if (L >= 1 && L <= p.Nmax) nt = (L + kTile - 1) / kTile;
+        else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
+        sm.ntile[b] = nt;
+        run += nt * p.Hkv;
+      }
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < kWarp; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int acc = incl - run;
+    for (int i = 0; i < per; ++i) {
+      const int b = lane * per + i;
+      if (b < p.B) {
+        sm.tstart[b] = acc;
+        acc += sm.ntile[b] * p.Hkv;
+      }
+    }
+    if (lane == kWarp - 1) sm.tstart[p.B] = incl;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)  // for the select kernel
+    for (int i = threadIdx.x; i <= p.B; i += kThreads) p.tstart[i] = sm.tstart[i];
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
+  const long T = sm.tstart[p.B];
+  const long W = (long)gridDim.x * kWarps;
+  const long gw = (long)blockIdx.x * kWarps + warp;
+  const int t_begin = split_start(T, W, gw);
+  const int t_end = split_start(T, W, gw + 1);
+  if (t_begin >= t_end) return;
 
-  uint64_t* bars = sm.bar[warp];
-  int* uq = sm.uq[warp];
-  unsigned char* slots = &sm.slot[warp][0][0];
-  const uint64_t pol = l2_evict_first_policy();
-  const uint64_t keep_pol = l2_evict_last_policy();
-  if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  unsigned char* ring = &sm.slot[warp][0][0];
+  const uint32_t ring_s = smem_u32(ring);
+  auto issue = [&](const TileCursor& c, int slot) {
+    const char* src = reinterpret_cast<const char*>(p.k + ((size_t)c.pair(p.Hkv) * p.Nmax + c.tile * kTile) * D);
+    const int rows = min(kTile, c.L - c.tile * kTile);
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+      const int off = (i * kWarp + lane) * 16;
+      const int row = off / (D * 2);
+      const bool ok = row < rows;
+      cp_async16(ring_s + slot * kTileBytes + off, src + (ok ? off : 0), ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+
+  // Prologue: kStages-1 tiles in flight.
+  TileCursor prod = cursor_at(sm, p.B, p.Hkv, t_begin);
+  int issued = t_begin;
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (issued < t_end) {
+      issue(prod, s);
+      cursor_next(sm, p.B, p.Hkv, prod);
+      ++issued;
+    } else {
+      cp_async_commit();
+    }
   }
-  __syncwarp();
-
-  // Unit queue: lane 0 keeps one request of kGrab consecutive units in
-  // flight (consecutive units mostly share a pair, so q is reloaded rarely).
-  unsigned pending = 0;
-  if (lane == 0) pending = atomicAdd(&p.queues[0], (unsigned)kGrab);
-  int grab = 0, grab_left = 0;
-  auto take = [&]() -> int {
-    if (grab_left == 0) {
-      grab = (int)__shfl_sync(0xffffffffu, pending, 0);
-      grab_left = kGrab;
-      if (lane == 0 && grab < total) pending = atomicAdd(&p.queues[0], (unsigned)kGrab);
-    }
-    const int u = grab++;
-    --grab_left;
-    return u < total ? u : total;
-  };
-
-  // Producer: the unit being issued and its tile cursor.
-  int pu = take(), pt = 0, pnt = 0, qh = 0, qt = 0;
-  UnitRef pr;
-  auto start_unit = [&]() {
-    pr = unit_of(sm, p.B, p.Hkv, pu);
-    pnt = (min(kUnit, pr.L - pr.unit * kUnit) + kTile - 1) / kTile;
-    if (lane == 0) uq[qh % kQueue] = pu;
-    ++qh;
-  };
-  if (pu < total) start_unit();
-  long issued = 0;
-  auto issue = [&]() {  // copy the producer's current tile into the next slot
-    const int key0 = pr.unit * kUnit + pt * kTile;
-    const unsigned bytes = (unsigned)min(kTile, pr.L - key0) * D * 2;
-    const int s = (int)(issued % kStages);
-    if (lane == 0) {
-      mbar_expect_tx(&bars[s], bytes);
-      bulk_g2s(slots + (size_t)s * kTileBytes, p.k + ((size_t)pr.pair * p.Nmax + key0) * D, bytes, &bars[s], pol);
-    }
-    ++issued;
-    if (++pt == pnt) {
-      pt = 0;
-      pu = take();
-      if (pu < total) start_unit();
-    }
-  };
-  while (pu < total && issued < kStages) issue();
-  __syncwarp();
 
   const float scale = p.sm_scale;
   const int h0 = 2 * t, h1 = 2 * t + 1;
+  TileCursor c = cursor_at(sm, p.B, p.Hkv, t_begin);
+  int cur_pair = -1;
+  int run_first = 0;  // first global tile of the current pair (for the stats slot)
   uint32_t qf[NP][4];
-  int qpair = -1;
-  long consumed = 0;
-  while (qt < qh) {
-    const UnitRef r = unit_of(sm, p.B, p.Hkv, uq[qt % kQueue]);
-    ++qt;
-    const int ntile = (min(kUnit, r.L - r.unit * kUnit) + kTile - 1) / kTile;
-    if (r.pair != qpair) {
-      qpair = r.pair;
+  float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
+  auto flush = [&](int pair) {  // this warp's partial of `pair`
+    ms_warp_merge(m0, z0, 4);
+    ms_warp_merge(m1, z1, 4);
+    if (g == 0) {
+      const int slot = (int)gw - split_owner(T, W, run_first);
+      float2* st = p.stats + ((size_t)pair * p.spp + slot) * G;
+      if (h0 < G) st[h0] = make_float2(m0, z0);
+      if (h1 < G) st[h1] = make_float2(m1, z1);
+    }
+    m0 = -CUDART_INF_F;
+    z0 = 0.f;
+    m1 = -CUDART_INF_F;
+    z1 = 0.f;
+  };
+
+  int slot = 0;
+  for (int tau = t_begin; tau < t_end; ++tau) {
+    // Keep kStages-1 copies ahead: refill the slot consumed last iteration.
+    if (issued < t_end) {
+      issue(prod, (slot + kStages - 1) % kStages);
+      cursor_next(sm, p.B, p.Hkv, prod);
+      ++issued;
+    } else {
+      cp_async_commit();
+    }
+    const int pair = c.pair(p.Hkv);
+    if (pair != cur_pair) {
+      if (cur_pair >= 0) flush(cur_pair);
+      cur_pair = pair;
+      run_first = sm.tstart[c.b] + c.kvh * c.nt;
       if (g < G) {
-        const __nv_bfloat16* qrow = p.q + ((size_t)r.b * p.Hq + r.kvh * G + g) * D;
+        const __nv_bfloat16* qrow = p.q + ((size_t)c.b * p.Hq + c.kvh * G + g) * D;
 #pragma unroll
         for (int pp = 0; pp < NP; ++pp) {
           const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * pp + 8 * t);
@@ -312,132 +359,137 @@ __device__ void phase_scores(const DecodeParams& p, ScoreSmem<D>& sm, int total)
         for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
       }
     }
-    float* lrow = p.logits + (size_t)r.pair * G * p.lstride;
-    const int L = r.L;
-    float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
-    for (int tt = 0; tt < ntile; ++tt) {
-      const int s = (int)(consumed % kStages);
-      const unsigned parity = (unsigned)((consumed / kStages) & 1);
-      if (!mbar_wait(&bars[s], parity)) set_status(p.status, TOPT_ETIMEOUT);
-      const unsigned char* tile = slots + (size_t)s * kTileBytes;
-      uint4 ka[NP], kb[NP];
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const unsigned char* tb = ring + slot * kTileBytes;
+    uint4 ka[NP], kb[NP];
 #pragma unroll
-      for (int pp = 0; pp < NP; ++pp) {
-        ka[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)g * D * 2 + (32 * pp + 8 * t) * 2);
-        kb[pp] = *reinterpret_cast<const uint4*>(tile + (size_t)(g + 8) * D * 2 + (32 * pp + 8 * t) * 2);
-      }
-      // One accumulator per slab: NP independent MMA chains of two.
-      float cs[NP][4];
+    for (int pp = 0; pp < NP; ++pp) {
+      ka[pp] = *reinterpret_cast<const uint4*>(tb + (size_t)g * D * 2 + (32 * pp + 8 * t) * 2);
+      kb[pp] = *reinterpret_cast<const uint4*>(tb + (size_t)(g + 8) * D * 2 + (32 * pp + 8 * t) * 2);
+    }
+    __syncwarp();  // the slot may be refilled from here on
+    float cs[NP][4];
 #pragma unroll
-      for (int pp = 0; pp < NP; ++pp) {
-        cs[pp][0] = cs[pp][1] = cs[pp][2] = cs[pp][3] = 0.f;
-        const uint32_t wa[4] = {ka[pp].x, ka[pp].y, ka[pp].z, ka[pp].w};
-        const uint32_t wb[4] = {kb[pp].x, kb[pp].y, kb[pp].z, kb[pp].w};
+    for (int pp = 0; pp < NP; ++pp) {
+      cs[pp][0] = cs[pp][1] = cs[pp][2] = cs[pp][3] = 0.f;
+      const uint32_t wa[4] = {ka[pp].x, ka[pp].y, ka[pp].z, ka[pp].w};
+      const uint32_t wb[4] = {kb[pp].x, kb[pp].y, kb[pp].z, kb[pp].w};
 #pragma unroll
-        for (int ss = 0; ss < 2; ++ss) {
-          const uint32_t af[4] = {wa[2 * ss], wb[2 * ss], wa[2 * ss + 1], wb[2 * ss + 1]};
-          const uint32_t bf[2] = {qf[pp][2 * ss], qf[pp][2 * ss + 1]};
-          mma_16816_bf16(cs[pp], af, bf);
-        }
-      }
-      ++consumed;
-      // Every lane's shared-memory reads of the slot have completed (their
-      // values fed the MMAs above); refill the slot.
-      __syncwarp();
-      if (pu < total) issue();
-      float cc[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = cs[0][e];
-#pragma unroll
-        for (int pp = 1; pp < NP; ++pp) v += cs[pp][e];
-        cc[e] = v;
-      }
-      const int key0 = r.unit * kUnit + tt * kTile;
-      const int j0 = key0 + g;
-      const int j1 = key0 + g + 8;
-      const float a00 = j0 < L ? cc[0] * scale : -CUDART_INF_F;
-      const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
-      const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
-      const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
-      if (h0 < G) {
-        if (j0 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j0, a00, keep_pol);
-        if (j1 < L) st_hint_f32(lrow + (size_t)h0 * p.lstride + j1, a10, keep_pol);
-        ms_add2(m0, z0, a00, a10);
-      }
-      if (h1 < G) {
-        if (j0 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j0, a01, keep_pol);
-        if (j1 < L) st_hint_f32(lrow + (size_t)h1 * p.lstride + j1, a11, keep_pol);
-        ms_add2(m1, z1, a01, a11);
+      for (int ss = 0; ss < 2; ++ss) {
+        const uint32_t af[4] = {wa[2 * ss], wb[2 * ss], wa[2 * ss + 1], wb[2 * ss + 1]};
+        const uint32_t bf[2] = {qf[pp][2 * ss], qf[pp][2 * ss + 1]};
+        mma_16816_bf16(cs[pp], af, bf);
       }
     }
-    // Partial of this unit: merge over the 8 key rows (lane bits 2..4).
-    ms_warp_merge(m0, z0, 4);
-    ms_warp_merge(m1, z1, 4);
-    if (g == 0) {
-      float2* st = p.stats + ((size_t)r.pair * p.upp + r.unit) * G;
-      if (h0 < G) st[h0] = make_float2(m0, z0);
-      if (h1 < G) st[h1] = make_float2(m1, z1);
+    float cc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = cs[0][e];
+#pragma unroll
+      for (int pp = 1; pp < NP; ++pp) v += cs[pp][e];
+      cc[e] = v;
     }
+    const int key0 = c.tile * kTile;
+    const int j0 = key0 + g;
+    const int j1 = key0 + g + 8;
+    const int L = c.L;
+    const float a00 = j0 < L ? cc[0] * scale : -CUDART_INF_F;
+    const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
+    const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
+    const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
+    float* lrow = p.logits + (size_t)pair * p.lstride * GC;
+    if (G == 1) {
+      if (t == 0) {
+        if (j0 < L) lrow[j0] = a00;
+        if (j1 < L) lrow[j1] = a10;
+      }
+    } else if (h0 < G) {
+      if (j0 < L) *reinterpret_cast<float2*>(lrow + (size_t)j0 * GC + h0) = make_float2(a00, a01);
+      if (j1 < L) *reinterpret_cast<float2*>(lrow + (size_t)j1 * GC + h0) = make_float2(a10, a11);
+    }
+    if (h0 < G) ms_add2(m0, z0, a00, a10);
+    if (h1 < G) ms_add2(m1, z1, a01, a11);
+    cursor_next(sm, p.B, p.Hkv, c);
+    slot = (slot + 1) % kStages;
   }
-  // Every issued copy has been waited for; retire the barriers.
-  __syncwarp();
-  if (lane == 0)
-    for (int s = 0; s < kStages; ++s)
-      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[s])) : "memory");
-  __syncwarp();
+  flush(cur_pair);
+  cp_async_wait<0>();
 }
 
 // ----------------------------------------------------------------------------
-// Select: one slice of one pair per item.
+// Select: one slice of one pair per CTA.
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int item) {
+__global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const DecodeParams p) {
   constexpr int LPR = D / 8;              // lanes per V row (16 bytes each)
   constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
+  constexpr int GC = score_cols(G);
   constexpr int kGatherUnroll = gather_unroll<G>();
-  SelectSmem<D, G>& ls = sm;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
+  const int item = blockIdx.x;
   const int pair = item / p.ipp;
   const int slice = item - pair * p.ipp;
   const int b = pair / p.Hkv;
   const int kvh = pair - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Inputs of the call can be read before the score kernel has finished.
   const int L = p.seq_len[b];
+  float th_pre = 0.f;
+  if (L >= 1 && L <= p.Nmax && threadIdx.x < G)
+    th_pre = p.theta[(size_t)(kvh * G + threadIdx.x) * p.Lmax + (min(L, p.Lmax) - 1)];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (L < 1 || L > p.Nmax) return;  // reported by the score kernel
-  const int nu = (L + kUnit - 1) / kUnit;
 
-  // The slice's scores, all loads in flight at once: group gi of warp w is
-  // keys s0 + gi*128 + w*32 + lane.
+  // The slice's scores, one vector load per key: group gi of warp w is keys
+  // s0 + gi*128 + w*32 + lane.
   const int s0 = slice * SK;
-  const float* lrow = p.logits + (size_t)pair * G * p.lstride;
-  const uint64_t pol = l2_evict_first_policy();
+  const float* lrow = p.logits + (size_t)pair * p.lstride * GC;
   float wv[NGRP][G];
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
     const int j = s0 + gi * kThreads + warp * kWarp + lane;
+    if (j < L) {
+      if (G == 1) {
+        wv[gi][0] = __ldcg(lrow + j);
+      } else {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-      wv[gi][h] = j < L ? ld_cg_hint_f32(lrow + (size_t)h * p.lstride + j, pol) : -CUDART_INF_F;
+        for (int h = 0; h < G; h += 2) {
+          const float2 v = ld_cg_f2(lrow + (size_t)j * GC + h);
+          wv[gi][h] = v.x;
+          if (h + 1 < G) wv[gi][h + 1] = v.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) wv[gi][h] = -CUDART_INF_F;
+    }
   }
 
-  // Softmax statistics of the whole row, per head, from the unit partials
-  // (the thresholds are fetched alongside).
-  float th_pre = 0.f;
-  if (threadIdx.x < G) th_pre = p.theta[(size_t)(kvh * G + threadIdx.x) * p.Lmax + (min(L, p.Lmax) - 1)];
+  // Softmax statistics of the whole row, per head, from the warp partials.
   {
+    const long T = p.tstart[p.B];
+    const long W = p.score_warps;
+    const int nt = (L + kTile - 1) / kTile;
+    const long first = p.tstart[b] + (long)kvh * nt;
+    const int w_first = split_owner(T, W, first);
+    const int nslots = split_owner(T, W, first + nt - 1) - w_first + 1;
     float m[G], z[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m[h] = -CUDART_INF_F;
       z[h] = 0.f;
     }
-    for (int c = threadIdx.x; c < nu; c += kThreads) {
+    for (int c = threadIdx.x; c < nslots; c += kThreads) {
+      // warps with an empty range (more warps than tiles) wrote no partial
+      if (split_start(T, W, w_first + c) == split_start(T, W, w_first + c + 1)) continue;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float2 v = __ldcg(p.stats + ((size_t)pair * p.upp + c) * G + h);
+        const float2 v = __ldcg(p.stats + ((size_t)pair * p.spp + c) * G + h);
         ms_merge(m[h], z[h], v.x, v.y);
       }
     }
@@ -445,8 +497,8 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
     for (int h = 0; h < G; ++h) {
       ms_warp_merge(m[h], z[h], 1);
       if (lane == 0) {
-        ls.m[warp][h] = m[h];
-        ls.z[warp][h] = z[h];
+        sm.m[warp][h] = m[h];
+        sm.z[warp][h] = z[h];
       }
     }
     __syncthreads();
@@ -454,12 +506,11 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
       const int h = threadIdx.x;
       float mm = -CUDART_INF_F, zz = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) ms_merge(mm, zz, ls.m[w][h], ls.z[w][h]);
-      const float th = th_pre;
+      for (int w = 0; w < kWarps; ++w) ms_merge(mm, zz, sm.m[w][h], sm.z[w][h]);
       sm.M[h] = mm;
       sm.Z[h] = zz;
-      sm.th[h] = th;
-      sm.T[h] = score_bound(p.mode, th, mm, zz);
+      sm.th[h] = th_pre;
+      sm.T[h] = score_bound(p.mode, th_pre, mm, zz);
     }
     __syncthreads();
   }
@@ -494,21 +545,21 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
     uni[gi] = un;
     wcount += __popc(un);
   }
-  if (lane == 0) ls.cnt[warp] = wcount;
+  if (lane == 0) sm.cnt[warp] = wcount;
   __syncthreads();
   int base = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    base += (w < warp) ? ls.cnt[w] : 0;
-    total += ls.cnt[w];
+    base += (w < warp) ? sm.cnt[w] : 0;
+    total += sm.cnt[w];
   }
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
     if ((uni[gi] >> lane) & 1u) {
       const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
-      ls.j[pos] = s0 + gi * kThreads + warp * kWarp + lane;
+      sm.j[pos] = s0 + gi * kThreads + warp * kWarp + lane;
 #pragma unroll
-      for (int h = 0; h < G; ++h) ls.w[pos][h] = wv[gi][h];
+      for (int h = 0; h < G; ++h) sm.w[pos][h] = wv[gi][h];
     }
     base += __popc(uni[gi]);
   }
@@ -528,7 +579,7 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
       const int r = r0 + u * SLOTS + slot;
-      if (r < total) vv[u] = ld_nc16(vbase + (size_t)ls.j[r] * D);
+      if (r < total) vv[u] = ld_nc16(vbase + (size_t)sm.j[r] * D);
     }
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
@@ -538,7 +589,7 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
                              bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float wh = ls.w[r][h];
+          const float wh = sm.w[r][h];
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
         }
@@ -560,13 +611,13 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ls.acc[warp][h][dl * 8 + e] = acc[h][e];
+      for (int e = 0; e < 8; ++e) sm.acc[warp][h][dl * 8 + e] = acc[h][e];
   }
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      ls.r[warp][h] = Rl[h];
-      ls.kt[warp][h] = kt[h];
+      sm.r[warp][h] = Rl[h];
+      sm.kt[warp][h] = kt[h];
     }
   }
   __syncthreads();
@@ -576,7 +627,7 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += ls.acc[w][idx / D][idx % D];
+      for (int w = 0; w < kWarps; ++w) s += sm.acc[w][idx / D][idx % D];
       p.part_num[pc * G * D + idx] = s;
     }
   }
@@ -585,8 +636,8 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
     int k = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      r += ls.r[w][threadIdx.x];
-      k += ls.kt[w][threadIdx.x];
+      r += sm.r[w][threadIdx.x];
+      k += sm.kt[w][threadIdx.x];
     }
     p.part_r[pc * G + threadIdx.x] = r;
     p.part_kt[pc * G + threadIdx.x] = k;
@@ -630,73 +681,8 @@ __device__ void phase_select(const DecodeParams& p, SelectSmem<D, G>& sm, int it
   }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 6) decode_scores_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  ScoreSmem<D>& sm = *reinterpret_cast<ScoreSmem<D>*>(smem_raw);
-  // The select kernel may be scheduled now; it waits for this grid's data.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // Units per sequence (every KV head of a sequence has the same length).
-  if (threadIdx.x < kWarp) {
-    const int lane = threadIdx.x;
-    const int per = (p.B + kWarp - 1) / kWarp;
-    int run = 0;
-    for (int i = 0; i < per; ++i) {
-      const int b = lane * per + i;
-      if (b < p.B) {
-        const int L = p.seq_len[b];
-        sm.len[b] = L;
-        int nu = 0;
-        if (L >= 1 && L <= p.Nmax) nu = (L + kUnit - 1) / kUnit;
-        else if (blockIdx.x == 0) set_status(p.status, TOPT_EINVAL);
-        sm.nunit[b] = nu > 0 ? nu : 1;
-        run += nu * p.Hkv;
-      }
-    }
-    int incl = run;
-#pragma unroll
-    for (int off = 1; off < kWarp; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    int acc = incl - run;
-    for (int i = 0; i < per; ++i) {
-      const int b = lane * per + i;
-      if (b < p.B) {
-        sm.ustart[b] = acc;
-        const int L = sm.len[b];
-        if (L >= 1 && L <= p.Nmax) acc += ((L + kUnit - 1) / kUnit) * p.Hkv;
-      }
-    }
-    if (lane == kWarp - 1) sm.ustart[p.B] = incl;
-  }
-  __syncthreads();
-
-  phase_scores<D, G>(p, sm, sm.ustart[p.B]);
-
-  // The last CTA out leaves the unit queue zeroed for the next call.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&p.queues[1], 1u) == gridDim.x - 1u) {
-      p.queues[0] = 0u;
-      p.queues[1] = 0u;
-    }
-  }
-}
-
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
-  // Wait until the score kernel has finished and its writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  phase_select<D, G>(p, sm, blockIdx.x);
-}
-
-// Resident CTAs of the persistent score grid, per device and instantiation
-// (also sets both kernels' shared-memory limits once).
+// Resident CTAs of the score grid, per device and instantiation (also sets
+// both kernels' shared-memory limits once).
 template <int D, int G>
 cudaError_t grid_of(int& grid) {
   static int cached[kMaxDevices] = {};
@@ -757,6 +743,7 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   if ((e = grid_of<D, G>(grid)) != cudaSuccess) return e;
   const int pairs = p.B * p.Hkv;
   p.ipp = slices_per_pair(p.Nmax, G);
+  p.score_warps = grid * kWarps;
   const DecodeLayout l = decode_layout(a, p.ipp);
   if (a.workspace_bytes < l.total) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.workspace);
@@ -767,8 +754,8 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   p.part_kt = reinterpret_cast<int*>(ws + l.part_kt);
   p.part_nu = reinterpret_cast<int*>(ws + l.part_nu);
   unsigned* counters = reinterpret_cast<unsigned*>(ws + l.counters);
-  p.queues = counters;
-  p.ticket = counters + 4;
+  p.tstart = reinterpret_cast<int*>(counters);
+  p.ticket = counters + 2 * (kMaxBatch + 1);
   if ((e = record(a.events[0], s)) != cudaSuccess) return e;
   decode_scores_kernel<D, G><<<grid, kThreads, sizeof(ScoreSmem<D>), s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -870,9 +857,10 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.status = a.status;
   p.mask_words = (a.cache_len + 31) / 32;
-  p.upp = (a.cache_len + kUnit - 1) / kUnit;
+  p.spp = (a.cache_len + kTile - 1) / kTile + 1;
   p.lstride = logit_stride(a.cache_len);
   p.ipp = 1;
+  p.score_warps = 1;
   const int G = a.n_q_heads / a.n_kv_heads;
   if (a.head_dim == 128) return launch_d<128>(p, G, a, s);
   if (a.head_dim == 64) return launch_d<64>(p, G, a, s);
