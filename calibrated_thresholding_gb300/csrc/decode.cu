@@ -77,7 +77,7 @@ struct DecodeParams {
   int mask_words, spp, ipp, lstride, score_warps;
   // workspace
   float* logits;      // [pairs][lstride][score_cols(G)]
-  float2* stats;      // [pairs][spp][G]: one partial per warp run, spp = tiles/pair + 1
+  float2* stats;      // [pairs][spp][G]: a warp run's partial at the run's first tile
   float* part_num;    // [pairs][ipp][G][D]
   float* part_r;      // [pairs][ipp][G]
   int* part_kt;       // [pairs][ipp][G]
@@ -314,15 +314,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
   const int h0 = 2 * t, h1 = 2 * t + 1;
   TileCursor c = cursor_at(sm, p.B, p.Hkv, t_begin);
   int cur_pair = -1;
-  int run_first = 0;  // first global tile of the current pair (for the stats slot)
+  int run_first = 0;  // first global tile of the current pair
+  int run_slot = 0;   // this warp's first tile of that pair, relative to run_first
   uint32_t qf[NP][4];
   float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
   auto flush = [&](int pair) {  // this warp's partial of `pair`
     ms_warp_merge(m0, z0, 4);
     ms_warp_merge(m1, z1, 4);
     if (g == 0) {
-      const int slot = (int)gw - split_owner(T, W, run_first);
-      float2* st = p.stats + ((size_t)pair * p.spp + slot) * G;
+      float2* st = p.stats + ((size_t)pair * p.spp + run_slot) * G;
       if (h0 < G) st[h0] = make_float2(m0, z0);
       if (h1 < G) st[h1] = make_float2(m1, z1);
     }
@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
       if (cur_pair >= 0) flush(cur_pair);
       cur_pair = pair;
       run_first = sm.tstart[c.b] + c.kvh * c.nt;
+      run_slot = tau - run_first;  // this warp's run of the pair starts at tau
       if (g < G) {
         const __nv_bfloat16* qrow = p.q + ((size_t)c.b * p.Hq + c.kvh * G + g) * D;
 #pragma unroll
@@ -485,11 +486,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
       z[h] = 0.f;
     }
     for (int c = threadIdx.x; c < nslots; c += kThreads) {
-      // warps with an empty range (more warps than tiles) wrote no partial
-      if (split_start(T, W, w_first + c) == split_start(T, W, w_first + c + 1)) continue;
+      // each warp covering the pair wrote one partial at its run's first tile;
+      // warps with an empty range (more warps than tiles) wrote none
+      const long ws = split_start(T, W, w_first + c);
+      if (ws == split_start(T, W, w_first + c + 1)) continue;
+      const int slot = (int)((ws > first ? ws : first) - first);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float2 v = __ldcg(p.stats + ((size_t)pair * p.spp + c) * G + h);
+        const float2 v = __ldcg(p.stats + ((size_t)pair * p.spp + slot) * G + h);
         ms_merge(m[h], z[h], v.x, v.y);
       }
     }
