@@ -50,10 +50,9 @@ constexpr int kMaxDevices = 64;
 
 // V rows in flight per thread slot of the gather (register budget).
 template <int G>
-__host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 16 : (G <= 4 ? 8 : 6); }
+__host__ __device__ constexpr int gather_unroll() { return G <= 4 ? 8 : 4; }
 
-// Keys per select slice: the CTA holds the slice's G x keys scores in
-// registers, at most 32 per thread.
+// Keys per select slice: 32 x 128 / G scores (16 KB) staged per CTA.
 template <int G>
 __host__ __device__ constexpr int slice_keys() { return kThreads * (32 / G > 0 ? 32 / G : 1); }
 
@@ -127,12 +126,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ float2 ld_cg_f2(const float* p) {
-  float2 v;
-  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-  return v;
-}
-
 // Online (max, sum) update with two new scores (either may be -inf).
 __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) {
   const float mt = fmaxf(x0, x1);
@@ -162,13 +155,15 @@ template <int D, int G>
 struct SelectSmem {
   float M[G], Z[G], T[G], th[G];
   int last;
-  int j[slice_keys<G>()];       // union keys of the slice
-  float w[slice_keys<G>()][G];  // exp(a - m) per head (0 if the head drops the key)
-  float acc[kWarps][G][D];
-  float r[kWarps][G];
-  int kt[kWarps][G];
   int cnt[kWarps];
   float m[kWarps][G], z[kWarps][G];
+  float r[kWarps][G];
+  int kt[kWarps][G];
+  int j[slice_keys<G>()];  // union keys of the slice
+  union {
+    alignas(16) float sc[slice_keys<G>() * score_cols(G)];  // the slice's scores, [key][column]
+    float acc[kWarps][G][D];                    // per-warp sums, after the gather
+  } u;
 };
 
 // Tile bookkeeping shared by the producer and consumer of a warp's run.
@@ -422,13 +417,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
 // Select: one slice of one pair per CTA.
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const DecodeParams p) {
-  constexpr int LPR = D / 8;              // lanes per V row (16 bytes each)
-  constexpr int SLOTS = kThreads / LPR;   // V rows per CTA instruction
+__global__ void __launch_bounds__(kThreads, 8) decode_select_kernel(const DecodeParams p) {
+  constexpr int DPL = D / kWarp;          // d values per lane in the gather (whole warp per V row)
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
   constexpr int GC = score_cols(G);
   constexpr int kGatherUnroll = gather_unroll<G>();
+  constexpr int kChunks = SK * GC * 4 / 16;  // 16-byte copies of the slice's scores
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
   const int item = blockIdx.x;
@@ -446,29 +441,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (L < 1 || L > p.Nmax) return;  // reported by the score kernel
 
-  // The slice's scores, one vector load per key: group gi of warp w is keys
-  // s0 + gi*128 + w*32 + lane.
+  // Stage the slice's scores in shared memory (keys beyond the stride are
+  // never copied; keys beyond L are ignored below).
   const int s0 = slice * SK;
-  const float* lrow = p.logits + (size_t)pair * p.lstride * GC;
-  float wv[NGRP][G];
-#pragma unroll
-  for (int gi = 0; gi < NGRP; ++gi) {
-    const int j = s0 + gi * kThreads + warp * kWarp + lane;
-    if (j < L) {
-      if (G == 1) {
-        wv[gi][0] = __ldcg(lrow + j);
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; h += 2) {
-          const float2 v = ld_cg_f2(lrow + (size_t)j * GC + h);
-          wv[gi][h] = v.x;
-          if (h + 1 < G) wv[gi][h + 1] = v.y;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) wv[gi][h] = -CUDART_INF_F;
-    }
+  {
+    const char* src = reinterpret_cast<const char*>(p.logits + ((size_t)pair * p.lstride + s0) * GC);
+    const int limit = (min(s0 + SK, p.lstride) - s0) * GC * 4;  // bytes inside the pair's row
+    const uint32_t dst = smem_u32(sm.u.sc);
+    for (int i = threadIdx.x; i < kChunks; i += kThreads)
+      if (i * 16 < limit) cp_async16(dst + i * 16, src + i * 16, 16u);
+    cp_async_commit();
   }
 
   // Softmax statistics of the whole row, per head, from the warp partials.
@@ -505,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
         sm.z[warp][h] = z[h];
       }
     }
+    cp_async_wait<0>();
     __syncthreads();
     if (threadIdx.x < G) {
       const int h = threadIdx.x;
@@ -518,8 +501,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
     }
     __syncthreads();
   }
+  float T[G], M[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    T[h] = sm.T[h];
+    M[h] = sm.M[h];
+  }
 
-  // Thresholds, masks and the union of the group.
+  // Thresholds, masks and the union of the group: group gi of warp w is keys
+  // s0 + gi*128 + w*32 + lane.
   uint32_t* mrow = p.mask ? p.mask + ((size_t)b * p.Hq + kvh * G) * p.mask_words : nullptr;
   float Rl[G];
   int kt[G];
@@ -532,15 +522,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
   int wcount = 0;
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
+    const int jl = gi * kThreads + warp * kWarp + lane;  // key within the slice
     const int j0 = s0 + gi * kThreads + warp * kWarp;
-    const bool valid = j0 + lane < L;
+    const bool valid = s0 + jl < L;
     unsigned un = 0u;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float a = wv[gi][h];
-      const bool keep = valid && (a >= sm.T[h]);
-      wv[gi][h] = keep ? __expf(a - sm.M[h]) : 0.f;
-      Rl[h] += wv[gi][h];
+      const float a = valid ? sm.u.sc[jl * GC + h] : -CUDART_INF_F;
+      const bool keep = valid && (a >= T[h]);
+      Rl[h] += keep ? __expf(a - M[h]) : 0.f;
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
       kt[h] += __popc(bal);
       un |= bal;
@@ -559,64 +549,58 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
   }
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
-    if ((uni[gi] >> lane) & 1u) {
-      const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
-      sm.j[pos] = s0 + gi * kThreads + warp * kWarp + lane;
-#pragma unroll
-      for (int h = 0; h < G; ++h) sm.w[pos][h] = wv[gi][h];
-    }
+    if ((uni[gi] >> lane) & 1u) sm.j[base + __popc(uni[gi] & ((1u << lane) - 1u))] = gi * kThreads + warp * kWarp + lane;
     base += __popc(uni[gi]);
   }
   __syncthreads();
 
-  // Gather the union's V rows.
-  const int slot = threadIdx.x / LPR;
-  const int dl = threadIdx.x % LPR;
-  const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * 8;
-  float acc[G][8];
+  // Gather the union's V rows, one row per warp instruction (DPL d values per
+  // lane); a row's weights are recomputed from the staged scores exactly as
+  // R was above.
+  const __nv_bfloat16* vbase = p.v + ((size_t)pair * p.Nmax + s0) * D + lane * DPL;
+  float acc[G][DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-  for (int r0 = 0; r0 < total; r0 += SLOTS * kGatherUnroll) {
-    uint4 vv[kGatherUnroll];
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+  for (int r0 = warp; r0 < total; r0 += kWarps * kGatherUnroll) {
+    uint2 vv[kGatherUnroll];
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * SLOTS + slot;
-      if (r < total) vv[u] = ld_nc16(vbase + (size_t)sm.j[r] * D);
+      const int r = r0 + u * kWarps;
+      if (r < total) {
+        const __nv_bfloat16* src = vbase + (size_t)sm.j[r] * D;
+        if (DPL == 4) {
+          vv[u] = __ldg(reinterpret_cast<const uint2*>(src));
+        } else {
+          vv[u].x = __ldg(reinterpret_cast<const unsigned*>(src));
+          vv[u].y = 0u;
+        }
+      }
     }
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * SLOTS + slot;
+      const int r = r0 + u * kWarps;
       if (r < total) {
-        const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
-                             bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
+        const int jl = sm.j[r];
+        const float vf[4] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y)};
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float wh = sm.w[r][h];
+          const float a = sm.u.sc[jl * GC + h];
+          const float wh = (a >= T[h]) ? __expf(a - M[h]) : 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
+          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
         }
       }
     }
   }
-
-  // Reduce over the rows of a warp instruction, then over warps.
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < G; ++h) Rl[h] = warp_sum(Rl[h]);
+  __syncthreads();  // the staged scores are no longer read: acc may reuse them
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
+  for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int off = LPR; off < kWarp; off <<= 1) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], off);
-    }
-    Rl[h] = warp_sum(Rl[h]);
-  }
-  if (lane < LPR) {
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm.acc[warp][h][dl * 8 + e] = acc[h][e];
-  }
+    for (int e = 0; e < DPL; ++e) sm.u.acc[warp][h][lane * DPL + e] = acc[h][e];
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -631,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_select_kernel(const Decode
     for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += sm.acc[w][idx / D][idx % D];
+      for (int w = 0; w < kWarps; ++w) s += sm.u.acc[w][idx / D][idx % D];
       p.part_num[pc * G * D + idx] = s;
     }
   }
