@@ -419,24 +419,33 @@ def main():
                     e.record(stream)
         handles = [[[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in s_] for s_ in ev]
     else:
-        # One step captured as a CUDA graph; the decode call records its events
-        # as timing nodes, so every replay re-times the step's kernels.
-        ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
-        for l_ in ev1:
-            for e in l_:
-                e.record(stream)
-        torch.cuda.synchronize(dev)
-        h1 = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in ev1]
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(graph, stream=cap):
-            state.run_step(L, ctypes.c_void_p(cap.cuda_stream), h1)
-        state.clear_events()
-        stream.wait_stream(cap)
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize(dev)
+        # One step captured as a CUDA graph, twice: `graph` times the whole
+        # decode call of every layer (events before the score kernel and after
+        # the select kernel, which leave the two kernels' overlap intact);
+        # `graph_split` adds an event between them to time the score kernel.
+        def capture(with_split):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+            for l_ in evs:
+                for e in l_:
+                    e.record(stream)
+            torch.cuda.synchronize(dev)
+            hs = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in evs]
+            if not with_split:
+                for l_ in hs:
+                    l_[1] = None
+            gr = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(gr, stream=cap):
+                state.run_step(L, ctypes.c_void_p(cap.cuda_stream), hs)
+            state.clear_events()
+            stream.wait_stream(cap)
+            for _ in range(3):
+                gr.replay()
+            torch.cuda.synchronize(dev)
+            return gr, evs
+        graph, ev1 = capture(False)
+        graph_split, ev_split = capture(True)
     barrier()
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -462,9 +471,15 @@ def main():
     if args.eager:
         score_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
         kern_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][2]) for s_ in range(args.steps) for l_ in range(layers)]
-    else:  # the last replay of the timed region
-        score_ms = [ev1[l_][0].elapsed_time(ev1[l_][1]) for l_ in range(layers)]
+    else:
+        # whole calls: the last replay of the timed region; score kernel: a
+        # short run of the split graph right after it
         kern_ms = [ev1[l_][0].elapsed_time(ev1[l_][2]) for l_ in range(layers)]
+        score_ms = []
+        for _ in range(max(5, args.steps // 20)):
+            graph_split.replay()
+            torch.cuda.synchronize(dev)
+            score_ms += [ev_split[l_][0].elapsed_time(ev_split[l_][1]) for l_ in range(layers)]
     ms_per_step = ms / args.steps
     tokens = wl.B * args.steps * world
     value = tokens / (ms / 1e3)
