@@ -50,11 +50,12 @@ constexpr int kMaxDevices = 64;
 
 // V rows in flight per thread slot of the gather (register budget).
 template <int G>
-__host__ __device__ constexpr int gather_unroll() { return G <= 4 ? 8 : 4; }
+__host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 8 : 4; }
 
-// Keys per select slice: 32 x 128 / G scores (16 KB) staged per CTA.
+// Most keys per select slice: 128-key groups, at most 40 staged scores and
+// 24 groups per thread.  Calls use balanced slices of at most this length.
 template <int G>
-__host__ __device__ constexpr int slice_keys() { return kThreads * (32 / G > 0 ? 32 / G : 1); }
+__host__ __device__ constexpr int slice_keys() { return kThreads * (40 / G < 24 ? 40 / G : 24); }
 
 // Score columns per key in the workspace: G rounded up to even (8-byte stores).
 __host__ __device__ constexpr int score_cols(int G) { return G == 1 ? 1 : (G + 1) / 2 * 2; }
@@ -73,7 +74,7 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  int mask_words, spp, ipp, lstride, score_warps;
+  int mask_words, spp, ipp, slice_len, lstride, score_warps;
   // workspace
   float* logits;      // [pairs][lstride][score_cols(G)]
   float2* stats;      // [pairs][spp][G]: a warp run's partial at the run's first tile
@@ -162,7 +163,8 @@ struct SelectSmem {
   int j[slice_keys<G>()];  // union keys of the slice
   union {
     alignas(16) float sc[slice_keys<G>() * score_cols(G)];  // the slice's scores, [key][column]
-    float acc[kWarps][G][D];                    // per-warp sums, after the gather
+    alignas(16) float w[slice_keys<G>()][G];                // then: exp(a - m) of the union
+    float acc[kWarps][G][D];                                // then: per-warp sums
   } u;
 };
 
@@ -417,13 +419,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
 // Select: one slice of one pair per CTA.
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 8) decode_select_kernel(const DecodeParams p) {
-  constexpr int DPL = D / kWarp;          // d values per lane in the gather (whole warp per V row)
+__global__ void __launch_bounds__(kThreads, 6) decode_select_kernel(const DecodeParams p) {
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
   constexpr int GC = score_cols(G);
   constexpr int kGatherUnroll = gather_unroll<G>();
-  constexpr int kChunks = SK * GC * 4 / 16;  // 16-byte copies of the slice's scores
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SelectSmem<D, G>& sm = *reinterpret_cast<SelectSmem<D, G>*>(smem_raw);
   const int item = blockIdx.x;
@@ -443,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 8) decode_select_kernel(const Decode
 
   // Stage the slice's scores in shared memory (keys beyond the stride are
   // never copied; keys beyond L are ignored below).
-  const int s0 = slice * SK;
+  const int SL = p.slice_len;  // keys in every slice, a multiple of 128, <= SK
+  const int s0 = slice * SL;
   {
     const char* src = reinterpret_cast<const char*>(p.logits + ((size_t)pair * p.lstride + s0) * GC);
-    const int limit = (min(s0 + SK, p.lstride) - s0) * GC * 4;  // bytes inside the pair's row
+    const int limit = (min(s0 + SL, p.lstride) - s0) * GC * 4;  // bytes inside the pair's row
     const uint32_t dst = smem_u32(sm.u.sc);
-    for (int i = threadIdx.x; i < kChunks; i += kThreads)
-      if (i * 16 < limit) cp_async16(dst + i * 16, src + i * 16, 16u);
+    for (int i = threadIdx.x; i * 16 < limit; i += kThreads) cp_async16(dst + i * 16, src + i * 16, 16u);
     cp_async_commit();
   }
 
@@ -519,28 +519,31 @@ __global__ void __launch_bounds__(kThreads, 8) decode_select_kernel(const Decode
     kt[h] = 0;
   }
   unsigned uni[NGRP];
+  float wv[NGRP][G];
   int wcount = 0;
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
     const int jl = gi * kThreads + warp * kWarp + lane;  // key within the slice
     const int j0 = s0 + gi * kThreads + warp * kWarp;
-    const bool valid = s0 + jl < L;
+    const bool in_slice = gi * kThreads < SL;  // warp-uniform
+    const bool valid = in_slice && s0 + jl < L;
     unsigned un = 0u;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float a = valid ? sm.u.sc[jl * GC + h] : -CUDART_INF_F;
       const bool keep = valid && (a >= T[h]);
-      Rl[h] += keep ? __expf(a - M[h]) : 0.f;
+      wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
+      Rl[h] += wv[gi][h];
       const unsigned bal = __ballot_sync(0xffffffffu, keep);
       kt[h] += __popc(bal);
       un |= bal;
-      if (mrow && lane == 0 && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      if (mrow && lane == 0 && in_slice && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
     }
     uni[gi] = un;
     wcount += __popc(un);
   }
   if (lane == 0) sm.cnt[warp] = wcount;
-  __syncthreads();
+  __syncthreads();  // every score is in registers: the weights may overwrite them
   int base = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
@@ -549,58 +552,66 @@ __global__ void __launch_bounds__(kThreads, 8) decode_select_kernel(const Decode
   }
 #pragma unroll
   for (int gi = 0; gi < NGRP; ++gi) {
-    if ((uni[gi] >> lane) & 1u) sm.j[base + __popc(uni[gi] & ((1u << lane) - 1u))] = gi * kThreads + warp * kWarp + lane;
+    if ((uni[gi] >> lane) & 1u) {
+      const int pos = base + __popc(uni[gi] & ((1u << lane) - 1u));
+      sm.j[pos] = gi * kThreads + warp * kWarp + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h) sm.u.w[pos][h] = wv[gi][h];
+    }
     base += __popc(uni[gi]);
   }
   __syncthreads();
 
-  // Gather the union's V rows, one row per warp instruction (DPL d values per
-  // lane); a row's weights are recomputed from the staged scores exactly as
-  // R was above.
-  const __nv_bfloat16* vbase = p.v + ((size_t)pair * p.Nmax + s0) * D + lane * DPL;
-  float acc[G][DPL];
+  // Gather the union's V rows: LPR lanes per row, 16 bytes (8 d values) each.
+  constexpr int LPR = D / 8;
+  constexpr int RPI = kThreads / LPR;  // rows per CTA instruction
+  const int rsub = threadIdx.x / LPR;
+  const int dl = threadIdx.x % LPR;
+  const __nv_bfloat16* vbase = p.v + ((size_t)pair * p.Nmax + s0) * D + dl * 8;
+  float acc[G][8];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
-  for (int r0 = warp; r0 < total; r0 += kWarps * kGatherUnroll) {
-    uint2 vv[kGatherUnroll];
+    for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
+  for (int r0 = 0; r0 < total; r0 += RPI * kGatherUnroll) {
+    uint4 vv[kGatherUnroll];
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * kWarps;
-      if (r < total) {
-        const __nv_bfloat16* src = vbase + (size_t)sm.j[r] * D;
-        if (DPL == 4) {
-          vv[u] = __ldg(reinterpret_cast<const uint2*>(src));
-        } else {
-          vv[u].x = __ldg(reinterpret_cast<const unsigned*>(src));
-          vv[u].y = 0u;
-        }
-      }
+      const int r = r0 + u * RPI + rsub;
+      if (r < total) vv[u] = ld_nc16(vbase + (size_t)sm.j[r] * D);
     }
 #pragma unroll
     for (int u = 0; u < kGatherUnroll; ++u) {
-      const int r = r0 + u * kWarps;
+      const int r = r0 + u * RPI + rsub;
       if (r < total) {
-        const int jl = sm.j[r];
-        const float vf[4] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y)};
+        const float vf[8] = {bf16lo(vv[u].x), bf16hi(vv[u].x), bf16lo(vv[u].y), bf16hi(vv[u].y),
+                             bf16lo(vv[u].z), bf16hi(vv[u].z), bf16lo(vv[u].w), bf16hi(vv[u].w)};
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float a = sm.u.sc[jl * GC + h];
-          const float wh = (a >= T[h]) ? __expf(a - M[h]) : 0.f;
+          const float wh = sm.u.w[r][h];
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
         }
       }
     }
   }
+  // Reduce over the rows of a warp instruction, then over warps.
 #pragma unroll
-  for (int h = 0; h < G; ++h) Rl[h] = warp_sum(Rl[h]);
-  __syncthreads();  // the staged scores are no longer read: acc may reuse them
+  for (int h = 0; h < G; ++h) {
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+    for (int e = 0; e < 8; ++e) {
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) sm.u.acc[warp][h][lane * DPL + e] = acc[h][e];
+      for (int off = LPR; off < kWarp; off <<= 1) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], off);
+    }
+    Rl[h] = warp_sum(Rl[h]);
+  }
+  __syncthreads();  // the weights are no longer read: acc may reuse them
+  if (lane < LPR) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm.u.acc[warp][h][dl * 8 + e] = acc[h][e];
+  }
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -698,6 +709,7 @@ cudaError_t grid_of(int& grid) {
   return cudaSuccess;
 }
 
+// Fewest balanced slices of at most slice_keys<G>() keys.
 int slices_per_pair(int cache_len, int G) {
   int sk = 0;
   switch (G) {
@@ -731,6 +743,7 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   if ((e = grid_of<D, G>(grid)) != cudaSuccess) return e;
   const int pairs = p.B * p.Hkv;
   p.ipp = slices_per_pair(p.Nmax, G);
+  p.slice_len = ((p.Nmax + p.ipp - 1) / p.ipp + kThreads - 1) / kThreads * kThreads;
   p.score_warps = grid * kWarps;
   const DecodeLayout l = decode_layout(a, p.ipp);
   if (a.workspace_bytes < l.total) return cudaErrorInvalidValue;
