@@ -14,6 +14,11 @@ copied from pinned host memory and outputs copied back; roofline = the score
 kernel's algorithmic bytes / its CUDA-event duration; cpu_baseline = the
 float64 oracle on a bounded sample, on the host cores.
 
+The line also carries ``prefill``: the LLaMA-3-8B-shaped causal prefill
+(batch 1, 32 query / 8 KV heads, d = 128, 4096 tokens, k = 64) in both
+threshold modes, as dense-equivalent TFLOP/s of the executed tiles against
+the bf16 tensor peak.  ``--workload cfg3`` prints that prefill as the line.
+
 ``--impl reference`` times the float64 oracle instead (the method has no
 other implementation); it needs no GPU.
 """
@@ -59,7 +64,9 @@ def parse():
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["topt", "reference"], default="topt")
-    p.add_argument("--workload", choices=["cfg2", "cfg4", "cfg5"], default="cfg2")
+    p.add_argument("--workload", choices=["cfg2", "cfg3", "cfg4", "cfg5"], default="cfg2")
+    p.add_argument("--no-prefill", action="store_true", help="leave out the prefill object")
+    p.add_argument("--prefill-steps", type=int, default=30)
     p.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -90,6 +97,18 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s: the burst figure (the prefill kernel is timed alone)."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 # ---------------------------------------------------------------------------
@@ -263,6 +282,119 @@ def kept_ratio_by_bucket(state):
 
 
 # ---------------------------------------------------------------------------
+# the prefill workload
+# ---------------------------------------------------------------------------
+PREFILL_MODES = (("post-softmax+VMC", 1, 0), ("pre-softmax+exact SDC+VMC", 0, 1))
+L2_FLUSH_BYTES = 256 << 20     # written between timed prefill calls (L2 is 129 MB)
+
+
+class PrefillState:
+    """One causal prefill of `wl` resident on the GPU, theta calibrated on the GPU."""
+
+    def __init__(self, wl, dev, mode, sdc):
+        self.wl, self.dev, self.mode, self.sdc = wl, dev, mode, sdc
+        B, Hq, Hkv, d, S = wl.B, wl.Hq, wl.Hkv, wl.d, wl.S
+        self.ch = synth.outlier_channels(synth.seed_of(wl.name, "channels"), Hkv, d)
+        cal = topt.Calibrator(Hq, S, wl.k, mode)
+        row_len = torch.arange(1, S + 1, device=dev, dtype=torch.int32)
+        for s_ in range(wl.n_cal):
+            Q, K, _ = self.inputs(synth.seed_of(wl.name, "cal", s_), 1)
+            cal.add(Q, K, row_len, reset=(s_ == 0))
+        self.theta = cal.finalize().clone()
+        self.Q, self.K, self.V = self.inputs(synth.seed_of(wl.name, "eval"), B)
+        self.out = torch.empty((B, Hq, S, d), device=dev)
+        self.kept = torch.empty((B, Hq, S), device=dev, dtype=torch.int32)
+        self.tiles = torch.zeros(2, device=dev, dtype=torch.int64)
+        self.args = topt.prefill_args(self.Q, self.K, self.V, self.theta, mode=mode, sdc=sdc,
+                                      vmc=True, out=self.out, kept=self.kept, tiles=self.tiles)
+        self.ws = torch.empty(max(1, topt.prefill_workspace_bytes(self.args)), device=dev,
+                              dtype=torch.uint8)
+        self.args.workspace = ctypes.c_void_p(self.ws.data_ptr())
+        self.args.workspace_bytes = self.ws.numel()
+        self.tile_rows, self.tile_keys = topt.prefill_tile_shape(self.args)
+
+    def inputs(self, seed, B):
+        wl = self.wl
+        gen = synth.generator(seed & 0xffffffff, self.dev)
+        K = synth.keys(gen, B, wl.Hkv, wl.S, wl.d, self.ch, device=self.dev)
+        V = synth.values(gen, B, wl.Hkv, wl.S, wl.d, device=self.dev)
+        Q = synth.prefill_queries(gen, K, wl.Hq)
+        return Q, K, V
+
+    def call(self, L, stream, events=(None, None)):
+        self.args.events[0], self.args.events[1] = events
+        rc = L.topt_prefill(ctypes.byref(self.args), stream)
+        self.args.events[0] = self.args.events[1] = None
+        if rc:
+            raise topt.ToptError("topt_prefill", rc)
+
+
+def time_prefill(L, st, stream, steps, warmup):
+    """CUDA-event times (s) of whole calls and of the attention kernel, L2 flushed between."""
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    flush = torch.empty(L2_FLUSH_BYTES, device=st.dev, dtype=torch.uint8)
+    for _ in range(warmup):
+        st.call(L, sh)
+    torch.cuda.synchronize(st.dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:            # a torch event exists once recorded: create them all first
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(st.dev)
+    st.tiles.zero_()
+    for e in ev:
+        flush.fill_(1)
+        e[0].record(stream)
+        st.call(L, sh, (ctypes.c_void_p(e[1].cuda_event), ctypes.c_void_p(e[2].cuda_event)))
+        e[3].record(stream)
+    torch.cuda.synchronize(st.dev)
+    call_s = [e[0].elapsed_time(e[3]) / 1e3 for e in ev]
+    kern_s = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
+    tiles = [int(x) // steps for x in st.tiles.tolist()]
+    return call_s, kern_s, tiles
+
+
+def prefill_flops(st, tiles):
+    """Dense-equivalent flops of one call: QK^T over every causal tile plus P.V
+    over the executed tiles (the pass-1 recomputation of QK^T not counted)."""
+    per_tile = 2.0 * st.wl.d * st.tile_rows * st.tile_keys
+    executed, causal = tiles
+    return per_tile * (causal + executed), per_tile * (2 * causal + executed)
+
+
+def prefill_report(L, wl, dev, stream, steps, warmup):
+    peak, kind = tensor_peak()
+    out = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "S": wl.S,
+           "k": wl.k, "modes": []}
+    for name, mode, sdc in PREFILL_MODES:
+        st = PrefillState(wl, dev, mode, sdc)
+        call_s, kern_s, tiles = time_prefill(L, st, stream, steps, warmup)
+        useful, issued = prefill_flops(st, tiles)
+        kern = float(np.mean(kern_s))
+        call = float(np.mean(call_s))
+        achieved = useful / kern / 1e12
+        kept = st.kept.double()
+        out["modes"].append({
+            "mode": name, "tflops_call": useful / call / 1e12, "ms_per_call": call * 1e3,
+            "tokens_per_s": wl.B * wl.S / call,
+            "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                         if kind == "measured" else "fallback 1.9 PFLOP/s",
+                         "traffic": None, "avg_launch_ms": kern * 1e3,
+                         "flops_per_launch": useful,
+                         "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
+                         "issued_tflops": issued / kern / 1e12},
+            "tiles_executed": tiles[0], "tiles_causal": tiles[1],
+            "tiles_skipped_frac": 1.0 - tiles[0] / max(1, tiles[1]),
+            "tile": [st.tile_rows, st.tile_keys],
+            "kept_over_k": round(kept[..., wl.k:].mean().item() / wl.k, 4)})
+        del st
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
 def oracle_rows_per_second(q, K, V, seq_len, theta, mu, wl, rows, seconds, cores):
@@ -329,10 +461,98 @@ def cpu_baseline(wl, seconds, layers_total):
                       f"scaled to {rows_per_step} rows per step"}
 
 
+def causal_flops(wl):
+    """Dense-equivalent flops of one prefill call over the causal triangle:
+    QK^T and P.V on every (i, j <= i) element, 2 d flops each."""
+    return 4.0 * wl.d * wl.B * wl.Hq * (wl.S * (wl.S + 1) / 2)
+
+
+def host_prefill_sample(wl, n_cal=2, heads=4):
+    """One KV group of the prefill workload on the host, theta from the oracle's
+    calibration over n_cal sequences (all rows)."""
+    import oracle.topt_ref as ref
+    ch = synth.outlier_channels(synth.seed_of(wl.name, "channels"), wl.Hkv, wl.d)[:1]
+    samples = {}
+    for mode in (0, 1):
+        gen = synth.generator(synth.seed_of(wl.name, "host", mode), "cpu")
+        Kc = synth.keys(gen, n_cal, 1, wl.S, wl.d, ch)
+        Qc = synth.prefill_queries(gen, Kc, heads)
+        th, _ = ref.calibrate_ref(synth.as_f64(Qc), synth.as_f64(Kc), list(range(1, wl.S + 1)),
+                                  wl.k, mode, 0.0, wl.S)
+        K = synth.keys(gen, 1, 1, wl.S, wl.d, ch)
+        V = synth.values(gen, 1, 1, wl.S, wl.d)
+        Q = synth.prefill_queries(gen, K, heads)
+        samples[mode] = (synth.as_f64(Q), synth.as_f64(K), synth.as_f64(V), th)
+    return samples
+
+
+def oracle_prefill_row_seconds(sample, mode, sdc, rows, cores):
+    """Wall-clock seconds per prefill row of the oracle on `cores` threads."""
+    import oracle.topt_ref as ref
+    Q, K, V, th = sample
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(lambda r: ref.prefill_ref(Q, K, V, th, mode, sdc, True, rows=[r]), rows))
+    return (time.perf_counter() - t0) / len(rows)
+
+
+def prefill_rows_sample(wl, n, heads=4, seed=0):
+    rng = np.random.default_rng(seed)
+    return [(0, int(rng.integers(heads)), int(i)) for i in rng.integers(0, wl.S, n)]
+
+
+def prefill_cpu_baseline(wl, seconds):
+    cores = host_cores()
+    sample = host_prefill_sample(wl)
+    done, spent = 0, 0.0
+    while spent < seconds:
+        rows = prefill_rows_sample(wl, 8 * cores, seed=done)
+        spent += oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores) * len(rows)
+        done += len(rows)
+    t_row = spent / done
+    rows_per_call = wl.B * wl.Hq * wl.S
+    return {"value": causal_flops(wl) / (t_row * rows_per_call) / 1e12, "unit": "TFLOP/s",
+            "cores": cores, "kind": "oracle",
+            "sample": f"{done} prefill rows (uniform row index, post-softmax+VMC, k={wl.k}), "
+                      f"float64 numpy, {cores} threads; scaled to {rows_per_call} rows per call"}
+
+
+def run_reference_prefill(args, wl):
+    cores = host_cores()
+    sample = host_prefill_sample(wl)
+    per_step = 4 * cores
+
+    def one_step(i):
+        rows = prefill_rows_sample(wl, per_step, seed=i)
+        return oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores)
+
+    for i in range(args.warmup):
+        one_step(i)
+    t_row = sum(one_step(args.warmup + i) for i in range(args.steps)) / args.steps
+    rows_per_call = wl.B * wl.Hq * wl.S
+    ms = t_row * rows_per_call * 1e3
+    value = causal_flops(wl) / (ms / 1e3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                       "S": wl.S, "k": wl.k, "mode": "post-softmax+VMC"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} prefill rows per step of {rows_per_call}, "
+                                       "float64 numpy oracle"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     """--impl reference: the float64 oracle, timed per step on a bounded sample."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
+        return
+    if args.workload == "cfg3":
+        run_reference_prefill(args, workloads.CFG3)
         return
     wl = WORKLOADS[args.workload]
     layers_total = args.layers or wl.layers
@@ -386,6 +606,9 @@ def main():
         torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.workload == "cfg3":
+        main_prefill(args, dev, rank, local, world)
+        return
     wl = WORKLOADS[args.workload]
     layers = args.layers or wl.layers
 
@@ -538,10 +761,114 @@ def main():
         line["e2e"] = e2e
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if not args.no_prefill:
+        del state
+        torch.cuda.empty_cache()
+        line["prefill"] = prefill_report(L, workloads.CFG3, dev, stream, args.prefill_steps, 3)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def main_prefill(args, dev, rank, local, world):
+    """--workload cfg3: the causal prefill as the bench line (post-softmax + VMC)."""
+    wl = workloads.CFG3
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = prefill_cpu_baseline(wl, args.cpu_seconds)
+    from calibrated_thresholding_gb300 import build
+    build.build()
+    L = topt.lib()
+    name, mode, sdc = PREFILL_MODES[0]
+    st = PrefillState(wl, dev, mode, sdc)
+    stream = torch.cuda.current_stream(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    t0 = time.time()
+    call_s, kern_s, tiles = time_prefill(L, st, stream, args.steps, args.warmup)
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    ms = float(np.sum(call_s)) * 1e3
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    call = ms / 1e3 / args.steps
+    value = causal_flops(wl) * world / call / 1e12
+    useful, issued = prefill_flops(st, tiles)
+    kern = float(np.mean(kern_s))
+    peak, kind = tensor_peak()
+    achieved = useful / kern / 1e12
+    e2e = None if args.no_e2e else prefill_e2e(st, args, dev, world)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": call * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "S": wl.S, "k": wl.k, "mode": name,
+                   "flops": "dense-equivalent over the causal triangle: QK^T + P.V, 2 d per element",
+                   "l2": f"{L2_FLUSH_BYTES >> 20} MiB written between timed calls",
+                   "parallelism": f"replicas x{world} (independent prefills per GPU)"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                     if kind == "measured" else "fallback 1.9 PFLOP/s",
+                     "traffic": None, "avg_launch_ms": kern * 1e3, "flops_per_launch": useful,
+                     "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
+                     "issued_tflops": issued / kern / 1e12},
+        "tiles_executed": tiles[0], "tiles_causal": tiles[1],
+        "tiles_skipped_frac": 1.0 - tiles[0] / max(1, tiles[1]),
+        "kept_over_k": round(st.kept.double()[..., wl.k:].mean().item() / wl.k, 4),
+        "gpu_launches": args.steps * 5,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def prefill_e2e(st, args, dev, world):
+    """The prefill through topt.prefill with Q, K, V copied in from pinned host
+    memory and the output copied back, every step."""
+    wl = st.wl
+    host = [x.cpu().pin_memory() for x in (st.Q, st.K, st.V)]
+    out_host = torch.empty_like(st.out, device="cpu").pin_memory()
+
+    def step():
+        for d_, h_ in zip((st.Q, st.K, st.V), host):
+            d_.copy_(h_, non_blocking=True)
+        topt.prefill(st.Q, st.K, st.V, st.theta, mode=st.mode, sdc=st.sdc, vmc=True, out=st.out,
+                     kept=st.kept, workspace=st.ws)
+        out_host.copy_(st.out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    steps = max(5, args.steps // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    dt_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt_s = float(t.item())
+    h2d = sum(h_.numel() * h_.element_size() for h_ in host)
+    return {"value": causal_flops(wl) * steps * world / dt_s / 1e12, "unit": "TFLOP/s",
+            "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": out_host.numel() * 4}
 
 
 def run_e2e(state, args, dev, world):

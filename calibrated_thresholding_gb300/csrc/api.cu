@@ -42,6 +42,8 @@ topt_status check_prefill_shape(const topt_prefill_args* a) {
   if (a->dtype != TOPT_BF16 && a->dtype != TOPT_F32) return TOPT_EDTYPE;
   if ((size_t)a->batch * a->n_q_heads > 65535u * 1024u || a->n_q_heads > 65535 || a->batch > 65535)
     return TOPT_ESHAPE;
+  // tensor-core grid: one CTA per 128 query rows of every (batch, head)
+  if ((size_t)a->batch * a->n_q_heads * ((size_t)(a->seq + 127) / 128) > 0x7fffffffu) return TOPT_ESHAPE;
   return check_common_mode(a->mode, a->sdc);
 }
 

@@ -15,6 +15,18 @@ constexpr int kWarp = 32;
 // Round a byte count up to 256 so every workspace sub-buffer stays aligned.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Records the caller's profiling event `ev` (a cudaEvent_t, or NULL) on s;
+// under stream capture as an external event node.
+inline cudaError_t record_event(void* ev, cudaStream_t s) {
+  if (!ev) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal)
+             : cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

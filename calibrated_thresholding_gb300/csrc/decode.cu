@@ -726,16 +726,6 @@ int slices_per_pair(int cache_len, int G) {
 }
 
 // Profiling events; under stream capture they become timing nodes of the graph.
-cudaError_t record(void* ev, cudaStream_t s) {
-  if (!ev) return cudaSuccess;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(s, &cs);
-  if (e != cudaSuccess) return e;
-  return cs == cudaStreamCaptureStatusActive
-             ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal)
-             : cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
-}
-
 template <int D, int G>
 cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s) {
   int grid = 0;
@@ -757,7 +747,7 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   unsigned* counters = reinterpret_cast<unsigned*>(ws + l.counters);
   p.tstart = reinterpret_cast<int*>(counters);
   p.ticket = counters + 2 * (kMaxBatch + 1);
-  if ((e = record(a.events[0], s)) != cudaSuccess) return e;
+  if ((e = record_event(a.events[0], s)) != cudaSuccess) return e;
   decode_scores_kernel<D, G><<<grid, kThreads, sizeof(ScoreSmem<D>), s>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -770,9 +760,9 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if ((e = record(a.events[1], s)) != cudaSuccess) return e;
+  if ((e = record_event(a.events[1], s)) != cudaSuccess) return e;
   if ((e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G>, p)) != cudaSuccess) return e;
-  return record(a.events[2], s);
+  return record_event(a.events[2], s);
 }
 
 template <int D>

@@ -21,6 +21,13 @@ cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s);
 size_t prefill_workspace_bytes(const topt_prefill_args& a);
 void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys);
 cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s);
+// tensor-core path (bf16): 128-row x 64-key tiles; v16 is the fp16 copy of V
+// (prefill_tc_v16_bytes), vmax/vexp one word per (batch, kv head).
+size_t prefill_tc_v16_bytes(const topt_prefill_args& a);
+int prefill_tc_rows();
+int prefill_tc_keys();
+cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
+                           const float* mu, cudaStream_t s);
 
 // --------------------------------------------------------------- calibrate
 size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);

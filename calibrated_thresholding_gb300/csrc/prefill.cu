@@ -1,4 +1,6 @@
-// Top-theta causal prefill, CUDA-core variant (any supported dtype).
+// Top-theta causal prefill: workspace layout and dispatch, the CUDA-core
+// variant (fp32 inputs) and the causal prefix means of V used by VMC.  bf16
+// inputs run on the tensor cores (prefill_tc.cu).
 //
 // [TopTheta] = "Top-Theta Attention: Sparsifying Transformers by Compensated
 // Thresholding" (arXiv 2502.08363v2).  Row i of head h sees keys 0..i
@@ -208,31 +210,42 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   }
 }
 
+// Causal prefix means mu_i = mean(V_0..V_i) into p.mu.
 template <typename T, int D>
-cudaError_t launch_td(const PrefillParams& p, cudaStream_t s) {
+cudaError_t launch_means(const PrefillParams& p, cudaStream_t s) {
   cudaError_t e;
-  if (p.vmc) {
-    const int nchunk = (p.S + kMeanChunk - 1) / kMeanChunk;
-    chunk_sum_kernel<T, D><<<dim3(nchunk, p.B * p.Hkv), D, 0, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    prefix_mean_kernel<T, D><<<dim3(nchunk, p.B * p.Hkv), D, 0, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  prefill_simt_kernel<T, D><<<dim3((p.S + kRows - 1) / kRows, p.Hq, p.B), kThreads, 0, s>>>(p);
+  const int nchunk = (p.S + kMeanChunk - 1) / kMeanChunk;
+  chunk_sum_kernel<T, D><<<dim3(nchunk, p.B * p.Hkv), D, 0, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  prefix_mean_kernel<T, D><<<dim3(nchunk, p.B * p.Hkv), D, 0, s>>>(p);
   return cudaGetLastError();
 }
 
+template <typename T, int D>
+cudaError_t launch_td(const PrefillParams& p, void* const events[2], cudaStream_t s) {
+  cudaError_t e;
+  if (p.vmc && (e = launch_means<T, D>(p, s)) != cudaSuccess) return e;
+  if ((e = record_event(events[0], s)) != cudaSuccess) return e;
+  prefill_simt_kernel<T, D><<<dim3((p.S + kRows - 1) / kRows, p.Hq, p.B), kThreads, 0, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return record_event(events[1], s);
+}
+
 struct PrefillLayout {
-  size_t mu, csum, total;
+  size_t mu, csum, v16, vmax, vexp, total;
 };
 
 PrefillLayout prefill_layout(const topt_prefill_args& a) {
   PrefillLayout l;
   const size_t bh = (size_t)a.batch * a.n_kv_heads;
   const size_t nchunk = (a.seq + kMeanChunk - 1) / kMeanChunk;
+  const bool tc = a.dtype == TOPT_BF16;
   size_t off = 0;
   l.mu = off;   off += a.vmc ? align256(bh * a.seq * (size_t)a.head_dim * sizeof(float)) : 0;
   l.csum = off; off += a.vmc ? align256(bh * nchunk * (size_t)a.head_dim * sizeof(float)) : 0;
+  l.v16 = off;  off += tc ? align256(prefill_tc_v16_bytes(a)) : 0;
+  l.vmax = off; off += tc ? align256(bh * sizeof(uint32_t)) : 0;
+  l.vexp = off; off += tc ? align256(bh * sizeof(int32_t)) : 0;
   l.total = off;
   return l;
 }
@@ -241,9 +254,10 @@ PrefillLayout prefill_layout(const topt_prefill_args& a) {
 
 size_t prefill_workspace_bytes(const topt_prefill_args& a) { return prefill_layout(a).total; }
 
-void prefill_tile_shape(const topt_prefill_args&, int32_t* rows, int32_t* keys) {
-  *rows = kRows;
-  *keys = kKeys;
+void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys) {
+  const bool tc = a.dtype == TOPT_BF16;
+  *rows = tc ? prefill_tc_rows() : kRows;
+  *keys = tc ? prefill_tc_keys() : kKeys;
 }
 
 cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s) {
@@ -273,9 +287,16 @@ cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s) {
   p.mu = a.vmc ? reinterpret_cast<float*>(ws + l.mu) : nullptr;
   p.csum = a.vmc ? reinterpret_cast<float*>(ws + l.csum) : nullptr;
   if (a.dtype == TOPT_BF16) {
-    return a.head_dim == 128 ? launch_td<__nv_bfloat16, 128>(p, s) : launch_td<__nv_bfloat16, 64>(p, s);
+    // prefix means on the CUDA cores, attention on the tensor cores
+    if (a.vmc) {
+      const cudaError_t e = a.head_dim == 128 ? launch_means<__nv_bfloat16, 128>(p, s)
+                                              : launch_means<__nv_bfloat16, 64>(p, s);
+      if (e != cudaSuccess) return e;
+    }
+    return prefill_tc_run(a, ws + l.v16, reinterpret_cast<uint32_t*>(ws + l.vmax),
+                          reinterpret_cast<int32_t*>(ws + l.vexp), p.mu, s);
   }
-  return a.head_dim == 128 ? launch_td<float, 128>(p, s) : launch_td<float, 64>(p, s);
+  return a.head_dim == 128 ? launch_td<float, 128>(p, a.events, s) : launch_td<float, 64>(p, a.events, s);
 }
 
 }  // namespace topt

@@ -1,0 +1,622 @@
+// Top-theta causal prefill on the tensor cores (tcgen05), bf16 q/k/v.
+//
+// [TopTheta] = "Top-Theta Attention: Sparsifying Transformers by Compensated
+// Thresholding" (arXiv 2502.08363v2).  Row i of head h sees keys 0..i
+// ([TopTheta §2.2, prefill phase]); each score is compared against the row's
+// calibrated threshold theta[h][i] ([TopTheta §3, Fig. 1]), SDC [Eq. 4] and
+// VMC [Eq. 5-7] normalise the output as in the CUDA-core variant.
+//
+// One CTA = 128 query rows of one (batch, head); ten warps:
+//   warps 0-7  two threads per query row (the row is its TMEM lane; warps w
+//              and w+4 share a lane quadrant and take 64 of the tile's 128
+//              columns each): pass 1 row maximum and sum, pass 2 threshold
+//              and P, epilogue
+//   warp 8     TMA producer: the Q block once, K tiles for both passes, V
+//              tiles for pass 2 (128-byte swizzled boxes of 64 elements)
+//   warp 9     TMEM allocation; lane 0 issues tcgen05.mma
+// Scores S = Q K^T (128 rows x 128 keys, fp32) rotate through three TMEM
+// buffers so the tensor core computes the next tiles while the row threads
+// read one.  The output accumulator O (128 x d, fp32) stays in TMEM for the
+// whole of pass 2.  Pass 2 writes P = exp(a - m) of kept elements (0
+// elsewhere) as fp16 pairs into the score buffer it was read from, and
+// O += P V takes P straight from TMEM; it is issued only when some row of the
+// tile kept an element, and the executed and causal tile counts are reported.
+// 128-key tiles keep both MMAs at N >= 128, the width at which one tcgen05.mma
+// runs at the tensor core's full rate.
+//
+// P is fp16: rounding it to bf16 costs up to ~2e-3 relative output error on
+// peaked rows, fp16 ~3e-4.  One MMA takes A and B in the same 16-bit type, so
+// V is read from an fp16 copy scaled per (batch, kv head) by 2^-e with e set
+// so that max|V| 2^-e lies in [2^14, 2^15): the scaling is exact and every
+// bf16 value above 2^-17 max|V| converts exactly; O is multiplied by 2^e.
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace topt {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;          // query rows per CTA = TMEM lanes
+constexpr int BN = 128;          // keys per tile
+constexpr int KST = 3;           // K ring stages
+constexpr int VST = 2;           // V ring stages
+constexpr int SBUF = 3;          // score buffers in TMEM
+constexpr int kRowWarps = 8;     // two warps per TMEM lane quadrant, 64 columns each
+constexpr int kProducerWarp = kRowWarps;
+constexpr int kMmaWarp = kRowWarps + 1;
+constexpr int kTcThreads = 32 * (kRowWarps + 2);
+constexpr uint32_t kTmemCols = 512;  // score buffers at columns 0, 128, 256; O at 384
+constexpr uint32_t kOCol = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Shared-memory layout (byte offsets from a 1024-aligned base).  Operand
+// tiles are stored as the 128-byte-swizzle layout TMA writes: rows of 128
+// bytes (64 16-bit elements), 16-byte chunk c of row r at chunk c ^ (r & 7).
+template <int D>
+struct TcLayout {
+  static constexpr int NP = D / 64;          // 64-element panels along d
+  static constexpr uint32_t QP = BM * 128;   // one Q panel
+  static constexpr uint32_t KP = BN * 128;   // one K or V panel
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K = Q + NP * QP;
+  static constexpr uint32_t V = K + KST * NP * KP;
+  static constexpr uint32_t BAR = V + VST * NP * KP;
+  // barriers: Q full; K full/empty; V full/empty; S full; S read by the rows;
+  // P.V done (frees a score buffer holding P); P full; O ready; MMA drain
+  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST,
+                       B_VE = B_VF + VST, B_SF = B_VE + VST, B_SR = B_SF + SBUF,
+                       B_PD = B_SR + SBUF, B_PF = B_PD + SBUF, B_O = B_PF + 2, B_DRAIN = B_O + 1,
+                       NBAR = B_DRAIN + 1;
+  // misc words: abort flag, TMEM address, O written; any-kept flags [2][8] bytes
+  static constexpr uint32_t MISC = BAR + NBAR * 8;
+  static constexpr uint32_t ANY = (MISC + 16 + 7) & ~7u;
+  // row statistics of the two half-rows: [2 halves][BM] float2, twice
+  static constexpr uint32_t XCH1 = ANY + 2 * kRowWarps;
+  static constexpr uint32_t XCH2 = XCH1 + 2 * BM * 8;
+  static constexpr uint32_t BYTES = XCH2 + 2 * BM * 8;
+  static constexpr uint32_t ALLOC = BYTES + 1024;  // room to align the base
+  static_assert(kRowWarps == 8, "one 8-byte word of any-kept flags per P buffer");
+  static_assert(ALLOC <= 227 * 1024, "shared memory");
+};
+
+struct TcParams {
+  int B, Hq, Hkv, S, Lmax, mode, sdc, vmc, mask_words, nqb;
+  float gamma, sm_scale;
+  const float* theta;
+  float* out;
+  int32_t* kept;
+  uint32_t* mask;
+  unsigned long long* tiles;
+  int32_t* status;
+  const float* mu;       // [B][Hkv][S][D] prefix means (when vmc)
+  const int32_t* vexp;   // [B * Hkv] exponent e of the fp16 V copy (V16 = V 2^-e)
+};
+
+// Barrier of the 256 row threads (warps 0-7) only.
+__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// fp16 pair of (lo, hi); adds the rounded values to sum, so that R sums the
+// very weights P.V multiplies.
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi, float& sum) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  const float2 back = __half22float2(h);
+  sum += back.x + back.y;
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Visible-column mask of 32 columns when columns c <= lim are visible.
+__device__ __forceinline__ uint32_t vis_mask(int lim) {
+  return lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  using L = TcLayout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  unsigned char* gb = smem_raw + (sb - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::MISC);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gb + L::MISC + 4);
+  volatile int* o_written = reinterpret_cast<volatile int*>(gb + L::MISC + 8);
+  volatile uint8_t* anyf = reinterpret_cast<volatile uint8_t*>(gb + L::ANY);  // [2][kRowWarps]
+  auto bar = [sb](int i) -> uint32_t { return sb + L::BAR + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heaviest row blocks (most causal key tiles) first
+  const int per = p.Hq * p.B;
+  const int qb = p.nqb - 1 - (int)(blockIdx.x / per);
+  const int rem = (int)(blockIdx.x % per);
+  const int h = rem % p.Hq, b = rem / p.Hq;
+  const int kvh = h / (p.Hq / p.Hkv);
+  const int row0 = qb * BM;
+  const int nt = (min(row0 + BM, p.S) - 1) / BN + 1;  // causal key tiles
+  const int bh_q = b * p.Hq + h, bh_kv = b * p.Hkv + kvh;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NBAR; ++i) {
+      const bool per_warp = (i >= L::B_SR && i < L::B_SR + SBUF) || i == L::B_PF || i == L::B_PF + 1;
+      mbar_init(bar(i), per_warp ? kRowWarps : (i == L::B_O ? 2 : 1));
+    }
+    *abort_flag = 0;
+    *o_written = 0;
+    mbar_init_fence();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(gb + L::MISC + 4), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int kcount[KST] = {}, vcount[VST] = {};
+      int ks = 0, kph = 0, vs = 0, vph = 0;
+      mbar_expect_tx(bar(L::B_Q), L::NP * L::QP);
+      for (int pn = 0; pn < L::NP; ++pn)
+        tma_load_3d(sb + L::Q + pn * L::QP, &tmQ, bar(L::B_Q), 64 * pn, row0, bh_q);
+      for (int tt = 0; tt < 2 * nt; ++tt) {
+        const int kt = tt < nt ? tt : tt - nt;
+        if (!mbar_wait(bar(L::B_KE + ks), kph ^ 1, abort_flag)) break;
+        mbar_expect_tx(bar(L::B_KF + ks), L::NP * L::KP);
+        for (int pn = 0; pn < L::NP; ++pn)
+          tma_load_3d(sb + L::K + (ks * L::NP + pn) * L::KP, &tmK, bar(L::B_KF + ks), 64 * pn,
+                      kt * BN, bh_kv);
+        ++kcount[ks];
+        if (++ks == KST) { ks = 0; kph ^= 1; }
+        if (tt >= nt) {
+          if (!mbar_wait(bar(L::B_VE + vs), vph ^ 1, abort_flag)) break;
+          mbar_expect_tx(bar(L::B_VF + vs), L::NP * L::KP);
+          for (int pn = 0; pn < L::NP; ++pn)
+            tma_load_3d(sb + L::V + (vs * L::NP + pn) * L::KP, &tmV, bar(L::B_VF + vs), 64 * pn,
+                        kt * BN, bh_kv);
+          ++vcount[vs];
+          if (++vs == VST) { vs = 0; vph ^= 1; }
+        }
+      }
+      // every copy this thread issued lands before the CTA releases its memory
+      bool drained = mbar_wait_drain(bar(L::B_Q), 0);
+      for (int s = 0; s < KST; ++s)
+        if (kcount[s]) drained &= mbar_wait_drain(bar(L::B_KF + s), (kcount[s] - 1) & 1);
+      for (int s = 0; s < VST; ++s)
+        if (vcount[s]) drained &= mbar_wait_drain(bar(L::B_VF + s), (vcount[s] - 1) & 1);
+      if (!drained) set_status(p.status, TOPT_ETIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(BN, 1, 1, 0);  // bf16 Q, bf16 K (K-major)
+      constexpr uint32_t idO = idesc_f16(D, 0, 0, 1);   // fp16 P (TMEM), fp16 V (N-major)
+      // descriptor words: every shared operand has 8-row groups 1024 bytes apart
+      constexpr uint32_t hi = sdesc_hi(1024);
+      const uint32_t q_lo = sdesc_lo(sb + L::Q, 16);
+      const uint32_t k_lo = sdesc_lo(sb + L::K, 16);
+      const uint32_t v_lo = sdesc_lo(sb + L::V, L::KP);
+      volatile unsigned long long* any8 = reinterpret_cast<volatile unsigned long long*>(anyf);
+      uint32_t started = 0;
+      unsigned long long executed = 0;
+      int vs = 0, vph = 0;            // V stage and phase of the next P.V
+      uint32_t pd_par = 0;            // per score buffer: parity of its next P.V-done phase
+      auto pv = [&](int u) -> bool {
+        const int t = nt + u, sbuf = t % SBUF, pb = u & 1;
+        if (!mbar_wait(bar(L::B_PF + pb), (u >> 1) & 1, abort_flag)) return false;
+        const bool any = any8[pb] != 0ull;
+        if (!mbar_wait(bar(L::B_VF + vs), vph, abort_flag)) return false;
+        if (any) {
+          tc_fence_after();
+          // P of keys 64 hf + j sits in columns 64 hf + j / 2 of the score buffer
+          const uint32_t pa = tmem + (uint32_t)sbuf * BN;
+          const uint32_t va = v_lo + vs * (L::NP * L::KP >> 4);
+#pragma unroll
+          for (int s = 0; s < BN / 16; ++s)
+            tc_mma_f16_ts(tmem + kOCol, pa + (s < 4 ? 8 * s : 64 + 8 * (s - 4)), va + 128 * s, hi,
+                          idO, started | (uint32_t)s);
+          started = 1;
+          ++executed;
+          tc_commit(bar(L::B_PD + sbuf));
+          tc_commit(bar(L::B_VE + vs));
+        } else {
+          mbar_arrive(bar(L::B_PD + sbuf));
+          mbar_arrive(bar(L::B_VE + vs));
+        }
+        if (++vs == VST) { vs = 0; vph ^= 1; }
+        return true;
+      };
+      bool ok = mbar_wait(bar(L::B_Q), 0, abort_flag);
+      int ks = 0, kph = 0;
+      for (int tt = 0; ok && tt < 2 * nt; ++tt) {
+        const int sbuf = tt % SBUF, use = tt / SBUF;
+        if (!(ok = mbar_wait(bar(L::B_KF + ks), kph, abort_flag))) break;
+        // the score buffer was read by the rows (previous use) ...
+        if (!(ok = mbar_wait(bar(L::B_SR + sbuf), (use & 1) ^ 1, abort_flag))) break;
+        // ... and, when that use was a pass-2 tile, its P was consumed by P.V
+        if (tt - SBUF >= nt) {
+          if (!(ok = mbar_wait(bar(L::B_PD + sbuf), (pd_par >> sbuf) & 1, abort_flag))) break;
+          pd_par ^= 1u << sbuf;
+        }
+        tc_fence_after();
+        const uint32_t ka = k_lo + ks * (L::NP * L::KP >> 4);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+          tc_mma_f16_w(tmem + (uint32_t)sbuf * BN, q_lo + (s >> 2) * (L::QP >> 4) + 2 * (s & 3),
+                       ka + (s >> 2) * (L::KP >> 4) + 2 * (s & 3), hi, idS, (uint32_t)s);
+        tc_commit(bar(L::B_SF + sbuf));
+        tc_commit(bar(L::B_KE + ks));
+        if (++ks == KST) { ks = 0; kph ^= 1; }
+        if (tt - 1 >= nt) ok = pv(tt - 1 - nt);
+      }
+      if (ok) ok = pv(nt - 1);
+      if (ok) {
+        *o_written = (int)started;
+        tc_commit(bar(L::B_O));
+        mbar_arrive(bar(L::B_O));
+      }
+      tc_commit(bar(L::B_DRAIN));
+      const bool drained = mbar_wait_drain(bar(L::B_DRAIN), 0);
+      if (!ok || !drained) set_status(p.status, TOPT_ETIMEOUT);
+      if (p.tiles) {
+        atomicAdd(p.tiles + 0, executed);
+        atomicAdd(p.tiles + 1, (unsigned long long)nt);
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- query rows
+    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows) and columns
+    // 64 (w / 4) .. + 63 of each score tile: each row is split in two halves.
+    const int quad = warp & 3, hf = warp >> 2;
+    const int r = quad * 32 + lane;
+    const int i = row0 + r;
+    const bool row_ok = i < p.S;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + 64u * hf;
+    const float c2 = p.sm_scale * kLog2e;
+    bool ok = true;
+
+    // pass 1: m2 = max_j a_j log2(e), z = sum_j 2^(a_j log2(e) - m2) over this half
+    float m2 = -CUDART_INF_F, z = 0.f;
+    for (int t = 0; t < nt; ++t) {
+      const int sbuf = t % SBUF;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld64(trow + (uint32_t)sbuf * BN, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
+      const int lim = i - t * BN - 64 * hf;  // columns c <= lim of this half are visible
+      if (!__all_sync(0xffffffffu, lim >= 63)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) v[c] = __float_as_uint(-CUDART_INF_F);
+      }
+      float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+      const float mn = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
+      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden half so far
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), c2, -mref));
+      z = z * ex2(m2 - mref) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+      m2 = mn;
+    }
+    // merge the two halves of the row (both threads get bit-identical m2, z;
+    // every row thread reaches this barrier, also after an abort)
+    {
+      float2* xch = reinterpret_cast<float2*>(gb + L::XCH1);
+      xch[hf * BM + r] = make_float2(m2, z);
+      rows_sync();
+      const float2 o = xch[(hf ^ 1) * BM + r];
+      const float M = fmaxf(m2, o.x);
+      z = z * ex2(m2 - M) + o.y * ex2(o.x - M);
+      m2 = M;
+    }
+    const float m = m2 * kLn2;
+    const int Lrow = i + 1;
+    const float th = row_ok ? p.theta[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)] : 0.f;
+    const float bound = score_bound(p.mode, th, m, z);
+    const float braw = bound / p.sm_scale;  // keep iff raw score >= braw
+
+    // pass 2: keep on visible keys; P = exp(a - m) where kept, 0 elsewhere,
+    // written as fp16 pairs over the first half of this thread's columns
+    float R = 0.f;
+    int cnt = 0;
+    uint32_t* mrow = (p.mask && row_ok) ? p.mask + ((size_t)bh_q * p.S + i) * p.mask_words : nullptr;
+    for (int u = 0; ok && u < nt; ++u) {
+      const int t = nt + u, sbuf = t % SBUF, pb = u & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld64(trow + (uint32_t)sbuf * BN, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
+      const int lim = row_ok ? i - u * BN - 64 * hf : -1;
+      uint32_t k0 = 0u, k1 = 0u;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        k0 |= (uint32_t)(__uint_as_float(v[c]) >= braw) << c;
+        k1 |= (uint32_t)(__uint_as_float(v[c + 32]) >= braw) << c;
+      }
+      k0 &= vis_mask(lim);
+      k1 &= vis_mask(lim - 32);
+      const unsigned any = __ballot_sync(0xffffffffu, (k0 | k1) != 0u);
+      uint32_t w[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = ((j < 4 ? k0 : k1) >> (8 * (j & 3))) & 0xffu;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[4 * j + e] = 0u;
+        if (__any_sync(0xffffffffu, bits != 0u)) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * j + 2 * e;
+            const float p0 = (bits >> (2 * e)) & 1u ? ex2(fmaf(__uint_as_float(v[c]), c2, -m2)) : 0.f;
+            const float p1 =
+                (bits >> (2 * e + 1)) & 1u ? ex2(fmaf(__uint_as_float(v[c + 1]), c2, -m2)) : 0.f;
+            w[4 * j + e] = half2_bits(p0, p1, R);
+          }
+        }
+      }
+      tmem_st32(trow + (uint32_t)sbuf * BN, w);
+      tc_fence_before();
+      if (lane == 0) anyf[pb * kRowWarps + warp] = any != 0u ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_PF + pb));
+      cnt += __popc(k0) + __popc(k1);
+      if (mrow) {
+        const int w0 = 4 * u + 2 * hf;
+        if (w0 < p.mask_words) mrow[w0] = k0;
+        if (w0 + 1 < p.mask_words) mrow[w0 + 1] = k1;
+      }
+    }
+    if (mrow)
+      for (int wd = 4 * nt + 2 * hf; wd < p.mask_words; wd += 4) {
+        mrow[wd] = 0u;
+        if (wd + 1 < p.mask_words) mrow[wd + 1] = 0u;
+      }
+    // merge R and the kept count of the two halves (every row thread reaches
+    // this barrier, also after an abort)
+    {
+      float2* xch = reinterpret_cast<float2*>(gb + L::XCH2);
+      xch[hf * BM + r] = make_float2(R, __int_as_float(cnt));
+      rows_sync();
+      const float2 o = xch[(hf ^ 1) * BM + r];
+      R = R + o.x;
+      cnt += __float_as_int(o.y);
+    }
+
+    // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7]
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_O), 0, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const bool have_o = *o_written != 0;
+      float sc = 0.f, beta = 0.f;
+      if (row_ok) out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, Lrow, cnt, sc, beta);
+      const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
+      float* orow = p.out + ((size_t)bh_q * p.S + i) * D;
+      const float* murow = p.vmc ? p.mu + ((size_t)bh_kv * p.S + i) * D : nullptr;
+      const uint32_t orow_t = tmem + ((uint32_t)(quad * 32) << 16) + kOCol;
+#pragma unroll
+      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(orow_t + c0, o);
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            float4 val;
+            val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
+            val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
+            val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
+            val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
+            if (murow) {
+              const float4 mu4 = *reinterpret_cast<const float4*>(murow + c0 + c);
+              val.x = fmaf(beta, mu4.x, val.x);
+              val.y = fmaf(beta, mu4.y, val.y);
+              val.z = fmaf(beta, mu4.z, val.z);
+              val.w = fmaf(beta, mu4.w, val.w);
+            }
+            *reinterpret_cast<float4*>(orow + c0 + c) = val;
+          }
+        }
+      }
+      if (row_ok && hf == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) set_status(p.status, TOPT_ETIMEOUT);
+}
+
+// ------------------------------------------------------ fp16 copy of V --
+// Largest |v| of each (batch, kv head) into vmax (float bits; zeroed first).
+template <int D>
+__global__ void __launch_bounds__(256) vabsmax_kernel(const uint4* __restrict__ v, int S,
+                                                      uint32_t* __restrict__ vmax) {
+  const int bh = blockIdx.y;
+  const size_t n16 = (size_t)S * D / 8;
+  const uint4* src = v + (size_t)bh * n16;
+  float mx = 0.f;
+  for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < n16;
+       w += (size_t)gridDim.x * blockDim.x) {
+    const uint4 x = ld_nc16(src + w);
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x))),
+                         fmaxf(fabsf(bf16lo(x.y)), fabsf(bf16hi(x.y)))));
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(x.z)), fabsf(bf16hi(x.z))),
+                         fmaxf(fabsf(bf16lo(x.w)), fabsf(bf16hi(x.w)))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, wmax[w]);
+    atomicMax(vmax + bh, __float_as_uint(mx));  // mx >= 0: integer order = float order
+  }
+}
+
+// e with max|v| 2^-e in [2^14, 2^15) (0 for an all-zero or non-finite head).
+__device__ __forceinline__ int v16_exponent(uint32_t maxbits) {
+  const float mx = __uint_as_float(maxbits);
+  if (!(mx > 0.f) || !(mx <= 3.4e38f)) return 0;
+  return min(max(ilogbf(mx) - 14, -110), 110);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) v16_kernel(const uint4* __restrict__ v, int S,
+                                                  const uint32_t* __restrict__ vmax,
+                                                  uint4* __restrict__ v16, int32_t* __restrict__ vexp) {
+  const int bh = blockIdx.y;
+  const size_t n16 = (size_t)S * D / 8;
+  const int e = v16_exponent(vmax[bh]);
+  const float scale = __int_as_float((127 - e) << 23);
+  const uint4* src = v + (size_t)bh * n16;
+  uint4* dst = v16 + (size_t)bh * n16;
+  for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < n16;
+       w += (size_t)gridDim.x * blockDim.x) {
+    const uint4 x = ld_nc16(src + w);
+    uint4 y;
+    y.x = pack_half2(bf16lo(x.x) * scale, bf16hi(x.x) * scale);
+    y.y = pack_half2(bf16lo(x.y) * scale, bf16hi(x.y) * scale);
+    y.z = pack_half2(bf16lo(x.z) * scale, bf16hi(x.z) * scale);
+    y.w = pack_half2(bf16lo(x.w) * scale, bf16hi(x.w) * scale);
+    dst[w] = y;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) vexp[bh] = e;
+}
+
+// ------------------------------------------------------------ tensor maps --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [BH][S][D] 16-bit tensor; boxes of 64 elements x `rows` rows x 1, 128-byte
+// swizzle; rows beyond S read as zero.
+bool tensor_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int D, int S, int BH,
+                int rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint32_t* vmax,
+                  int32_t* vexp, cudaStream_t s) {
+  const int BHkv = a.batch * a.n_kv_heads;
+  // fp16 copy of V scaled per head
+  cudaError_t e = cudaMemsetAsync(vmax, 0, sizeof(uint32_t) * BHkv, s);
+  if (e != cudaSuccess) return e;
+  const size_t n16 = (size_t)a.seq * D / 8;
+  const int chunks = (int)std::min<size_t>(64, (n16 + 1023) / 1024);
+  vabsmax_kernel<D><<<dim3(chunks, BHkv), 256, 0, s>>>(static_cast<const uint4*>(a.v), a.seq, vmax);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  v16_kernel<D><<<dim3(chunks, BHkv), 256, 0, s>>>(static_cast<const uint4*>(a.v), a.seq, vmax,
+                                                   static_cast<uint4*>(v16), vexp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tv;
+  if (!tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
+      !tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, D, a.seq, BHkv, BN) ||
+      !tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v16, D, a.seq, BHkv, BN))
+    return cudaErrorInvalidValue;
+  const int smem = (int)TcLayout<D>::ALLOC;
+  if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  const unsigned grid = (unsigned)((size_t)p.nqb * a.n_q_heads * a.batch);
+  if ((e = record_event(a.events[0], s)) != cudaSuccess) return e;
+  prefill_tc_kernel<D><<<grid, kTcThreads, smem, s>>>(tq, tk, tv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return record_event(a.events[1], s);
+}
+
+}  // namespace
+
+size_t prefill_tc_v16_bytes(const topt_prefill_args& a) {
+  return (size_t)a.batch * a.n_kv_heads * a.seq * a.head_dim * 2;
+}
+
+int prefill_tc_rows() { return BM; }
+int prefill_tc_keys() { return BN; }
+
+cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
+                           const float* mu, cudaStream_t s) {
+  TcParams p;
+  p.B = a.batch;
+  p.Hq = a.n_q_heads;
+  p.Hkv = a.n_kv_heads;
+  p.S = a.seq;
+  p.Lmax = a.theta_len;
+  p.mode = a.mode;
+  p.sdc = a.sdc;
+  p.vmc = a.vmc;
+  p.mask_words = (a.seq + 31) / 32;
+  p.nqb = (a.seq + BM - 1) / BM;
+  p.gamma = a.gamma;
+  p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
+  p.theta = a.theta;
+  p.out = a.out;
+  p.kept = a.kept;
+  p.mask = a.mask;
+  p.tiles = a.tiles;
+  p.status = a.status;
+  p.mu = mu;
+  p.vexp = vexp;
+  return a.head_dim == 128 ? run_d<128>(a, p, v16, vmax, vexp, s) : run_d<64>(a, p, v16, vmax, vexp, s);
+}
+
+}  // namespace topt

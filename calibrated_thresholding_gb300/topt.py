@@ -47,7 +47,7 @@ class PrefillArgs(ctypes.Structure):
                 ("seq", i32), ("theta_len", i32), ("dtype", i32), ("mode", i32), ("sdc", i32),
                 ("vmc", i32), ("gamma", f32), ("q", vp), ("k", vp), ("v", vp), ("theta", vp),
                 ("out", vp), ("kept", vp), ("mask", vp), ("tiles", vp), ("status", vp),
-                ("workspace", vp), ("workspace_bytes", sz)]
+                ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 2)]
 
 
 class CalibArgs(ctypes.Structure):

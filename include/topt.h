@@ -155,6 +155,10 @@ typedef struct {
   int32_t* status;
   void* workspace;
   size_t workspace_bytes;
+  /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
+   * `stream` right before [0] and right after [1] the attention kernel (after
+   * the preparation kernels: prefix means, fp16 copy of V). */
+  void* events[2];
 } topt_prefill_args;
 
 topt_status topt_prefill_workspace(const topt_prefill_args* args, size_t* bytes);

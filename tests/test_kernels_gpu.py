@@ -220,9 +220,14 @@ PREFILL_MODES = [
 ]
 
 
-@pytest.mark.parametrize("d,dtype", [(64, torch.float32), (128, torch.bfloat16), (64, torch.bfloat16)])
-def test_prefill_matches_oracle(d, dtype):
-    B, Hq, Hkv, S, k = 2, 4, 2, 100, 8
+@pytest.mark.parametrize("d,dtype,B,Hq,Hkv,S", [
+    (64, torch.float32, 2, 4, 2, 100),
+    (128, torch.bfloat16, 2, 4, 2, 100),
+    (64, torch.bfloat16, 2, 4, 2, 100),
+    (128, torch.bfloat16, 1, 4, 1, 300),    # three 128-row blocks, ragged last block and key tile
+])
+def test_prefill_matches_oracle(d, dtype, B, Hq, Hkv, S):
+    k = 8
     Q, K, V = prefill_case(71, B, Hq, Hkv, d, S, dtype)
     for mode, sdc, vmc in PREFILL_MODES:
         theta, _ = calibrate_prefill_rows(72, 2, Hq, Hkv, d, S, k, mode, 80, dtype=dtype)
