@@ -6,14 +6,16 @@
 // calibrated threshold theta[h][i] ([TopTheta §3, Fig. 1]), SDC [Eq. 4] and
 // VMC [Eq. 5-7] normalise the output as in the CUDA-core variant.
 //
-// One CTA = 128 query rows of one (batch, head); ten warps:
-//   warps 0-7  two threads per query row (the row is its TMEM lane; warps w
-//              and w+4 share a lane quadrant and take 64 of the tile's 128
-//              columns each): pass 1 row maximum and sum, pass 2 threshold
-//              and P, epilogue
-//   warp 8     TMA producer: the Q block once, K tiles for both passes, V
+// One CTA = 128 query rows of one (batch, head); nineteen warps:
+//   warps 0-15 four threads per query row (the row is its TMEM lane; warps
+//              w, w+4, w+8, w+12 share a lane quadrant and take 32 of the
+//              tile's 128 columns each): pass 1 row maximum and sum, pass 2
+//              threshold and P, epilogue
+//   warp 16    TMA producer: the Q block once, K tiles for both passes, V
 //              tiles for pass 2 (128-byte swizzled boxes of 64 elements)
-//   warp 9     TMEM allocation; lane 0 issues tcgen05.mma
+//   warp 17    TMEM allocation; lane 0 issues the QK^T tcgen05.mma
+//   warp 18    lane 0 issues the P.V tcgen05.mma (two issuing threads, so the
+//              barrier bookkeeping of one overlaps the MMAs of the other)
 // Scores S = Q K^T (128 rows x 128 keys, fp32) rotate through three TMEM
 // buffers so the tensor core computes the next tiles while the row threads
 // read one.  The output accumulator O (128 x d, fp32) stays in TMEM for the
@@ -44,13 +46,16 @@ using namespace tc;
 
 constexpr int BM = 128;          // query rows per CTA = TMEM lanes
 constexpr int BN = 128;          // keys per tile
-constexpr int KST = 3;           // K ring stages
+constexpr int KST = 3;           // K ring stages (= score buffers: a finished QK^T frees both)
 constexpr int VST = 2;           // V ring stages
 constexpr int SBUF = 3;          // score buffers in TMEM
-constexpr int kRowWarps = 8;     // two warps per TMEM lane quadrant, 64 columns each
+constexpr int kRowWarps = 16;    // four warps per TMEM lane quadrant
+constexpr int kParts = kRowWarps / 4;  // parts of a score row (one per warp of a quadrant)
+constexpr int CP = BN / kParts;        // score columns of one part
 constexpr int kProducerWarp = kRowWarps;
-constexpr int kMmaWarp = kRowWarps + 1;
-constexpr int kTcThreads = 32 * (kRowWarps + 2);
+constexpr int kMmaWarp = kRowWarps + 1;    // issues QK^T; allocates TMEM
+constexpr int kPvWarp = kRowWarps + 2;     // issues P.V
+constexpr int kTcThreads = 32 * (kRowWarps + 3);
 constexpr uint32_t kTmemCols = 512;  // score buffers at columns 0, 128, 256; O at 384
 constexpr uint32_t kOCol = 384;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,21 +73,24 @@ struct TcLayout {
   static constexpr uint32_t K = Q + NP * QP;
   static constexpr uint32_t V = K + KST * NP * KP;
   static constexpr uint32_t BAR = V + VST * NP * KP;
-  // barriers: Q full; K full/empty; V full/empty; S full; S read by the rows;
-  // P.V done (frees a score buffer holding P); P full; O ready; MMA drain
-  static constexpr int B_Q = 0, B_KF = 1, B_KE = B_KF + KST, B_VF = B_KE + KST,
-                       B_VE = B_VF + VST, B_SF = B_VE + VST, B_SR = B_SF + SBUF,
-                       B_PD = B_SR + SBUF, B_PF = B_PD + SBUF, B_O = B_PF + 2, B_DRAIN = B_O + 1,
-                       NBAR = B_DRAIN + 1;
-  // misc words: abort flag, TMEM address, O written; any-kept flags [2][8] bytes
+  // barriers: Q full; K full; V full/empty; S full (the QK^T of a score
+  // buffer finished, which also frees the K stage of the same index); S read
+  // by the rows; P.V done (frees a score buffer holding P); P full; O ready;
+  // drains of the two MMA threads
+  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + KST, B_VE = B_VF + VST,
+                       B_SF = B_VE + VST, B_SR = B_SF + SBUF, B_PD = B_SR + SBUF,
+                       B_PF = B_PD + SBUF, B_O = B_PF + SBUF, B_DRAIN = B_O + 1,
+                       NBAR = B_DRAIN + 2;
+  // misc words: abort flag, TMEM address, O written; any-kept flags [SBUF][kRowWarps] bytes
   static constexpr uint32_t MISC = BAR + NBAR * 8;
   static constexpr uint32_t ANY = (MISC + 16 + 7) & ~7u;
-  // row statistics of the two half-rows: [2 halves][BM] float2, twice
-  static constexpr uint32_t XCH1 = ANY + 2 * kRowWarps;
-  static constexpr uint32_t XCH2 = XCH1 + 2 * BM * 8;
-  static constexpr uint32_t BYTES = XCH2 + 2 * BM * 8;
+  // row statistics of the parts of each row: [kParts][BM] float2, twice
+  static constexpr uint32_t XCH1 = ANY + SBUF * kRowWarps;
+  static constexpr uint32_t XCH2 = XCH1 + kParts * BM * 8;
+  static constexpr uint32_t BYTES = XCH2 + kParts * BM * 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;  // room to align the base
-  static_assert(kRowWarps == 8, "one 8-byte word of any-kept flags per P buffer");
+  static_assert(kRowWarps % 8 == 0, "8-byte words of any-kept flags per P buffer");
+  static_assert(KST == SBUF, "a K stage is freed by the QK^T of the score buffer of the same index");
   static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
@@ -99,26 +107,14 @@ struct TcParams {
   const int32_t* vexp;   // [B * Hkv] exponent e of the fp16 V copy (V16 = V 2^-e)
 };
 
-// Barrier of the 256 row threads (warps 0-7) only.
-__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier of the row threads only.
+__device__ __forceinline__ void rows_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kRowWarps) : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// fp16 pair of (lo, hi); adds the rounded values to sum, so that R sums the
-// very weights P.V multiplies.
-__device__ __forceinline__ uint32_t half2_bits(float lo, float hi, float& sum) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  const float2 back = __half22float2(h);
-  sum += back.x + back.y;
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Visible-column mask of 32 columns when columns c <= lim are visible.
-__device__ __forceinline__ uint32_t vis_mask(int lim) {
-  return lim >= 31 ? 0xffffffffu : (lim < 0 ? 0u : ((2u << lim) - 1u));
 }
 
 template <int D>
@@ -133,7 +129,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::MISC);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gb + L::MISC + 4);
   volatile int* o_written = reinterpret_cast<volatile int*>(gb + L::MISC + 8);
-  volatile uint8_t* anyf = reinterpret_cast<volatile uint8_t*>(gb + L::ANY);  // [2][kRowWarps]
+  volatile uint8_t* anyf = reinterpret_cast<volatile uint8_t*>(gb + L::ANY);  // [SBUF][kRowWarps]
   auto bar = [sb](int i) -> uint32_t { return sb + L::BAR + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,7 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
-      const bool per_warp = (i >= L::B_SR && i < L::B_SR + SBUF) || i == L::B_PF || i == L::B_PF + 1;
+      const bool per_warp = (i >= L::B_SR && i < L::B_SR + SBUF) || (i >= L::B_PF && i < L::B_PF + SBUF);
       mbar_init(bar(i), per_warp ? kRowWarps : (i == L::B_O ? 2 : 1));
     }
     *abort_flag = 0;
@@ -180,7 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_3d(sb + L::Q + pn * L::QP, &tmQ, bar(L::B_Q), 64 * pn, row0, bh_q);
       for (int tt = 0; tt < 2 * nt; ++tt) {
         const int kt = tt < nt ? tt : tt - nt;
-        if (!mbar_wait(bar(L::B_KE + ks), kph ^ 1, abort_flag)) break;
+        if (!mbar_wait(bar(L::B_SF + ks), kph ^ 1, abort_flag)) break;
         mbar_expect_tx(bar(L::B_KF + ks), L::NP * L::KP);
         for (int pn = 0; pn < L::NP; ++pn)
           tma_load_3d(sb + L::K + (ks * L::NP + pn) * L::KP, &tmK, bar(L::B_KF + ks), 64 * pn,
@@ -207,33 +203,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------------- MMA
+    // ------------------------------------------------------------ QK^T MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(BN, 1, 1, 0);  // bf16 Q, bf16 K (K-major)
-      constexpr uint32_t idO = idesc_f16(D, 0, 0, 1);   // fp16 P (TMEM), fp16 V (N-major)
       // descriptor words: every shared operand has 8-row groups 1024 bytes apart
       constexpr uint32_t hi = sdesc_hi(1024);
       const uint32_t q_lo = sdesc_lo(sb + L::Q, 16);
       const uint32_t k_lo = sdesc_lo(sb + L::K, 16);
+      uint32_t pd_par = 0;  // per score buffer: parity of its next P.V-done phase
+      bool ok = mbar_wait(bar(L::B_Q), 0, abort_flag);
+      int sbuf = 0, use = 0;  // score buffer (= K stage) of tile tt and its use count
+      for (int tt = 0; ok && tt < 2 * nt; ++tt) {
+        if (!(ok = mbar_wait(bar(L::B_KF + sbuf), use & 1, abort_flag))) break;
+        if (tt >= SBUF) {
+          if (tt - SBUF >= nt) {
+            // the buffer held P of a pass-2 tile: P.V done (the rows read S
+            // before they wrote P)
+            ok = mbar_wait(bar(L::B_PD + sbuf), (pd_par >> sbuf) & 1, abort_flag);
+            pd_par ^= 1u << sbuf;
+          } else {
+            ok = mbar_wait(bar(L::B_SR + sbuf), (use & 1) ^ 1, abort_flag);
+          }
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t ka = k_lo + sbuf * (L::NP * L::KP >> 4);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+          tc_mma_f16_w(tmem + (uint32_t)sbuf * BN, q_lo + (s >> 2) * (L::QP >> 4) + 2 * (s & 3),
+                       ka + (s >> 2) * (L::KP >> 4) + 2 * (s & 3), hi, idS, (uint32_t)s);
+        tc_commit(bar(L::B_SF + sbuf));
+        if (++sbuf == SBUF) { sbuf = 0; ++use; }
+      }
+      tc_commit(bar(L::B_DRAIN));
+      const bool drained = mbar_wait_drain(bar(L::B_DRAIN), 0);
+      if (!ok || !drained) set_status(p.status, TOPT_ETIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------- P.V MMA
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_f16(D, 0, 0, 1);  // fp16 P (TMEM), fp16 V (N-major)
+      constexpr uint32_t hi = sdesc_hi(1024);
       const uint32_t v_lo = sdesc_lo(sb + L::V, L::KP);
       volatile unsigned long long* any8 = reinterpret_cast<volatile unsigned long long*>(anyf);
-      uint32_t started = 0;
+      uint32_t started = 0, pf_par = 0;
       unsigned long long executed = 0;
-      int vs = 0, vph = 0;            // V stage and phase of the next P.V
-      uint32_t pd_par = 0;            // per score buffer: parity of its next P.V-done phase
-      auto pv = [&](int u) -> bool {
-        const int t = nt + u, sbuf = t % SBUF, pb = u & 1;
-        if (!mbar_wait(bar(L::B_PF + pb), (u >> 1) & 1, abort_flag)) return false;
-        const bool any = any8[pb] != 0ull;
-        if (!mbar_wait(bar(L::B_VF + vs), vph, abort_flag)) return false;
+      int vs = 0, vph = 0;  // V stage and phase
+      bool ok = true;
+      for (int u = 0; ok && u < nt; ++u) {
+        const int sbuf = (nt + u) % SBUF;
+        if (!(ok = mbar_wait(bar(L::B_PF + sbuf), (pf_par >> sbuf) & 1, abort_flag))) break;
+        pf_par ^= 1u << sbuf;
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < kRowWarps / 8; ++q) any |= any8[sbuf * (kRowWarps / 8) + q] != 0ull;
+        if (!(ok = mbar_wait(bar(L::B_VF + vs), vph, abort_flag))) break;
         if (any) {
           tc_fence_after();
-          // P of keys 64 hf + j sits in columns 64 hf + j / 2 of the score buffer
+          // P of key j = CP q + c sits in column CP q + c / 2 of the score buffer
           const uint32_t pa = tmem + (uint32_t)sbuf * BN;
           const uint32_t va = v_lo + vs * (L::NP * L::KP >> 4);
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s)
-            tc_mma_f16_ts(tmem + kOCol, pa + (s < 4 ? 8 * s : 64 + 8 * (s - 4)), va + 128 * s, hi,
+            tc_mma_f16_ts(tmem + kOCol, pa + CP * (16 * s / CP) + (16 * s % CP) / 2, va + 128 * s, hi,
                           idO, started | (uint32_t)s);
           started = 1;
           ++executed;
@@ -244,39 +277,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(bar(L::B_VE + vs));
         }
         if (++vs == VST) { vs = 0; vph ^= 1; }
-        return true;
-      };
-      bool ok = mbar_wait(bar(L::B_Q), 0, abort_flag);
-      int ks = 0, kph = 0;
-      for (int tt = 0; ok && tt < 2 * nt; ++tt) {
-        const int sbuf = tt % SBUF, use = tt / SBUF;
-        if (!(ok = mbar_wait(bar(L::B_KF + ks), kph, abort_flag))) break;
-        // the score buffer was read by the rows (previous use) ...
-        if (!(ok = mbar_wait(bar(L::B_SR + sbuf), (use & 1) ^ 1, abort_flag))) break;
-        // ... and, when that use was a pass-2 tile, its P was consumed by P.V
-        if (tt - SBUF >= nt) {
-          if (!(ok = mbar_wait(bar(L::B_PD + sbuf), (pd_par >> sbuf) & 1, abort_flag))) break;
-          pd_par ^= 1u << sbuf;
-        }
-        tc_fence_after();
-        const uint32_t ka = k_lo + ks * (L::NP * L::KP >> 4);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s)
-          tc_mma_f16_w(tmem + (uint32_t)sbuf * BN, q_lo + (s >> 2) * (L::QP >> 4) + 2 * (s & 3),
-                       ka + (s >> 2) * (L::KP >> 4) + 2 * (s & 3), hi, idS, (uint32_t)s);
-        tc_commit(bar(L::B_SF + sbuf));
-        tc_commit(bar(L::B_KE + ks));
-        if (++ks == KST) { ks = 0; kph ^= 1; }
-        if (tt - 1 >= nt) ok = pv(tt - 1 - nt);
       }
-      if (ok) ok = pv(nt - 1);
       if (ok) {
         *o_written = (int)started;
         tc_commit(bar(L::B_O));
         mbar_arrive(bar(L::B_O));
       }
-      tc_commit(bar(L::B_DRAIN));
-      const bool drained = mbar_wait_drain(bar(L::B_DRAIN), 0);
+      tc_commit(bar(L::B_DRAIN + 1));
+      const bool drained = mbar_wait_drain(bar(L::B_DRAIN + 1), 0);
       if (!ok || !drained) set_status(p.status, TOPT_ETIMEOUT);
       if (p.tiles) {
         atomicAdd(p.tiles + 0, executed);
@@ -287,54 +295,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // --------------------------------------------------------- query rows
     // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows) and columns
-    // 64 (w / 4) .. + 63 of each score tile: each row is split in two halves.
-    const int quad = warp & 3, hf = warp >> 2;
+    // CP (w / 4) .. + CP - 1 of each score tile: each row is split in kParts.
+    const int quad = warp & 3, part = warp >> 2;
     const int r = quad * 32 + lane;
     const int i = row0 + r;
     const bool row_ok = i < p.S;
-    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + 64u * hf;
+    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(CP * part);
     const float c2 = p.sm_scale * kLog2e;
     bool ok = true;
 
-    // pass 1: m2 = max_j a_j log2(e), z = sum_j 2^(a_j log2(e) - m2) over this half
+    // pass 1: m2 = max_j a_j log2(e), z = sum_j 2^(a_j log2(e) - m2) over this part
     float m2 = -CUDART_INF_F, z = 0.f;
     for (int t = 0; t < nt; ++t) {
       const int sbuf = t % SBUF;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld64(trow + (uint32_t)sbuf * BN, v);
+      uint32_t v[CP];
+      tmem_ld<CP>(trow + (uint32_t)sbuf * BN, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
-      const int lim = i - t * BN - 64 * hf;  // columns c <= lim of this half are visible
-      if (!__all_sync(0xffffffffu, lim >= 63)) {
+      const int lim = i - t * BN - CP * part;  // columns c <= lim of this part are visible
+      if (!__all_sync(0xffffffffu, lim >= CP - 1)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < CP; ++c)
           if (c > lim) v[c] = __float_as_uint(-CUDART_INF_F);
       }
       float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+      for (int c = 0; c < CP; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
       const float mn = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
-      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden half so far
+      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden part so far
       float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), c2, -mref));
+      for (int c = 0; c < CP; ++c) sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), c2, -mref));
       z = z * ex2(m2 - mref) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
       m2 = mn;
     }
-    // merge the two halves of the row (both threads get bit-identical m2, z;
-    // every row thread reaches this barrier, also after an abort)
+    // merge the parts of the row in a fixed order, so every thread of the row
+    // gets bit-identical m2 and z (every row thread reaches this barrier, also
+    // after an abort)
     {
       float2* xch = reinterpret_cast<float2*>(gb + L::XCH1);
-      xch[hf * BM + r] = make_float2(m2, z);
+      xch[part * BM + r] = make_float2(m2, z);
       rows_sync();
-      const float2 o = xch[(hf ^ 1) * BM + r];
-      const float M = fmaxf(m2, o.x);
-      z = z * ex2(m2 - M) + o.y * ex2(o.x - M);
+      float2 o[kParts];
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) o[q] = xch[q * BM + r];
+      float M = o[0].x;
+#pragma unroll
+      for (int q = 1; q < kParts; ++q) M = fmaxf(M, o[q].x);
+      float Z = 0.f;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) Z += o[q].y * ex2(o[q].x - M);
       m2 = M;
+      z = Z;
     }
     const float m = m2 * kLn2;
     const int Lrow = i + 1;
@@ -343,73 +359,92 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float braw = bound / p.sm_scale;  // keep iff raw score >= braw
 
     // pass 2: keep on visible keys; P = exp(a - m) where kept, 0 elsewhere,
-    // written as fp16 pairs over the first half of this thread's columns
-    float R = 0.f;
+    // written as fp16 pairs over the first half of this thread's columns.  R
+    // sums the fp32 weights (P.V multiplies them rounded to fp16: relative
+    // difference below 2^-11 per weight).
+    float R0 = 0.f, R1 = 0.f;
     int cnt = 0;
     uint32_t* mrow = (p.mask && row_ok) ? p.mask + ((size_t)bh_q * p.S + i) * p.mask_words : nullptr;
     for (int u = 0; ok && u < nt; ++u) {
-      const int t = nt + u, sbuf = t % SBUF, pb = u & 1;
+      const int t = nt + u, sbuf = t % SBUF;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld64(trow + (uint32_t)sbuf * BN, v);
+      uint32_t v[CP];
+      tmem_ld<CP>(trow + (uint32_t)sbuf * BN, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
-      const int lim = row_ok ? i - u * BN - 64 * hf : -1;
-      uint32_t k0 = 0u, k1 = 0u;
+      const int lim = row_ok ? i - u * BN - CP * part : -1;
+      if (!__all_sync(0xffffffffu, lim >= CP - 1)) {
+        // hidden keys compare false against any bound (NaN)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        k0 |= (uint32_t)(__uint_as_float(v[c]) >= braw) << c;
-        k1 |= (uint32_t)(__uint_as_float(v[c + 32]) >= braw) << c;
+        for (int c = 0; c < CP; ++c)
+          if (c > lim) v[c] = 0x7fc00000u;
       }
-      k0 &= vis_mask(lim);
-      k1 &= vis_mask(lim - 32);
-      const unsigned any = __ballot_sync(0xffffffffu, (k0 | k1) != 0u);
-      uint32_t w[32];
+      // exponentials only in 8-key chunks where some row of the warp keeps a
+      // key (the chunk maximum against the bound decides)
+      uint32_t w[CP / 2];
+      int tcnt = 0;
+      bool wany = false;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t bits = ((j < 4 ? k0 : k1) >> (8 * (j & 3))) & 0xffu;
+      for (int j = 0; j < CP / 8; ++j) {
+        float cm = __uint_as_float(v[8 * j]);
+#pragma unroll
+        for (int e = 1; e < 8; ++e) cm = fmaxf(cm, __uint_as_float(v[8 * j + e]));
 #pragma unroll
         for (int e = 0; e < 4; ++e) w[4 * j + e] = 0u;
-        if (__any_sync(0xffffffffu, bits != 0u)) {
+        if (__any_sync(0xffffffffu, cm >= braw)) {
+          wany = true;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int c = 8 * j + 2 * e;
-            const float p0 = (bits >> (2 * e)) & 1u ? ex2(fmaf(__uint_as_float(v[c]), c2, -m2)) : 0.f;
-            const float p1 =
-                (bits >> (2 * e + 1)) & 1u ? ex2(fmaf(__uint_as_float(v[c + 1]), c2, -m2)) : 0.f;
-            w[4 * j + e] = half2_bits(p0, p1, R);
+            const float a0 = __uint_as_float(v[8 * j + 2 * e]);
+            const float a1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+            const bool q0 = a0 >= braw, q1 = a1 >= braw;
+            const float e0 = ex2(q0 ? fmaf(a0, c2, -m2) : -CUDART_INF_F);
+            const float e1 = ex2(q1 ? fmaf(a1, c2, -m2) : -CUDART_INF_F);
+            R0 += e0;
+            R1 += e1;
+            tcnt += (int)q0 + (int)q1;
+            w[4 * j + e] = pack_half2(e0, e1);
           }
         }
       }
-      tmem_st32(trow + (uint32_t)sbuf * BN, w);
+      tmem_st<CP / 2>(trow + (uint32_t)sbuf * BN, w);
       tc_fence_before();
-      if (lane == 0) anyf[pb * kRowWarps + warp] = any != 0u ? 1 : 0;
+      if (lane == 0) anyf[sbuf * kRowWarps + warp] = wany ? 1 : 0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_PF + pb));
-      cnt += __popc(k0) + __popc(k1);
+      if (lane == 0) mbar_arrive(bar(L::B_PF + sbuf));
+      cnt += tcnt;
       if (mrow) {
-        const int w0 = 4 * u + 2 * hf;
-        if (w0 < p.mask_words) mrow[w0] = k0;
-        if (w0 + 1 < p.mask_words) mrow[w0 + 1] = k1;
+#pragma unroll
+        for (int q = 0; q < CP / 32; ++q) {
+          uint32_t k = 0u;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) k |= (uint32_t)(__uint_as_float(v[32 * q + c]) >= braw) << c;
+          const int wd = (BN / 32) * u + (CP / 32) * part + q;
+          if (wd < p.mask_words) mrow[wd] = k;
+        }
       }
     }
+    float R = R0 + R1;
     if (mrow)
-      for (int wd = 4 * nt + 2 * hf; wd < p.mask_words; wd += 4) {
-        mrow[wd] = 0u;
-        if (wd + 1 < p.mask_words) mrow[wd + 1] = 0u;
-      }
-    // merge R and the kept count of the two halves (every row thread reaches
-    // this barrier, also after an abort)
+      for (int wd = (BN / 32) * nt + (CP / 32) * part; wd < p.mask_words; wd += BN / 32)
+        for (int q = 0; q < CP / 32 && wd + q < p.mask_words; ++q) mrow[wd + q] = 0u;
+    // merge R and the kept count of the parts, in a fixed order (every row
+    // thread reaches this barrier, also after an abort)
     {
       float2* xch = reinterpret_cast<float2*>(gb + L::XCH2);
-      xch[hf * BM + r] = make_float2(R, __int_as_float(cnt));
+      xch[part * BM + r] = make_float2(R, __int_as_float(cnt));
       rows_sync();
-      const float2 o = xch[(hf ^ 1) * BM + r];
-      R = R + o.x;
-      cnt += __float_as_int(o.y);
+      R = 0.f;
+      cnt = 0;
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) {
+        const float2 o = xch[q * BM + r];
+        R += o.x;
+        cnt += __float_as_int(o.y);
+      }
     }
 
     // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7]
@@ -420,33 +455,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float sc = 0.f, beta = 0.f;
       if (row_ok) out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, Lrow, cnt, sc, beta);
       const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
-      float* orow = p.out + ((size_t)bh_q * p.S + i) * D;
-      const float* murow = p.vmc ? p.mu + ((size_t)bh_kv * p.S + i) * D : nullptr;
-      const uint32_t orow_t = tmem + ((uint32_t)(quad * 32) << 16) + kOCol;
+      constexpr int OC = D / kParts;  // output columns of this thread
+      const int c0 = OC * part;
+      float* orow = p.out + ((size_t)bh_q * p.S + i) * D + c0;
+      const float* murow = p.vmc ? p.mu + ((size_t)bh_kv * p.S + i) * D + c0 : nullptr;
+      uint32_t o[OC];
+      tmem_ld<OC>(tmem + ((uint32_t)(quad * 32) << 16) + kOCol + (uint32_t)c0, o);
+      if (row_ok) {
 #pragma unroll
-      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(orow_t + c0, o);
-        if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            float4 val;
-            val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
-            val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
-            val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
-            val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
-            if (murow) {
-              const float4 mu4 = *reinterpret_cast<const float4*>(murow + c0 + c);
-              val.x = fmaf(beta, mu4.x, val.x);
-              val.y = fmaf(beta, mu4.y, val.y);
-              val.z = fmaf(beta, mu4.z, val.z);
-              val.w = fmaf(beta, mu4.w, val.w);
-            }
-            *reinterpret_cast<float4*>(orow + c0 + c) = val;
+        for (int c = 0; c < OC; c += 4) {
+          float4 val;
+          val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
+          val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
+          val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
+          val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
+          if (murow) {
+            const float4 mu4 = *reinterpret_cast<const float4*>(murow + c);
+            val.x = fmaf(beta, mu4.x, val.x);
+            val.y = fmaf(beta, mu4.y, val.y);
+            val.z = fmaf(beta, mu4.z, val.z);
+            val.w = fmaf(beta, mu4.w, val.w);
           }
+          *reinterpret_cast<float4*>(orow + c) = val;
         }
       }
-      if (row_ok && hf == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
+      if (row_ok && part == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
     }
   }
 
