@@ -134,7 +134,8 @@ topt_status topt_prefill(const topt_prefill_args* a, topt_stream stream) {
   topt_status st = check_prefill_shape(a);
   if (st != TOPT_OK) return st;
   if (!a->q || !a->k || !a->v || !a->theta || !a->out) return TOPT_EINVAL;
-  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v)) return TOPT_EINVAL;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
+    return TOPT_EINVAL;
   if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
   const size_t need = prefill_workspace_bytes(*a);
   if (need > 0 && (!a->workspace || a->workspace_bytes < need ||

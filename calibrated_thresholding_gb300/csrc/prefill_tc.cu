@@ -89,6 +89,8 @@ struct TcLayout {
   static constexpr uint32_t XCH2 = XCH1 + kParts * BM * 8;
   static constexpr uint32_t BYTES = XCH2 + kParts * BM * 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;  // room to align the base
+  static_assert(KST * NP * KP >= BM * (D + 4) * 4, "output staging fits in the K stages");
+  static_assert(kParts * BM * 8 >= BM * 4, "row betas fit in the first exchange area");
   static_assert(kRowWarps % 8 == 0, "8-byte words of any-kept flags per P buffer");
   static_assert(KST == SBUF, "a K stage is freed by the QK^T of the score buffer of the same index");
   static_assert(ALLOC <= 227 * 1024, "shared memory");
@@ -447,7 +449,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
 
-    // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7]
+    // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7].  The
+    // rows stage O * scale in shared memory (the K stages are idle by now),
+    // then all row threads stream the block out with coalesced 16-byte
+    // accesses, adding beta mu on the way.
+    constexpr int SD = D + 4;  // staging row stride in floats (conflict-free float4 writes)
+    float* stage = reinterpret_cast<float*>(gb + L::K);
+    float* betas = reinterpret_cast<float*>(gb + L::XCH1);  // free after the pass-1 merge
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_O), 0, abort_flag));
     if (ok) {
       tc_fence_after();
@@ -457,29 +465,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
       constexpr int OC = D / kParts;  // output columns of this thread
       const int c0 = OC * part;
-      float* orow = p.out + ((size_t)bh_q * p.S + i) * D + c0;
-      const float* murow = p.vmc ? p.mu + ((size_t)bh_kv * p.S + i) * D + c0 : nullptr;
       uint32_t o[OC];
       tmem_ld<OC>(tmem + ((uint32_t)(quad * 32) << 16) + kOCol + (uint32_t)c0, o);
-      if (row_ok) {
 #pragma unroll
-        for (int c = 0; c < OC; c += 4) {
-          float4 val;
-          val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
-          val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
-          val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
-          val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
-          if (murow) {
-            const float4 mu4 = *reinterpret_cast<const float4*>(murow + c);
-            val.x = fmaf(beta, mu4.x, val.x);
-            val.y = fmaf(beta, mu4.y, val.y);
-            val.z = fmaf(beta, mu4.z, val.z);
-            val.w = fmaf(beta, mu4.w, val.w);
-          }
-          *reinterpret_cast<float4*>(orow + c) = val;
-        }
+      for (int c = 0; c < OC; c += 4) {
+        float4 val;
+        val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
+        val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
+        val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
+        val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
+        *reinterpret_cast<float4*>(stage + r * SD + c0 + c) = val;
       }
+      if (part == 0) betas[r] = beta;
       if (row_ok && part == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
+    }
+    rows_sync();  // every row thread reaches it, also after an abort
+    if (!*abort_flag) {
+      const int rows_here = min(BM, p.S - row0);
+      float* out_blk = p.out + ((size_t)bh_q * p.S + row0) * D;
+      const float* mu_blk = p.vmc ? p.mu + ((size_t)bh_kv * p.S + row0) * D : nullptr;
+      for (int idx = threadIdx.x; idx < rows_here * (D / 4); idx += 32 * kRowWarps) {
+        const int rr = idx / (D / 4), c = 4 * (idx % (D / 4));
+        float4 val = *reinterpret_cast<const float4*>(stage + rr * SD + c);
+        if (mu_blk) {
+          const float bt = betas[rr];
+          const float4 mu4 = *reinterpret_cast<const float4*>(mu_blk + (size_t)rr * D + c);
+          val.x = fmaf(bt, mu4.x, val.x);
+          val.y = fmaf(bt, mu4.y, val.y);
+          val.z = fmaf(bt, mu4.z, val.z);
+          val.w = fmaf(bt, mu4.w, val.w);
+        }
+        *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) = val;
+      }
     }
   }
 

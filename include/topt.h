@@ -148,7 +148,8 @@ typedef struct {
   const void* k;        /* [B][Hkv][S][d] */
   const void* v;        /* [B][Hkv][S][d] */
   const float* theta;   /* [Hq][Lmax] */
-  float* out;           /* [B][Hq][S][d] fp32; VMC uses the prefix mean of V rows 0..i */
+  float* out;           /* [B][Hq][S][d] fp32, 16-byte aligned; VMC uses the prefix mean of
+                           V rows 0..i.  q, k, v are 16-byte aligned too. */
   int32_t* kept;        /* [B][Hq][S] k~ per row, or NULL */
   uint32_t* mask;       /* [B][Hq][S][ceil(S/32)] kept bitmap, or NULL */
   unsigned long long* tiles; /* [2] += (P.V tiles executed, causal tiles), or NULL */
