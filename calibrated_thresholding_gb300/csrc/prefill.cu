@@ -1,5 +1,5 @@
-// Top-theta causal prefill: workspace layout and dispatch, the CUDA-core
-// variant (fp32 inputs) and the causal prefix means of V used by VMC.  bf16
+// Top-theta causal prefill: workspace layout and dispatch, and the CUDA-core
+// variant (fp32 inputs) with the causal prefix means of V its VMC uses.  bf16
 // inputs run on the tensor cores (prefill_tc.cu).
 //
 // [TopTheta] = "Top-Theta Attention: Sparsifying Transformers by Compensated
@@ -232,7 +232,7 @@ cudaError_t launch_td(const PrefillParams& p, void* const events[2], cudaStream_
 }
 
 struct PrefillLayout {
-  size_t mu, csum, v16, vmax, vexp, total;
+  size_t mu, csum, v16, vmax, vexp, bsum, total;
 };
 
 PrefillLayout prefill_layout(const topt_prefill_args& a) {
@@ -241,11 +241,14 @@ PrefillLayout prefill_layout(const topt_prefill_args& a) {
   const size_t nchunk = (a.seq + kMeanChunk - 1) / kMeanChunk;
   const bool tc = a.dtype == TOPT_BF16;
   size_t off = 0;
-  l.mu = off;   off += a.vmc ? align256(bh * a.seq * (size_t)a.head_dim * sizeof(float)) : 0;
-  l.csum = off; off += a.vmc ? align256(bh * nchunk * (size_t)a.head_dim * sizeof(float)) : 0;
+  // CUDA-core path: prefix means and chunk sums (VMC)
+  l.mu = off;   off += (!tc && a.vmc) ? align256(bh * a.seq * (size_t)a.head_dim * sizeof(float)) : 0;
+  l.csum = off; off += (!tc && a.vmc) ? align256(bh * nchunk * (size_t)a.head_dim * sizeof(float)) : 0;
+  // tensor-core path: fp16 copy of V, its per-head scale, block column sums (VMC)
   l.v16 = off;  off += tc ? align256(prefill_tc_v16_bytes(a)) : 0;
   l.vmax = off; off += tc ? align256(bh * sizeof(uint32_t)) : 0;
   l.vexp = off; off += tc ? align256(bh * sizeof(int32_t)) : 0;
+  l.bsum = off; off += (tc && a.vmc) ? align256(prefill_tc_bsum_bytes(a)) : 0;
   l.total = off;
   return l;
 }
@@ -284,18 +287,12 @@ cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.tiles = a.tiles;
   p.status = a.status;
-  p.mu = a.vmc ? reinterpret_cast<float*>(ws + l.mu) : nullptr;
-  p.csum = a.vmc ? reinterpret_cast<float*>(ws + l.csum) : nullptr;
-  if (a.dtype == TOPT_BF16) {
-    // prefix means on the CUDA cores, attention on the tensor cores
-    if (a.vmc) {
-      const cudaError_t e = a.head_dim == 128 ? launch_means<__nv_bfloat16, 128>(p, s)
-                                              : launch_means<__nv_bfloat16, 64>(p, s);
-      if (e != cudaSuccess) return e;
-    }
+  p.mu = (a.vmc && a.dtype != TOPT_BF16) ? reinterpret_cast<float*>(ws + l.mu) : nullptr;
+  p.csum = (a.vmc && a.dtype != TOPT_BF16) ? reinterpret_cast<float*>(ws + l.csum) : nullptr;
+  if (a.dtype == TOPT_BF16)
     return prefill_tc_run(a, ws + l.v16, reinterpret_cast<uint32_t*>(ws + l.vmax),
-                          reinterpret_cast<int32_t*>(ws + l.vexp), p.mu, s);
-  }
+                          reinterpret_cast<int32_t*>(ws + l.vexp),
+                          reinterpret_cast<float*>(ws + l.bsum), s);
   return a.head_dim == 128 ? launch_td<float, 128>(p, a.events, s) : launch_td<float, 64>(p, a.events, s);
 }
 

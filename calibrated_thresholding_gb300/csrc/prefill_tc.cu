@@ -91,6 +91,7 @@ struct TcLayout {
   static constexpr uint32_t ALLOC = BYTES + 1024;  // room to align the base
   static_assert(KST * NP * KP >= BM * (D + 4) * 4, "output staging fits in the K stages");
   static_assert(kParts * BM * 8 >= BM * 4, "row betas fit in the first exchange area");
+  static_assert(VST * NP * KP >= (1 + 32 * kRowWarps / (D / 4)) * D * 4, "scan sums fit in the V stages");
   static_assert(kRowWarps % 8 == 0, "8-byte words of any-kept flags per P buffer");
   static_assert(KST == SBUF, "a K stage is freed by the QK^T of the score buffer of the same index");
   static_assert(ALLOC <= 227 * 1024, "shared memory");
@@ -105,9 +106,17 @@ struct TcParams {
   uint32_t* mask;
   unsigned long long* tiles;
   int32_t* status;
-  const float* mu;       // [B][Hkv][S][D] prefix means (when vmc)
+  const uint32_t* v;     // [B][Hkv][S][D] bf16 V (pairs), read by the epilogue when vmc
+  const float* bsum;     // [B * Hkv][nqb][D] column sums of each 128-row block of V (vmc)
   const int32_t* vexp;   // [B * Hkv] exponent e of the fp16 V copy (V16 = V 2^-e)
 };
+
+// Programmatic dependent launch: this grid lets the next one start / waits
+// for the previous one to complete with its memory visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Barrier of the row threads only.
 __device__ __forceinline__ void rows_sync() {
@@ -186,6 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++kcount[ks];
         if (++ks == KST) { ks = 0; kph ^= 1; }
         if (tt >= nt) {
+          if (tt == nt) pdl_wait();  // the fp16 copy of V is written by the previous grid
           if (!mbar_wait(bar(L::B_VE + vs), vph ^ 1, abort_flag)) break;
           mbar_expect_tx(bar(L::B_VF + vs), L::NP * L::KP);
           for (int pn = 0; pn < L::NP; ++pn)
@@ -452,10 +462,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7].  The
     // rows stage O * scale in shared memory (the K stages are idle by now),
     // then all row threads stream the block out with coalesced 16-byte
-    // accesses, adding beta mu on the way.
+    // stores, adding beta mu (prefix means computed here) on the way.
     constexpr int SD = D + 4;  // staging row stride in floats (conflict-free float4 writes)
     float* stage = reinterpret_cast<float*>(gb + L::K);
     float* betas = reinterpret_cast<float*>(gb + L::XCH1);  // free after the pass-1 merge
+    pdl_wait();  // vexp and the block sums come from the preparation grids
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_O), 0, abort_flag));
     if (ok) {
       tc_fence_after();
@@ -480,22 +491,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (row_ok && part == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
     }
     rows_sync();  // every row thread reaches it, also after an abort
-    if (!*abort_flag) {
-      const int rows_here = min(BM, p.S - row0);
-      float* out_blk = p.out + ((size_t)bh_q * p.S + row0) * D;
-      const float* mu_blk = p.vmc ? p.mu + ((size_t)bh_kv * p.S + row0) * D : nullptr;
-      for (int idx = threadIdx.x; idx < rows_here * (D / 4); idx += 32 * kRowWarps) {
-        const int rr = idx / (D / 4), c = 4 * (idx % (D / 4));
-        float4 val = *reinterpret_cast<const float4*>(stage + rr * SD + c);
-        if (mu_blk) {
-          const float bt = betas[rr];
-          const float4 mu4 = *reinterpret_cast<const float4*>(mu_blk + (size_t)rr * D + c);
-          val.x = fmaf(bt, mu4.x, val.x);
-          val.y = fmaf(bt, mu4.y, val.y);
-          val.z = fmaf(bt, mu4.z, val.z);
-          val.w = fmaf(bt, mu4.w, val.w);
+    const int rows_here = min(BM, p.S - row0);
+    float* out_blk = p.out + ((size_t)bh_q * p.S + row0) * D;
+    if (!p.vmc) {
+      if (!*abort_flag)
+        for (int idx = threadIdx.x; idx < rows_here * (D / 4); idx += 32 * kRowWarps) {
+          const int rr = idx / (D / 4), c = 4 * (idx % (D / 4));
+          *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) =
+              *reinterpret_cast<const float4*>(stage + rr * SD + c);
         }
-        *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) = val;
+    } else {
+      // mu_i = (sum of V rows 0..i) / (i + 1): the column sums of the blocks
+      // before this one plus a scan over this block's rows, by segments of
+      // RPS rows (thread: 4 columns x RPS rows), in fp32 from the bf16 V.
+      constexpr int QD = D / 4, NSEG = 32 * kRowWarps / QD, RPS = BM / NSEG;
+      const int c4 = threadIdx.x % QD, seg = threadIdx.x / QD, c = 4 * c4;
+      float* pre = reinterpret_cast<float*>(gb + L::V);  // [D]: V rows 0 .. row0-1
+      float* segsum = pre + D;                           // [NSEG][D]: totals of the segments
+      if (threadIdx.x < D) {
+        const float* bs = p.bsum + (size_t)bh_kv * p.nqb * D + threadIdx.x;
+        float acc = 0.f;
+        for (int q = 0; q < qb; ++q) acc += bs[(size_t)q * D];
+        pre[threadIdx.x] = acc;
+      }
+      float4 run[RPS];
+      float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t* vblk = p.v + ((size_t)bh_kv * p.S + row0) * (D / 2);
+#pragma unroll
+      for (int k = 0; k < RPS; ++k) {
+        const int rr = seg * RPS + k;
+        if (rr < rows_here) {
+          const uint2 x = *reinterpret_cast<const uint2*>(vblk + (size_t)rr * (D / 2) + c / 2);
+          tot.x += bf16lo(x.x);
+          tot.y += bf16hi(x.x);
+          tot.z += bf16lo(x.y);
+          tot.w += bf16hi(x.y);
+        }
+        run[k] = tot;
+      }
+      *reinterpret_cast<float4*>(segsum + seg * D + c) = tot;
+      rows_sync();
+      if (!*abort_flag) {
+        float4 base = *reinterpret_cast<const float4*>(pre + c);
+        for (int q = 0; q < seg; ++q) {
+          const float4 t4 = *reinterpret_cast<const float4*>(segsum + q * D + c);
+          base.x += t4.x;
+          base.y += t4.y;
+          base.z += t4.z;
+          base.w += t4.w;
+        }
+#pragma unroll
+        for (int k = 0; k < RPS; ++k) {
+          const int rr = seg * RPS + k;
+          if (rr < rows_here) {
+            const float inv = 1.f / (float)(row0 + rr + 1);
+            const float bt = betas[rr];
+            float4 val = *reinterpret_cast<const float4*>(stage + rr * SD + c);
+            val.x = fmaf(bt, (base.x + run[k].x) * inv, val.x);
+            val.y = fmaf(bt, (base.y + run[k].y) * inv, val.y);
+            val.z = fmaf(bt, (base.z + run[k].z) * inv, val.z);
+            val.w = fmaf(bt, (base.w + run[k].w) * inv, val.w);
+            *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) = val;
+          }
+        }
       }
     }
   }
@@ -511,30 +569,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ------------------------------------------------------ fp16 copy of V --
-// Largest |v| of each (batch, kv head) into vmax (float bits; zeroed first).
+// One 128-row block of V per CTA: the largest |v| of each (batch, kv head)
+// into vmax (float bits; zeroed first) and, when bsum is given, the column
+// sums of the block into bsum[bh][block][D].
 template <int D>
-__global__ void __launch_bounds__(256) vabsmax_kernel(const uint4* __restrict__ v, int S,
-                                                      uint32_t* __restrict__ vmax) {
-  const int bh = blockIdx.y;
-  const size_t n16 = (size_t)S * D / 8;
-  const uint4* src = v + (size_t)bh * n16;
+__global__ void __launch_bounds__(256) vstats_kernel(const uint4* __restrict__ v, int S,
+                                                     uint32_t* __restrict__ vmax,
+                                                     float* __restrict__ bsum) {
+  constexpr int W = D / 8;  // 16-byte words per row; every thread keeps one word column
+  pdl_launch_dependents();
+  const int qb = blockIdx.x, bh = blockIdx.y;
+  const int r0 = qb * BM, rows = min(BM, S - r0);
+  const uint4* src = v + ((size_t)bh * S + r0) * W;
+  float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float mx = 0.f;
-  for (size_t w = (size_t)blockIdx.x * blockDim.x + threadIdx.x; w < n16;
-       w += (size_t)gridDim.x * blockDim.x) {
+  for (int w = threadIdx.x; w < rows * W; w += blockDim.x) {
     const uint4 x = ld_nc16(src + w);
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x))),
-                         fmaxf(fabsf(bf16lo(x.y)), fabsf(bf16hi(x.y)))));
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo(x.z)), fabsf(bf16hi(x.z))),
-                         fmaxf(fabsf(bf16lo(x.w)), fabsf(bf16hi(x.w)))));
+    const float e[8] = {bf16lo(x.x), bf16hi(x.x), bf16lo(x.y), bf16hi(x.y),
+                        bf16lo(x.z), bf16hi(x.z), bf16lo(x.w), bf16hi(x.w)};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      cs[k] += e[k];
+      mx = fmaxf(mx, fabsf(e[k]));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   __shared__ float wmax[8];
+  __shared__ float part[256][9];
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) part[threadIdx.x][k] = cs[k];
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, wmax[w]);
     atomicMax(vmax + bh, __float_as_uint(mx));  // mx >= 0: integer order = float order
+  }
+  if (bsum && threadIdx.x < D) {
+    const int col = threadIdx.x, wc = col / 8, k = col % 8;
+    float acc = 0.f;
+    for (int t = wc; t < (int)blockDim.x; t += W) acc += part[t][k];
+    bsum[((size_t)bh * gridDim.x + qb) * D + col] = acc;
   }
 }
 
@@ -549,6 +624,8 @@ template <int D>
 __global__ void __launch_bounds__(256) v16_kernel(const uint4* __restrict__ v, int S,
                                                   const uint32_t* __restrict__ vmax,
                                                   uint4* __restrict__ v16, int32_t* __restrict__ vexp) {
+  pdl_wait();  // vmax is complete
+  pdl_launch_dependents();
   const int bh = blockIdx.y;
   const size_t n16 = (size_t)S * D / 8;
   const int e = v16_exponent(vmax[bh]);
@@ -612,11 +689,21 @@ cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint
   if (e != cudaSuccess) return e;
   const size_t n16 = (size_t)a.seq * D / 8;
   const int chunks = (int)std::min<size_t>(64, (n16 + 1023) / 1024);
-  vabsmax_kernel<D><<<dim3(chunks, BHkv), 256, 0, s>>>(static_cast<const uint4*>(a.v), a.seq, vmax);
+  vstats_kernel<D><<<dim3(p.nqb, BHkv), 256, 0, s>>>(static_cast<const uint4*>(a.v), a.seq, vmax,
+                                                     const_cast<float*>(p.bsum));
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  v16_kernel<D><<<dim3(chunks, BHkv), 256, 0, s>>>(static_cast<const uint4*>(a.v), a.seq, vmax,
-                                                   static_cast<uint4*>(v16), vexp);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(chunks, BHkv);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, v16_kernel<D>, static_cast<const uint4*>(a.v), a.seq,
+                              (const uint32_t*)vmax, static_cast<uint4*>(v16), vexp)) != cudaSuccess)
+    return e;
 
   CUtensorMap tq, tk, tv;
   if (!tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
@@ -629,12 +716,20 @@ cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint
     return e;
   const unsigned grid = (unsigned)((size_t)p.nqb * a.n_q_heads * a.batch);
   if ((e = record_event(a.events[0], s)) != cudaSuccess) return e;
-  prefill_tc_kernel<D><<<grid, kTcThreads, smem, s>>>(tq, tk, tv, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // programmatic launch: pass 1 overlaps the preparation grids (a profiling
+  // event in between serialises them, which only moves time between them)
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  if ((e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, tq, tk, tv, p)) != cudaSuccess) return e;
   return record_event(a.events[1], s);
 }
 
 }  // namespace
+
+size_t prefill_tc_bsum_bytes(const topt_prefill_args& a) {
+  return (size_t)a.batch * a.n_kv_heads * ((a.seq + BM - 1) / BM) * a.head_dim * sizeof(float);
+}
 
 size_t prefill_tc_v16_bytes(const topt_prefill_args& a) {
   return (size_t)a.batch * a.n_kv_heads * a.seq * a.head_dim * 2;
@@ -644,7 +739,7 @@ int prefill_tc_rows() { return BM; }
 int prefill_tc_keys() { return BN; }
 
 cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
-                           const float* mu, cudaStream_t s) {
+                           float* bsum, cudaStream_t s) {
   TcParams p;
   p.B = a.batch;
   p.Hq = a.n_q_heads;
@@ -664,7 +759,8 @@ cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax
   p.mask = a.mask;
   p.tiles = a.tiles;
   p.status = a.status;
-  p.mu = mu;
+  p.v = static_cast<const uint32_t*>(a.v);
+  p.bsum = a.vmc ? bsum : nullptr;
   p.vexp = vexp;
   return a.head_dim == 128 ? run_d<128>(a, p, v16, vmax, vexp, s) : run_d<64>(a, p, v16, vmax, vexp, s);
 }
