@@ -52,10 +52,17 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_scores_kernel
-# (one layer call of the default workload), with the hash of the kernel source
-# those counters were taken on.  Reported as null when the source differs.
-DECODE_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture
+# (profiles/decode_kernels_llama3_8b_decode.md, profiles/prefill_tc_kernel_llama3_8b_prefill.md),
+# with the hash of the kernel sources the counters were taken on; reported as
+# null once the sources differ.
+CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
+DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
+                  "source_sha256": "f198d8dfb6df450c3aa3fd9db40c389b2d4338ea5507a8ae9251ce0587e71c51",
+                  "bytes_per_launch": 268611840 + 13363712}   # decode_scores_kernel, one layer call
+PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
+                   "source_sha256": "5371ae7bb87b2d3dfd97eb476a43a0796f42052739f796de41cf461bcc4fe126",
+                   "bytes_per_launch": 59532544 + 22978304}   # prefill_tc_kernel, post-softmax + VMC
 
 
 def parse():
@@ -86,9 +93,16 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def source_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(CSRC, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(rec):
+    return rec["bytes_per_launch"] if source_sha(rec["sources"]) == rec["source_sha256"] else None
 
 
 def hbm_peak():
@@ -388,7 +402,8 @@ def prefill_report(L, wl, dev, stream, steps, warmup):
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                          if kind == "measured" else "fallback 1.9 PFLOP/s",
-                         "traffic": None, "avg_launch_ms": kern * 1e3,
+                         "traffic": recorded_traffic(PREFILL_TRAFFIC) if mode == 1 else None,
+                         "avg_launch_ms": kern * 1e3,
                          "flops_per_launch": useful,
                          "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
                          "issued_tflops": issued / kern / 1e12},
@@ -722,10 +737,7 @@ def main():
     q_bytes = wl.B * wl.Hq * wl.d * 2
     achieved = (k_bytes + q_bytes) / score_avg / 1e9
     call_gbs = alg_bytes / kern_avg / 1e9
-    traffic = None
-    src = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc", "decode.cu")
-    if DECODE_TRAFFIC["source_sha256"] == source_sha(src):
-        traffic = DECODE_TRAFFIC["bytes_per_launch"]
+    traffic = recorded_traffic(DECODE_TRAFFIC)
     vrows_per_group = float(np.mean([state.vrows[l].double().mean().item() for l in range(layers)]))
 
     e2e = None
@@ -824,7 +836,8 @@ def main_prefill(args, dev, rank, local, world):
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                      if kind == "measured" else "fallback 1.9 PFLOP/s",
-                     "traffic": None, "avg_launch_ms": kern * 1e3, "flops_per_launch": useful,
+                     "traffic": recorded_traffic(PREFILL_TRAFFIC), "avg_launch_ms": kern * 1e3,
+                     "flops_per_launch": useful,
                      "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
                      "issued_tflops": issued / kern / 1e12},
         "tiles_executed": tiles[0], "tiles_causal": tiles[1],
