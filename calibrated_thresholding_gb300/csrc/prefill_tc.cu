@@ -6,16 +6,18 @@
 // calibrated threshold theta[h][i] ([TopTheta §3, Fig. 1]), SDC [Eq. 4] and
 // VMC [Eq. 5-7] normalise the output as in the CUDA-core variant.
 //
-// One CTA = 128 query rows of one (batch, head); nineteen warps:
+// One CTA = 128 query rows of one (batch, head); twenty warps:
 //   warps 0-15 four threads per query row (the row is its TMEM lane; warps
 //              w, w+4, w+8, w+12 share a lane quadrant and take 32 of the
 //              tile's 128 columns each): pass 1 row maximum and sum, pass 2
 //              threshold and P, epilogue
-//   warp 16    TMA producer: the Q block once, K tiles for both passes, V
-//              tiles for pass 2 (128-byte swizzled boxes of 64 elements)
+//   warp 16    TMA producer: the Q block once, K tiles for both passes
+//              (128-byte swizzled boxes of 64 elements)
 //   warp 17    TMEM allocation; lane 0 issues the QK^T tcgen05.mma
 //   warp 18    lane 0 issues the P.V tcgen05.mma (two issuing threads, so the
 //              barrier bookkeeping of one overlaps the MMAs of the other)
+//   warp 19    TMA producer of the V tiles of pass 2 (it waits on P.V to free
+//              a stage, so it runs apart from the K producer)
 // Scores S = Q K^T (128 rows x 128 keys, fp32) rotate through three TMEM
 // buffers so the tensor core computes the next tiles while the row threads
 // read one.  The output accumulator O (128 x d, fp32) stays in TMEM for the
@@ -52,10 +54,11 @@ constexpr int SBUF = 3;          // score buffers in TMEM
 constexpr int kRowWarps = 16;    // four warps per TMEM lane quadrant
 constexpr int kParts = kRowWarps / 4;  // parts of a score row (one per warp of a quadrant)
 constexpr int CP = BN / kParts;        // score columns of one part
-constexpr int kProducerWarp = kRowWarps;
+constexpr int kProducerWarp = kRowWarps;   // TMA: Q and K
 constexpr int kMmaWarp = kRowWarps + 1;    // issues QK^T; allocates TMEM
 constexpr int kPvWarp = kRowWarps + 2;     // issues P.V
-constexpr int kTcThreads = 32 * (kRowWarps + 3);
+constexpr int kVProducerWarp = kRowWarps + 3;  // TMA: V (waits on P.V, so apart from K)
+constexpr int kTcThreads = 32 * (kRowWarps + 4);
 constexpr uint32_t kTmemCols = 512;  // score buffers at columns 0, 128, 256; O at 384
 constexpr uint32_t kOCol = 384;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -178,10 +181,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+    // --------------------------------------------------- producer: Q and K
     if (lane == 0) {
-      int kcount[KST] = {}, vcount[VST] = {};
-      int ks = 0, kph = 0, vs = 0, vph = 0;
+      int kcount[KST] = {};
+      int ks = 0, kph = 0;
       mbar_expect_tx(bar(L::B_Q), L::NP * L::QP);
       for (int pn = 0; pn < L::NP; ++pn)
         tma_load_3d(sb + L::Q + pn * L::QP, &tmQ, bar(L::B_Q), 64 * pn, row0, bh_q);
@@ -194,21 +197,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       kt * BN, bh_kv);
         ++kcount[ks];
         if (++ks == KST) { ks = 0; kph ^= 1; }
-        if (tt >= nt) {
-          if (tt == nt) pdl_wait();  // the fp16 copy of V is written by the previous grid
-          if (!mbar_wait(bar(L::B_VE + vs), vph ^ 1, abort_flag)) break;
-          mbar_expect_tx(bar(L::B_VF + vs), L::NP * L::KP);
-          for (int pn = 0; pn < L::NP; ++pn)
-            tma_load_3d(sb + L::V + (vs * L::NP + pn) * L::KP, &tmV, bar(L::B_VF + vs), 64 * pn,
-                        kt * BN, bh_kv);
-          ++vcount[vs];
-          if (++vs == VST) { vs = 0; vph ^= 1; }
-        }
       }
       // every copy this thread issued lands before the CTA releases its memory
       bool drained = mbar_wait_drain(bar(L::B_Q), 0);
       for (int s = 0; s < KST; ++s)
         if (kcount[s]) drained &= mbar_wait_drain(bar(L::B_KF + s), (kcount[s] - 1) & 1);
+      if (!drained) set_status(p.status, TOPT_ETIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp == kVProducerWarp) {
+    // ----------------------------------------------------- producer: V
+    if (lane == 0) {
+      int vcount[VST] = {};
+      int vs = 0, vph = 0;
+      pdl_wait();  // the fp16 copy of V is written by the previous grid
+      for (int u = 0; u < nt; ++u) {
+        if (!mbar_wait(bar(L::B_VE + vs), vph ^ 1, abort_flag)) break;
+        mbar_expect_tx(bar(L::B_VF + vs), L::NP * L::KP);
+        for (int pn = 0; pn < L::NP; ++pn)
+          tma_load_3d(sb + L::V + (vs * L::NP + pn) * L::KP, &tmV, bar(L::B_VF + vs), 64 * pn,
+                      u * BN, bh_kv);
+        ++vcount[vs];
+        if (++vs == VST) { vs = 0; vph ^= 1; }
+      }
+      bool drained = true;
       for (int s = 0; s < VST; ++s)
         if (vcount[s]) drained &= mbar_wait_drain(bar(L::B_VF + s), (vcount[s] - 1) & 1);
       if (!drained) set_status(p.status, TOPT_ETIMEOUT);
@@ -334,15 +346,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c = 0; c < CP; ++c)
           if (c > lim) v[c] = __float_as_uint(-CUDART_INF_F);
       }
-      float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+      // maximum by three-input max (two new scores per instruction), four chains
+      float mx[4] = {__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                     __uint_as_float(v[3])};
 #pragma unroll
-      for (int c = 0; c < CP; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
-      const float mn = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
+      for (int c = 4; c < CP; c += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          mx[q] = fmax3(mx[q], __uint_as_float(v[c + 2 * q]), __uint_as_float(v[c + 2 * q + 1]));
+      }
+      const float mn = fmaxf(m2, fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c2);
       const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden part so far
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+      // 2^(a log2(e) - mref) by packed fma, summed by packed add (two chains)
+      float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 cc = make_float2(c2, c2), mm = make_float2(-mref, -mref);
 #pragma unroll
-      for (int c = 0; c < CP; ++c) sm[c & 3] += ex2(fmaf(__uint_as_float(v[c]), c2, -mref));
-      z = z * ex2(m2 - mref) + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+      for (int c = 0; c < CP; c += 2) {
+        const float2 y = ffma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), cc, mm);
+        sm[(c >> 1) & 1] = fadd2(sm[(c >> 1) & 1], make_float2(ex2(y.x), ex2(y.y)));
+      }
+      const float2 st2 = fadd2(sm[0], sm[1]);
+      z = z * ex2(m2 - mref) + (st2.x + st2.y);
       m2 = mn;
     }
     // merge the parts of the row in a fixed order, so every thread of the row
@@ -400,28 +424,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int tcnt = 0;
       bool wany = false;
 #pragma unroll
-      for (int j = 0; j < CP / 8; ++j) {
-        float cm = __uint_as_float(v[8 * j]);
+      const float2 cc = make_float2(c2, c2), mm = make_float2(-m2, -m2);
+      float2 Rp = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 1; e < 8; ++e) cm = fmaxf(cm, __uint_as_float(v[8 * j + e]));
+      for (int j = 0; j < CP / 8; ++j) {
+        const float* vj = reinterpret_cast<const float*>(v) + 8 * j;
+        const float cm = fmax3(fmax3(vj[0], vj[1], vj[2]), fmax3(vj[3], vj[4], vj[5]),
+                               fmaxf(vj[6], vj[7]));
 #pragma unroll
         for (int e = 0; e < 4; ++e) w[4 * j + e] = 0u;
         if (__any_sync(0xffffffffu, cm >= braw)) {
           wany = true;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float a0 = __uint_as_float(v[8 * j + 2 * e]);
-            const float a1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+            const float a0 = vj[2 * e], a1 = vj[2 * e + 1];
             const bool q0 = a0 >= braw, q1 = a1 >= braw;
-            const float e0 = ex2(q0 ? fmaf(a0, c2, -m2) : -CUDART_INF_F);
-            const float e1 = ex2(q1 ? fmaf(a1, c2, -m2) : -CUDART_INF_F);
-            R0 += e0;
-            R1 += e1;
+            const float2 y = ffma2(make_float2(a0, a1), cc, mm);
+            const float e0 = ex2(q0 ? y.x : -CUDART_INF_F);
+            const float e1 = ex2(q1 ? y.y : -CUDART_INF_F);
+            Rp = fadd2(Rp, make_float2(e0, e1));
             tcnt += (int)q0 + (int)q1;
             w[4 * j + e] = pack_half2(e0, e1);
           }
         }
       }
+      R0 += Rp.x;
+      R1 += Rp.y;
       tmem_st<CP / 2>(trow + (uint32_t)sbuf * BN, w);
       tc_fence_before();
       if (lane == 0) anyf[sbuf * kRowWarps + warp] = wany ? 1 : 0;
