@@ -110,7 +110,7 @@ struct TcParams {
   unsigned long long* tiles;
   int32_t* status;
   const uint32_t* v;     // [B][Hkv][S][D] bf16 V (pairs), read by the epilogue when vmc
-  const float* bsum;     // [B * Hkv][nqb][D] column sums of each 128-row block of V (vmc)
+  const float* bsum;     // [B * Hkv][nqb][D] column sums of V rows before each 128-row block (vmc)
   const int32_t* vexp;   // [B * Hkv] exponent e of the fp16 V copy (V16 = V 2^-e)
 };
 
@@ -534,14 +534,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // RPS rows (thread: 4 columns x RPS rows), in fp32 from the bf16 V.
       constexpr int QD = D / 4, NSEG = 32 * kRowWarps / QD, RPS = BM / NSEG;
       const int c4 = threadIdx.x % QD, seg = threadIdx.x / QD, c = 4 * c4;
-      float* pre = reinterpret_cast<float*>(gb + L::V);  // [D]: V rows 0 .. row0-1
+      float* pre = reinterpret_cast<float*>(gb + L::V);  // [D]: sum of V rows 0 .. row0-1
       float* segsum = pre + D;                           // [NSEG][D]: totals of the segments
-      if (threadIdx.x < D) {
-        const float* bs = p.bsum + (size_t)bh_kv * p.nqb * D + threadIdx.x;
-        float acc = 0.f;
-        for (int q = 0; q < qb; ++q) acc += bs[(size_t)q * D];
-        pre[threadIdx.x] = acc;
-      }
+      if (threadIdx.x < D) pre[threadIdx.x] = p.bsum[((size_t)bh_kv * p.nqb + qb) * D + threadIdx.x];
       float4 run[RPS];
       float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
       const uint32_t* vblk = p.v + ((size_t)bh_kv * p.S + row0) * (D / 2);
@@ -651,10 +646,21 @@ __device__ __forceinline__ int v16_exponent(uint32_t maxbits) {
 template <int D>
 __global__ void __launch_bounds__(256) v16_kernel(const uint4* __restrict__ v, int S,
                                                   const uint32_t* __restrict__ vmax,
-                                                  uint4* __restrict__ v16, int32_t* __restrict__ vexp) {
-  pdl_wait();  // vmax is complete
+                                                  uint4* __restrict__ v16, int32_t* __restrict__ vexp,
+                                                  float* __restrict__ bsum, int nqb) {
+  pdl_wait();  // vmax and the block sums are complete
   pdl_launch_dependents();
   const int bh = blockIdx.y;
+  if (bsum && blockIdx.x == 0 && threadIdx.x < D) {
+    // block column sums -> exclusive prefix sums over the blocks of this head
+    float* col = bsum + (size_t)bh * nqb * D + threadIdx.x;
+    float run = 0.f;
+    for (int q = 0; q < nqb; ++q) {
+      const float x = col[(size_t)q * D];
+      col[(size_t)q * D] = run;
+      run += x;
+    }
+  }
   const size_t n16 = (size_t)S * D / 8;
   const int e = v16_exponent(vmax[bh]);
   const float scale = __int_as_float((127 - e) << 23);
@@ -730,7 +736,8 @@ cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if ((e = cudaLaunchKernelEx(&cfg, v16_kernel<D>, static_cast<const uint4*>(a.v), a.seq,
-                              (const uint32_t*)vmax, static_cast<uint4*>(v16), vexp)) != cudaSuccess)
+                              (const uint32_t*)vmax, static_cast<uint4*>(v16), vexp,
+                              const_cast<float*>(p.bsum), p.nqb)) != cudaSuccess)
     return e;
 
   CUtensorMap tq, tk, tv;
