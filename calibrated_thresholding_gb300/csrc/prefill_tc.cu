@@ -98,6 +98,8 @@ struct TcLayout {
   static_assert(kRowWarps % 8 == 0, "8-byte words of any-kept flags per P buffer");
   static_assert(KST == SBUF, "a K stage is freed by the QK^T of the score buffer of the same index");
   static_assert(ALLOC <= 227 * 1024, "shared memory");
+  static_assert(ANY % 8 == 0 && XCH1 % 8 == 0 && XCH2 % 8 == 0, "8-byte words and float2");
+  static_assert(V % 1024 == 0 && K % 1024 == 0 && Q % 1024 == 0, "128-byte-swizzle tiles");
 };
 
 struct TcParams {
