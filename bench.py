@@ -58,11 +58,11 @@ NOMINAL_HBM_GBS = 8000.0
 # null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
-                  "source_sha256": "f198d8dfb6df450c3aa3fd9db40c389b2d4338ea5507a8ae9251ce0587e71c51",
-                  "bytes_per_launch": 268611840 + 13363712}   # decode_scores_kernel, one layer call
+                  "source_sha256": "051db2bfe19b00d197c145490ff19df175c1384b2b9ae09735ebb81113afed27",
+                  "bytes_per_launch": 268612608 + 13519872}   # decode_scores_kernel, one layer call
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "5371ae7bb87b2d3dfd97eb476a43a0796f42052739f796de41cf461bcc4fe126",
-                   "bytes_per_launch": 59532544 + 22978304}   # prefill_tc_kernel, post-softmax + VMC
+                   "source_sha256": "d5a5ddde07a291483fdc28cd283121b792e4dabf1ac7fbc96dbfc0a69c6d04e1",
+                   "bytes_per_launch": 59529472 + 23480832}   # prefill_tc_kernel, post-softmax + VMC
 
 
 def parse():

@@ -659,9 +659,13 @@ __global__ void __launch_bounds__(kThreads, 6) decode_select_kernel(const Decode
     const int dd = idx - h * D;
     float num = 0.f, R = 0.f;
     int ktot = 0;
+    // independent L2 loads of several slices in flight
+#pragma unroll 4
     for (int c = 0; c < p.ipp; ++c) {
       const size_t q = (size_t)pair * p.ipp + c;
-      if (__ldcg(p.part_nu + q) > 0) num += __ldcg(p.part_num + q * G * D + idx);
+      const int nu = __ldcg(p.part_nu + q);
+      const float nv = __ldcg(p.part_num + q * G * D + idx);  // stale when nu == 0
+      num += nu > 0 ? nv : 0.f;
       R += __ldcg(p.part_r + q * G + h);
       ktot += __ldcg(p.part_kt + q * G + h);
     }
