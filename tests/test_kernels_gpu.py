@@ -225,6 +225,7 @@ PREFILL_MODES = [
     (128, torch.bfloat16, 2, 4, 2, 100),
     (64, torch.bfloat16, 2, 4, 2, 100),
     (128, torch.bfloat16, 1, 4, 1, 300),    # three 128-row blocks, ragged last block and key tile
+    (64, torch.bfloat16, 1, 2, 2, 257),     # one KV head per query head, ragged
 ])
 def test_prefill_matches_oracle(d, dtype, B, Hq, Hkv, S):
     k = 8
