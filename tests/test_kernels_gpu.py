@@ -246,3 +246,37 @@ def test_prefill_matches_oracle(d, dtype, B, Hq, Hkv, S):
                 hit += hh
                 total += tt
         assert tiles.tolist() == [hit, total]
+
+
+@pytest.mark.parametrize("d,dtype,S", [(128, torch.bfloat16, 129), (64, torch.bfloat16, 1),
+                                       (64, torch.float32, 129)])
+def test_prefill_dense_and_empty(d, dtype, S):
+    """theta = -inf keeps every causal key (dense attention, every tile executed);
+    a threshold nothing reaches skips every P.V tile: post-softmax and pre-softmax
+    with SDC give the prefix mean of V under VMC, the rest give 0."""
+    B, Hq, Hkv = 1, 4, 2
+    Q, K, V = prefill_case(81, B, Hq, Hkv, d, S, dtype)
+    dense = torch.full((Hq, S), float("-inf"), device="cuda")
+    for mode, sdc, vmc in PREFILL_MODES:
+        mask = torch.full((B, Hq, S, mask_words(S)), -1, device="cuda", dtype=torch.int32)
+        tiles = torch.zeros(2, device="cuda", dtype=torch.int64)
+        res = topt.prefill(Q, K, V, dense, mode=mode, sdc=sdc, vmc=vmc, mask=mask, tiles=tiles)
+        torch.cuda.synchronize()
+        want_kept = torch.arange(1, S + 1, dtype=torch.int32).expand(B, Hq, S)
+        assert torch.equal(res["kept"].cpu(), want_kept)
+        assert tiles[0].item() == tiles[1].item() > 0
+        check_prefill(Q, K, V, dense, mode, sdc, vmc, res)
+    Vf = V.double()
+    mu = Vf.cumsum(dim=2) / torch.arange(1, S + 1, device="cuda", dtype=torch.float64)[:, None]
+    mu_q = mu.repeat_interleave(Hq // Hkv, dim=1).float()
+    for mode, th in ((ref.POST, 1.5), (ref.PRE, 1e4)):
+        full = torch.full((Hq, S), th, device="cuda")
+        for sdc, vmc in ((ref.SDC_NONE, True), (ref.SDC_EXACT, True), (ref.SDC_NONE, False)):
+            tiles = torch.zeros(2, device="cuda", dtype=torch.int64)
+            res = topt.prefill(Q, K, V, full, mode=mode, sdc=sdc, vmc=vmc, tiles=tiles)
+            torch.cuda.synchronize()
+            assert int(res["kept"].sum()) == 0
+            assert tiles[0].item() == 0 and tiles[1].item() > 0
+            eligible = mode == ref.POST or sdc != ref.SDC_NONE
+            want = mu_q if (vmc and eligible) else torch.zeros_like(res["out"])
+            torch.testing.assert_close(res["out"], want, rtol=2e-5, atol=2e-5)
