@@ -144,6 +144,20 @@ topt_status topt_prefill(const topt_prefill_args* a, topt_stream stream) {
   return cuda_status(prefill_launch(*a, (cudaStream_t)stream));
 }
 
+topt_status topt_prefill_test_timeout(const topt_prefill_args* a, topt_stream stream) {
+  topt_status st = check_prefill_shape(a);
+  if (st != TOPT_OK) return st;
+  if (a->dtype != TOPT_BF16 || !a->status) return TOPT_EINVAL;
+  if (!a->q || !a->k || !a->v || !a->theta || !a->out) return TOPT_EINVAL;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
+    return TOPT_EINVAL;
+  const size_t need = prefill_workspace_bytes(*a);
+  if (need > 0 && (!a->workspace || a->workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(a->workspace) & 255u)))
+    return TOPT_EWORKSPACE;
+  return cuda_status(prefill_launch(*a, (cudaStream_t)stream, 1));
+}
+
 // --------------------------------------------------------------- calibrate
 topt_status topt_calibrate_workspace(const topt_calib_args* a, size_t* bytes) {
   topt_status st = check_calib_shape(a);

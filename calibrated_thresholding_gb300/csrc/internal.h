@@ -20,7 +20,8 @@ cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s);
 // ----------------------------------------------------------------- prefill
 size_t prefill_workspace_bytes(const topt_prefill_args& a);
 void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys);
-cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s);
+// withhold_k: test hook of topt_prefill_test_timeout (tensor-core path only)
+cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s, int withhold_k = 0);
 // tensor-core path (bf16): 128-row x 128-key tiles; v16 is the fp16 copy of V
 // (prefill_tc_v16_bytes), vmax/vexp one word per (batch, kv head), bsum the
 // column sums of 128-row blocks of V (prefill_tc_bsum_bytes; VMC only).
@@ -29,7 +30,7 @@ size_t prefill_tc_bsum_bytes(const topt_prefill_args& a);
 int prefill_tc_rows();
 int prefill_tc_keys();
 cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
-                           float* bsum, cudaStream_t s);
+                           float* bsum, cudaStream_t s, int withhold_k);
 
 // --------------------------------------------------------------- calibrate
 size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);

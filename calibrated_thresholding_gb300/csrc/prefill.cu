@@ -263,7 +263,7 @@ void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys
   *keys = tc ? prefill_tc_keys() : kKeys;
 }
 
-cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s) {
+cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s, int withhold_k) {
   const PrefillLayout l = prefill_layout(a);
   char* ws = static_cast<char*>(a.workspace);
   PrefillParams p;
@@ -292,7 +292,7 @@ cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s) {
   if (a.dtype == TOPT_BF16)
     return prefill_tc_run(a, ws + l.v16, reinterpret_cast<uint32_t*>(ws + l.vmax),
                           reinterpret_cast<int32_t*>(ws + l.vexp),
-                          reinterpret_cast<float*>(ws + l.bsum), s);
+                          reinterpret_cast<float*>(ws + l.bsum), s, withhold_k);
   return a.head_dim == 128 ? launch_td<float, 128>(p, a.events, s) : launch_td<float, 64>(p, a.events, s);
 }
 

@@ -114,6 +114,7 @@ struct TcParams {
   const uint32_t* v;     // [B][Hkv][S][D] bf16 V (pairs), read by the epilogue when vmc
   const float* bsum;     // [B * Hkv][nqb][D] column sums of V rows before each 128-row block (vmc)
   const int32_t* vexp;   // [B * Hkv] exponent e of the fp16 V copy (V16 = V 2^-e)
+  int withhold_k;        // test hook: never load the first K tile of a block
 };
 
 // Programmatic dependent launch: this grid lets the next one start / waits
@@ -192,6 +193,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_3d(sb + L::Q + pn * L::QP, &tmQ, bar(L::B_Q), 64 * pn, row0, bh_q);
       for (int tt = 0; tt < 2 * nt; ++tt) {
         const int kt = tt < nt ? tt : tt - nt;
+        if (p.withhold_k && tt == 0) {  // the QK^T thread's first wait must run out
+          if (++ks == KST) { ks = 0; kph ^= 1; }
+          continue;
+        }
         if (!mbar_wait(bar(L::B_SF + ks), kph ^ 1, abort_flag)) break;
         mbar_expect_tx(bar(L::B_KF + ks), L::NP * L::KP);
         for (int pn = 0; pn < L::NP; ++pn)
@@ -776,7 +781,7 @@ int prefill_tc_rows() { return BM; }
 int prefill_tc_keys() { return BN; }
 
 cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
-                           float* bsum, cudaStream_t s) {
+                           float* bsum, cudaStream_t s, int withhold_k) {
   TcParams p;
   p.B = a.batch;
   p.Hq = a.n_q_heads;
@@ -799,6 +804,7 @@ cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax
   p.v = static_cast<const uint32_t*>(a.v);
   p.bsum = a.vmc ? bsum : nullptr;
   p.vexp = vexp;
+  p.withhold_k = withhold_k;
   return a.head_dim == 128 ? run_d<128>(a, p, v16, vmax, vexp, s) : run_d<64>(a, p, v16, vmax, vexp, s);
 }
 

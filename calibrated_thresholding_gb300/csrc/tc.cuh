@@ -15,7 +15,7 @@
 namespace topt {
 namespace tc {
 
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

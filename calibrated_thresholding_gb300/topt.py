@@ -68,7 +68,7 @@ _lib = None
 _lock = threading.Lock()
 
 SYMBOLS = ["topt_decode_workspace", "topt_decode", "topt_decode_noalloc", "topt_prefill_workspace",
-           "topt_prefill_tile_shape", "topt_prefill", "topt_calibrate_workspace",
+           "topt_prefill_tile_shape", "topt_prefill", "topt_prefill_test_timeout", "topt_calibrate_workspace",
            "topt_calibrate", "topt_select_kth", "topt_vmean_update", "topt_version",
            "topt_status_string"]
 
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
             L.topt_prefill_workspace.argtypes = [P(PrefillArgs), P(sz)]
             L.topt_prefill_tile_shape.argtypes = [P(PrefillArgs), P(i32), P(i32)]
             L.topt_prefill.argtypes = [P(PrefillArgs), vp]
+            L.topt_prefill_test_timeout.argtypes = [P(PrefillArgs), vp]
             L.topt_calibrate_workspace.argtypes = [P(CalibArgs), P(sz)]
             L.topt_calibrate.argtypes = [P(CalibArgs), vp]
             L.topt_select_kth.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp]

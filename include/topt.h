@@ -168,6 +168,14 @@ topt_status topt_prefill_tile_shape(const topt_prefill_args* args, int32_t* tile
                                     int32_t* tile_keys);
 topt_status topt_prefill(const topt_prefill_args* args, topt_stream stream);
 
+/* Test hook of the bounded waits: topt_prefill (bf16 only, status required)
+ * with the first K tile of every 128-row block never loaded, so a wait of the
+ * tensor-core kernel runs out (1 s per block).  The kernel then stops every
+ * role, drains its own copies and MMAs, frees its tensor memory and sets
+ * *status = TOPT_ETIMEOUT; out is undefined.  Nothing faults and the CUDA
+ * context stays usable.  Not part of the method. */
+topt_status topt_prefill_test_timeout(const topt_prefill_args* args, topt_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Calibration [TopTheta §3.1, Algorithm 1], one layer per call.            */
 /* ------------------------------------------------------------------------ */
