@@ -73,6 +73,8 @@ def parse():
     p.add_argument("--impl", choices=["topt", "reference"], default="topt")
     p.add_argument("--workload", choices=["cfg2", "cfg3", "cfg4", "cfg5"], default="cfg2")
     p.add_argument("--no-prefill", action="store_true", help="leave out the prefill object")
+    p.add_argument("--dense", action="store_true",
+                   help="also time the decode step with theta = -inf (on for cfg5)")
     p.add_argument("--prefill-steps", type=int, default=30)
     p.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -271,6 +273,34 @@ class DecodeState:
             a.events[0] = None
             a.events[1] = None
             a.events[2] = None
+
+
+def time_dense(state, L, stream, steps, warmup):
+    """The decode step with every threshold at -inf (dense attention: every V row
+    read), timed eagerly with CUDA events; the thresholds are put back after."""
+    dense = torch.full_like(state.theta[0], float("-inf"))
+    saved = [a.theta for a in state.dargs]
+    for a in state.dargs:
+        a.theta = ctypes.c_void_p(dense.data_ptr())
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    try:
+        for _ in range(warmup):
+            state.run_step(L, sh)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(state.dev)
+        start.record(stream)
+        for _ in range(steps):
+            state.run_step(L, sh)
+        stop.record(stream)
+        torch.cuda.synchronize(state.dev)
+        ms = start.elapsed_time(stop) / steps
+        vrows = float(np.mean([state.vrows[l].double().mean().item() for l in range(state.layers)]))
+    finally:
+        for a, t in zip(state.dargs, saved):
+            a.theta = t
+    wl = state.wl
+    return {"ms_per_step": ms, "tokens_per_s": wl.B / (ms / 1e3), "vrows_per_group": vrows,
+            "theta": "-inf (every valid key kept)", "launch": "eager host launches"}
 
 
 def algorithmic_bytes(state):
@@ -778,6 +808,9 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if args.dense or args.workload == "cfg5":
+        # after every thresholded figure above: it overwrites kept and vrows
+        line["dense"] = time_dense(state, L, stream, max(10, args.steps // 4), args.warmup)
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if not args.no_prefill:
