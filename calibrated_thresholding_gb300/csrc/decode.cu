@@ -57,6 +57,14 @@ __host__ __device__ constexpr int gather_unroll() { return G <= 2 ? 8 : 4; }
 template <int G>
 __host__ __device__ constexpr int slice_keys() { return kThreads * (40 / G < 24 ? 40 / G : 24); }
 
+// Resident select CTAs per SM the register budget is sized for: 6 (80
+// registers) keeps the short per-CTA latency chains overlapped; from G = 6 on
+// the eight-head state spills at 80 registers, and 4 CTAs with 128 registers
+// measured faster (G = 8: 229 against 258 us per decode call of the
+// 70B-shaped workload; G = 4: 87.4 against 84.4 us, so it stays at 6).
+template <int G>
+__host__ __device__ constexpr int select_min_blocks() { return G >= 6 ? 4 : 6; }
+
 // Score columns per key in the workspace: G rounded up to even (8-byte stores).
 __host__ __device__ constexpr int score_cols(int G) { return G == 1 ? 1 : (G + 1) / 2 * 2; }
 
@@ -419,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
 // Select: one slice of one pair per CTA.
 // ----------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 6) decode_select_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, select_min_blocks<G>()) decode_select_kernel(const DecodeParams p) {
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
   constexpr int GC = score_cols(G);
