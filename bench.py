@@ -58,11 +58,11 @@ NOMINAL_HBM_GBS = 8000.0
 # null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
-                  "source_sha256": "051db2bfe19b00d197c145490ff19df175c1384b2b9ae09735ebb81113afed27",
-                  "bytes_per_launch": 268612608 + 13519872}   # decode_scores_kernel, one layer call
+                  "source_sha256": "493ab46e4573be8a0fc8cc15c4a76447fb21a36d812d94aeb9e4dec0f110bf55",
+                  "bytes_per_launch": 268611072 + 13505792}   # decode_scores_kernel, one layer call
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "d5a5ddde07a291483fdc28cd283121b792e4dabf1ac7fbc96dbfc0a69c6d04e1",
-                   "bytes_per_launch": 59529472 + 23480832}   # prefill_tc_kernel, post-softmax + VMC
+                   "source_sha256": "cb97c76275b0130056a5a5fc96f981626a4f10449d80b0e75ae92031b64498c0",
+                   "bytes_per_launch": 59533568 + 23594496}   # prefill_tc_kernel, post-softmax + VMC
 
 
 def parse():
