@@ -303,6 +303,30 @@ def time_dense(state, L, stream, steps, warmup):
             "theta": "-inf (every valid key kept)", "launch": "eager host launches"}
 
 
+def drift_sweep(state):
+    """k~/k per row-length bucket with the first layer's caches at ~16 lengths
+    spread over the buckets (theta calibrated on shorter rows is extended by the
+    last calibrated row), through topt.decode with fresh queries per length."""
+    wl = state.wl
+    K, V, theta = state.K[0], state.V[0], state.theta[0]
+    per_bucket = {}
+    lengths = list(workloads.DRIFT_LENGTHS)
+    for c in range(0, len(lengths), wl.B):
+        seq = (lengths[c:c + wl.B] + [lengths[-1]] * wl.B)[:wl.B]
+        gen = synth.generator(synth.seed_of(wl.name, "drift", c), state.dev)
+        q = synth.decode_queries(gen, K, wl.Hq, seq)
+        seq_len = torch.tensor(seq, device=state.dev, dtype=torch.int32)
+        mu = torch.stack([V[b, :, :L].float().mean(dim=1) for b, L in enumerate(seq)])
+        res = topt.decode(q, K, V, seq_len, theta, mode=wl.mode, sdc=wl.sdc, vmc=wl.vmc, mu=mu,
+                          workspace=state.ws)
+        kept = res["kept"].double().mean(dim=1).cpu().numpy()
+        for b, L in enumerate(seq[:len(lengths[c:c + wl.B])]):
+            for (lo, hi) in workloads.BUCKETS:
+                if lo <= L <= hi:
+                    per_bucket.setdefault(f"{lo}-{hi}", []).append(kept[b] / wl.k_of(0))
+    return {k: round(float(np.mean(v)), 4) for k, v in per_bucket.items()}
+
+
 def algorithmic_bytes(state):
     """Per decode call: whole K cache + union V rows + theta entries (+ q, mu, out)."""
     wl = state.wl
@@ -425,8 +449,10 @@ def prefill_report(L, wl, dev, stream, steps, warmup):
         call = float(np.mean(call_s))
         achieved = useful / kern / 1e12
         kept = st.kept.double()
+        kept_total = float(st.kept.double().sum().item())
         out["modes"].append({
             "mode": name, "tflops_call": useful / call / 1e12, "ms_per_call": call * 1e3,
+            "kept_elem_tflops_call": kept_elem_flops(wl, kept_total) / call / 1e12,
             "tokens_per_s": wl.B * wl.S / call,
             "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -519,6 +545,12 @@ def causal_flops(wl):
     return 4.0 * wl.d * wl.B * wl.Hq * (wl.S * (wl.S + 1) / 2)
 
 
+def kept_elem_flops(wl, kept_total):
+    """The metric's "kept-element" flops of one prefill call: QK^T on every causal
+    element plus P.V on every kept element, 2 d flops each."""
+    return 2.0 * wl.d * (wl.B * wl.Hq * (wl.S * (wl.S + 1) / 2) + kept_total)
+
+
 def host_prefill_sample(wl, n_cal=2, heads=4):
     """One KV group of the prefill workload on the host, theta from the oracle's
     calibration over n_cal sequences (all rows)."""
@@ -539,13 +571,16 @@ def host_prefill_sample(wl, n_cal=2, heads=4):
 
 
 def oracle_prefill_row_seconds(sample, mode, sdc, rows, cores):
-    """Wall-clock seconds per prefill row of the oracle on `cores` threads."""
+    """Wall-clock seconds per prefill row of the oracle on `cores` threads, and the
+    mean kept count of those rows."""
     import oracle.topt_ref as ref
     Q, K, V, th = sample
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(max_workers=cores) as ex:
-        list(ex.map(lambda r: ref.prefill_ref(Q, K, V, th, mode, sdc, True, rows=[r]), rows))
-    return (time.perf_counter() - t0) / len(rows)
+        res = list(ex.map(lambda r: ref.prefill_ref(Q, K, V, th, mode, sdc, True, rows=[r]), rows))
+    dt = (time.perf_counter() - t0) / len(rows)
+    kept = float(np.mean([next(iter(d.values()))["kept"] for d in res]))
+    return dt, kept
 
 
 def prefill_rows_sample(wl, n, heads=4, seed=0):
@@ -556,14 +591,17 @@ def prefill_rows_sample(wl, n, heads=4, seed=0):
 def prefill_cpu_baseline(wl, seconds):
     cores = host_cores()
     sample = host_prefill_sample(wl)
-    done, spent = 0, 0.0
+    done, spent, kept_sum = 0, 0.0, 0.0
     while spent < seconds:
         rows = prefill_rows_sample(wl, 8 * cores, seed=done)
-        spent += oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores) * len(rows)
+        dt, kept = oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores)
+        spent += dt * len(rows)
+        kept_sum += kept * len(rows)
         done += len(rows)
     t_row = spent / done
     rows_per_call = wl.B * wl.Hq * wl.S
-    return {"value": causal_flops(wl) / (t_row * rows_per_call) / 1e12, "unit": "TFLOP/s",
+    kept_total = kept_sum / done * rows_per_call
+    return {"value": kept_elem_flops(wl, kept_total) / (t_row * rows_per_call) / 1e12, "unit": "TFLOP/s",
             "cores": cores, "kind": "oracle",
             "sample": f"{done} prefill rows (uniform row index, post-softmax+VMC, k={wl.k}), "
                       f"float64 numpy, {cores} threads; scaled to {rows_per_call} rows per call"}
@@ -580,16 +618,19 @@ def run_reference_prefill(args, wl):
 
     for i in range(args.warmup):
         one_step(i)
-    t_row = sum(one_step(args.warmup + i) for i in range(args.steps)) / args.steps
+    runs = [one_step(args.warmup + i) for i in range(args.steps)]
+    t_row = sum(r[0] for r in runs) / args.steps
     rows_per_call = wl.B * wl.Hq * wl.S
+    kept_total = float(np.mean([r[1] for r in runs])) * rows_per_call
     ms = t_row * rows_per_call * 1e3
-    value = causal_flops(wl) / (ms / 1e3) / 1e12
+    value = kept_elem_flops(wl, kept_total) / (ms / 1e3) / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                       "S": wl.S, "k": wl.k, "mode": "post-softmax+VMC"},
+                       "S": wl.S, "k": wl.k, "mode": "post-softmax+VMC",
+                       "flops": "kept-element: 2 d per causal element (QK^T) + 2 d per kept element (P.V)"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} prefill rows per step of {rows_per_call}, "
                                        "float64 numpy oracle"},
@@ -808,6 +849,8 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if args.workload == "cfg4":
+        line["kept_over_k_by_bucket"] = drift_sweep(state)
     if args.dense or args.workload == "cfg5":
         # after every thresholded figure above: it overwrites kept and vrows
         line["dense"] = time_dense(state, L, stream, max(10, args.steps // 4), args.warmup)
@@ -850,7 +893,8 @@ def main_prefill(args, dev, rank, local, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     call = ms / 1e3 / args.steps
-    value = causal_flops(wl) * world / call / 1e12
+    kept_total = float(st.kept.double().sum().item())
+    value = kept_elem_flops(wl, kept_total) * world / call / 1e12
     useful, issued = prefill_flops(st, tiles)
     kern = float(np.mean(kern_s))
     peak, kind = tensor_peak()
@@ -862,7 +906,7 @@ def main_prefill(args, dev, rank, local, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                    "S": wl.S, "k": wl.k, "mode": name,
-                   "flops": "dense-equivalent over the causal triangle: QK^T + P.V, 2 d per element",
+                   "flops": "kept-element: 2 d per causal element (QK^T) + 2 d per kept element (P.V)",
                    "l2": f"{L2_FLUSH_BYTES >> 20} MiB written between timed calls",
                    "parallelism": f"replicas x{world} (independent prefills per GPU)"},
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
@@ -873,6 +917,7 @@ def main_prefill(args, dev, rank, local, world):
                      "flops_per_launch": useful,
                      "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
                      "issued_tflops": issued / kern / 1e12},
+        "dense_equiv_tflops_call": causal_flops(wl) * world / call / 1e12,
         "tiles_executed": tiles[0], "tiles_causal": tiles[1],
         "tiles_skipped_frac": 1.0 - tiles[0] / max(1, tiles[1]),
         "kept_over_k": round(st.kept.double()[..., wl.k:].mean().item() / wl.k, 4),
@@ -919,7 +964,8 @@ def prefill_e2e(st, args, dev, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         dt_s = float(t.item())
     h2d = sum(h_.numel() * h_.element_size() for h_ in host)
-    return {"value": causal_flops(wl) * steps * world / dt_s / 1e12, "unit": "TFLOP/s",
+    kept_total = float(st.kept.double().sum().item())
+    return {"value": kept_elem_flops(wl, kept_total) * steps * world / dt_s / 1e12, "unit": "TFLOP/s",
             "steps": steps, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": out_host.numel() * 4}
 
