@@ -35,9 +35,13 @@ reason in the design notes of the repository):
 * c12 an empty selection gives num = 0 and R = 0 (pre without SDC: out = 0).
 * c13 std uses ddof = 1; a single sample has std 0.
 * c16 post-softmax with SDC is post-softmax (SDC maps pre onto post).
+* c17 MKC: theta_r(k) = sup{theta : k_bar_r(theta) >= k} (App. D leaves the
+      inverse of a fractional, not always monotone k_bar open); Eq. 8 averages
+      only over the intervals that contain theta, as printed.
 """
 from __future__ import annotations
 
+import bisect
 import math
 
 import numpy as np
@@ -129,23 +133,140 @@ def finalize_thresholds(sets, Hq, Lmax, k, alpha):
             obs = np.asarray(sets[(h, L)], dtype=np.float64)
             std = float(np.std(obs, ddof=1)) if obs.size > 1 else 0.0
             value[L] = float(np.mean(obs)) + alpha * std
-        if not seen:
-            continue
-        for L in range(1, Lmax + 1):
-            if L <= k:
-                continue
-            if L in value:
-                theta[h, L - 1] = value[L]
-                continue
-            best = min(seen, key=lambda c: (abs(c - L), c))
-            theta[h, L - 1] = value[best]
+        theta[h] = fill_row_ids(value, Lmax, k)
     return theta
+
+
+def fill_row_ids(value, Lmax, k):
+    """One head's row of the table from the calibrated row ids ``value`` (L -> theta).
+
+    Rows with L <= k are dense (-inf, reading c4); a row id that was not
+    calibrated takes the value of the nearest calibrated one, ties to the
+    shorter row ([Verdict], reading c5); no calibrated row at all: dense.
+    """
+    row = np.full(Lmax, -np.inf)
+    seen = sorted(value)
+    if not seen:
+        return row
+    for L in range(k + 1, Lmax + 1):
+        if L in value:
+            row[L - 1] = value[L]
+        else:
+            best = min(seen, key=lambda c: (abs(c - L), c))
+            row[L - 1] = value[best]
+    return row
 
 
 def calibrate_ref(Qc, Kc, row_len, k, mode, alpha, Lmax):
     """Algorithm 1 for one layer: returns (theta [Hq][Lmax], sets)."""
     sets = collect_thresholds(Qc, Kc, row_len, k, mode)
     return finalize_thresholds(sets, Qc.shape[1], Lmax, k, alpha), sets
+
+
+# ---------------------------------------------------------------------------
+# Appendix D, Algorithm 2: multi-k cumulative calibration (MKC).
+# ---------------------------------------------------------------------------
+def mkc_interval_sequence(x):
+    """The interval sequence of one calibration row ([TopTheta App. D, Algorithm 2]).
+
+    The row is sorted ascending into v_0..v_{r-1}; interval j is [v_j, v_{j+1})
+    with effective k r-1-j, the number of elements of the row above any
+    threshold inside it.  Returned as (t0, lo, hi) triples, j = 0..r-2.
+    """
+    v = np.sort(np.asarray(x, dtype=np.float64))
+    r = v.shape[0]
+    return [(r - 1 - j, float(v[j]), float(v[j + 1])) for j in range(r - 1)]
+
+
+def mkc_collect(Qc, Kc, row_len, mode, sets=None):
+    """The sets Theta_r of Algorithm 2 for one layer, keyed by (head, r).
+
+    Every calibration row of every sequence contributes the interval sequence
+    of its scores (PRE) or of its softmax values (POST; Figure 15 of the same
+    appendix calibrates both).  Unlike Algorithm 1 no row is skipped: the
+    target k is not known yet.  Same indexing as ``collect_thresholds``.
+    """
+    Qc = np.asarray(Qc, dtype=np.float64)
+    Kc = np.asarray(Kc, dtype=np.float64)
+    N, Hq, R, _ = Qc.shape
+    g = Hq // Kc.shape[1]
+    if sets is None:
+        sets = {}
+    for n in range(N):
+        for h in range(Hq):
+            for i in range(R):
+                L = int(row_len[i])
+                a = row_scores(Qc[n, h, i], Kc[n, h // g], L)
+                x = a if mode == PRE else row_softmax(a)
+                sets.setdefault((h, L), []).append(mkc_interval_sequence(x))
+    return sets
+
+
+def merge_intervals(seqs):
+    """MergeIntervals of Algorithm 2: the step function k_bar(theta) of Eq. 8.
+
+    On every elementary piece [lo, hi) between consecutive endpoints of all
+    intervals, k_bar is the mean effective k of the intervals that contain the
+    piece (at most one per sequence).  Pieces no interval contains are left
+    out: k_bar is undefined there.  Returns (lo, hi, sum_t0, n_intervals)
+    with the mean kept as an exact ratio of integers.
+    """
+    ends = sorted({e for seq in seqs for (_, lo, hi) in seq for e in (lo, hi)})
+    starts = [[a for (_, a, _) in seq] for seq in seqs]
+    pieces = []
+    for lo, hi in zip(ends[:-1], ends[1:]):
+        tot = cnt = 0
+        for seq, st in zip(seqs, starts):
+            # the last interval starting at or below lo is the only candidate
+            j = bisect.bisect_right(st, lo) - 1
+            if j >= 0 and lo < seq[j][2]:
+                tot += seq[j][0]
+                cnt += 1
+        if cnt:
+            pieces.append((lo, hi, tot, cnt))
+    return pieces
+
+
+def mkc_theta(pieces, k):
+    """theta_r(k), the inverse of k_bar_r at k (reading c17).
+
+    The largest threshold up to which the calibration rows keep at least k
+    elements on average: sup{theta : k_bar(theta) >= k}, the upper end of the
+    highest piece whose mean effective k is at least k.  A threshold equal to
+    that end keeps the same elements of the calibration rows as the inside of
+    the piece, because an element equal to theta is kept (reading c1).  -inf
+    when no piece reaches k (every row of length r <= k).
+    """
+    best = -np.inf
+    for lo, hi, tot, cnt in pieces:
+        if tot >= k * cnt:
+            best = max(best, hi)
+    return best
+
+
+def mkc_ref(Qc, Kc, row_len, mode, ks, Hq_Lmax=None):
+    """Algorithm 2 for one layer: theta [len(ks)][Hq][Lmax] and the sets.
+
+    ``Hq_Lmax`` defaults to (Hq, max row length).  Each table is filled like
+    Algorithm 1's (``fill_row_ids``): dense rows with L <= k, nearest
+    calibrated row id elsewhere.
+    """
+    Qc = np.asarray(Qc, dtype=np.float64)
+    Hq = Qc.shape[1]
+    Lmax = int(max(row_len)) if Hq_Lmax is None else Hq_Lmax[1]
+    sets = mkc_collect(Qc, Kc, row_len, mode)
+    return mkc_finalize(sets, Hq, Lmax, ks), sets
+
+
+def mkc_finalize(sets, Hq, Lmax, ks):
+    """The per-k threshold tables from the merged sets (Algorithm 2, last step)."""
+    merged = {key: merge_intervals(seqs) for key, seqs in sets.items() if key[1] <= Lmax}
+    theta = np.full((len(ks), Hq, Lmax), -np.inf)
+    for ki, k in enumerate(ks):
+        for h in range(Hq):
+            value = {L: mkc_theta(pc, k) for (hh, L), pc in merged.items() if hh == h and L > k}
+            theta[ki, h] = fill_row_ids(value, Lmax, k)
+    return theta
 
 
 def theta_for_row(theta_row, L):

@@ -308,6 +308,122 @@ def test_output_error_metric():
 
 
 # ---------------------------------------------------------------------------
+# Multi-k cumulative calibration (App. D, Algorithm 2, Eq. 8).
+# ---------------------------------------------------------------------------
+def _mkc_inputs(rows, d=4):
+    """Calibration tensors whose scores are exactly ``rows`` (a_j = K[j][0])."""
+    N, L = len(rows), len(rows[0])
+    Qc = np.zeros((N, 1, 1, d))
+    Qc[:, 0, 0, 0] = 2.0
+    Kc = np.zeros((N, 1, L, d))
+    for n in range(N):
+        Kc[n, 0, :, 0] = rows[n]
+    return Qc, Kc
+
+
+def check_golden_mkc(golden_dir):
+    g = _load(golden_dir, "mkc_two_rows.json")
+    L, Lmax, ks = g["L"], g["Lmax"], g["ks"]
+    Qc, Kc = _mkc_inputs(g["sample_scores"], g["d"])
+    sets = ref.mkc_collect(Qc, Kc, [L], ref.PRE)
+    pieces = ref.merge_intervals(sets[(0, L)])
+    assert [list(p) for p in pieces] == g["pieces_pre"]
+    for mode, key in ((ref.PRE, "theta_pre"), (ref.POST, "theta_post")):
+        theta, _ = ref.mkc_ref(Qc, Kc, [L], mode, ks, (1, Lmax))
+        for ki, k in enumerate(ks):
+            t = float(g[key][ki])
+            want = [-np.inf if (LL <= k or not np.isfinite(t)) else t for LL in range(1, Lmax + 1)]
+            np.testing.assert_allclose(theta[ki, 0], want, rtol=1e-14, atol=0, err_msg=f"{key} k={k}")
+
+
+def test_golden_mkc_two_rows(golden_dir):
+    check_golden_mkc(golden_dir)
+
+
+def check_mkc_single_row(seed=5, trials=200):
+    """One calibration row: theta(k) is its k-th largest element, which is also
+    what Algorithm 1 gives with alpha = 0 (one sample, no spread)."""
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        L = int(rng.integers(2, 14))
+        if t % 2:
+            row = rng.integers(0, 4, L).astype(np.float64)        # ties
+        else:
+            row = rng.normal(size=L)
+        srt = sorted(row, reverse=True)
+        pieces = ref.merge_intervals([ref.mkc_interval_sequence(row)])
+        for k in range(1, L + 1):
+            # no interval starts below the row minimum, so a k-th largest that
+            # equals the minimum (ties at the bottom, or k = L) gives no theta
+            want = srt[k - 1] if srt[k - 1] > srt[-1] else -np.inf
+            assert ref.mkc_theta(pieces, k) == want, (row, k)
+        Qc, Kc = _mkc_inputs([row])
+        ks = list(range(1, L))
+        th, _ = ref.mkc_ref(Qc, Kc, [L], ref.POST, ks, (1, L + 2))
+        for ki, k in enumerate(ks):
+            if srt[k - 1] == srt[-1]:
+                continue
+            a1, _ = ref.calibrate_ref(Qc, Kc, [L], k, ref.POST, 0.0, L + 2)
+            np.testing.assert_allclose(th[ki], a1, rtol=1e-15, atol=0)
+
+
+def test_mkc_single_row_is_kth_largest():
+    check_mkc_single_row()
+
+
+def _kbar_direct(rows, theta):
+    """Eq. 8 by counting: mean over the rows whose [min, max) holds theta of the
+    number of their elements above theta; None where no row holds theta."""
+    cnt = [int(np.sum(r > theta)) for r in rows if r.min() <= theta < r.max()]
+    return None if not cnt else sum(cnt) / len(cnt)
+
+
+def check_mkc_bruteforce(seed=6, trials=300):
+    rng = np.random.default_rng(seed)
+    for t in range(trials):
+        N, L = int(rng.integers(1, 6)), int(rng.integers(2, 9))
+        if t % 3 == 0:
+            rows = [rng.integers(0, 5, L).astype(np.float64) for _ in range(N)]
+        else:
+            rows = [rng.normal(size=L) * rng.uniform(0.2, 3) + rng.normal() for _ in range(N)]
+        pooled = np.unique(np.concatenate(rows))
+        pieces = ref.merge_intervals([ref.mkc_interval_sequence(r) for r in rows])
+        for k in range(1, L + 1):
+            th = ref.mkc_theta(pieces, k)
+            for y in pooled[pooled >= th]:
+                kb = _kbar_direct(rows, y)
+                assert kb is None or kb < k, (rows, k, th, y)
+            if np.isfinite(th):
+                assert th in pooled
+                below = pooled[pooled < th]
+                kb = _kbar_direct(rows, below[-1])
+                assert kb is not None and kb >= k, (rows, k, th)
+            else:
+                for y in pooled:
+                    kb = _kbar_direct(rows, y)
+                    assert kb is None or kb < k
+        ths = [ref.mkc_theta(pieces, k) for k in range(1, L + 1)]
+        assert all(a >= b for a, b in zip(ths, ths[1:]))          # non-increasing in k
+
+
+def test_mkc_bruteforce_sup_of_kbar():
+    check_mkc_bruteforce()
+
+
+def test_mkc_rows_spanning_theta_give_pooled_order_statistic():
+    """When every row holds theta in its [min, max), Eq. 8 is the pooled count
+    over N rows, so theta(k) is the (k N)-th largest pooled element."""
+    rng = np.random.default_rng(7)
+    for _ in range(100):
+        N, L = int(rng.integers(1, 7)), int(rng.integers(4, 12))
+        rows = [np.concatenate([[50.0 + n], rng.normal(size=L - 2), [-50.0 - n]]) for n in range(N)]
+        pooled = np.sort(np.concatenate(rows))[::-1]
+        pieces = ref.merge_intervals([ref.mkc_interval_sequence(r) for r in rows])
+        for k in range(2, L - 1):
+            assert ref.mkc_theta(pieces, k) == pooled[k * N - 1], (N, L, k)
+
+
+# ---------------------------------------------------------------------------
 # The pins above catch plausible mistakes in the oracle.
 # ---------------------------------------------------------------------------
 def _planted(monkeypatch, name, fn, check):
@@ -362,4 +478,22 @@ def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
         return th
     _planted(monkeypatch, "finalize_thresholds", first_row,
              lambda: check_golden_nearest_row(golden_dir))
+
+    # MKC: Eq. 8 averaged over all rows instead of the rows holding theta
+    def merge_all_rows(seqs):
+        out = []
+        for lo, hi, tot, cnt in orig_merge(seqs):
+            tot = sum(next((t0 for t0, a, b in sq if a <= lo < b), len(sq) + 1 if sq and lo < sq[0][1] else 0)
+                      for sq in seqs)
+            out.append((lo, hi, tot, len(seqs)))
+        return out
+    orig_merge, orig_seq, orig_inv = ref.merge_intervals, ref.mkc_interval_sequence, ref.mkc_theta
+    _planted(monkeypatch, "merge_intervals", merge_all_rows, lambda: check_golden_mkc(golden_dir))
+    # effective k off by one (elements at or above the threshold)
+    _planted(monkeypatch, "mkc_interval_sequence",
+             lambda x: [(t0 + 1, a, b) for t0, a, b in orig_seq(x)], check_mkc_single_row)
+    # inverse taken at the lower end of the piece
+    _planted(monkeypatch, "mkc_theta",
+             lambda pieces, k: max([lo for lo, hi, t, c in pieces if t >= k * c], default=-np.inf),
+             check_mkc_bruteforce)
     assert ref.row_scores is orig_scores and ref.calibration_sample is orig_sample
