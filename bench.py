@@ -71,7 +71,8 @@ def parse():
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["topt", "reference"], default="topt")
-    p.add_argument("--workload", choices=["cfg2", "cfg3", "cfg4", "cfg5"], default="cfg2")
+    p.add_argument("--workload", choices=["cfg2", "cfg3", "cfg4", "cfg5", "mkc"], default="cfg2",
+                   help="mkc: multi-k cumulative calibration on the cfg3 calibration shape")
     p.add_argument("--no-prefill", action="store_true", help="leave out the prefill object")
     p.add_argument("--dense", action="store_true",
                    help="also time the decode step with theta = -inf (on for cfg5)")
@@ -702,6 +703,9 @@ def main():
     if args.workload == "cfg3":
         main_prefill(args, dev, rank, local, world)
         return
+    if args.workload == "mkc":
+        main_mkc(args, dev, rank, local, world)
+        return
     wl = WORKLOADS[args.workload]
     layers = args.layers or wl.layers
 
@@ -932,6 +936,83 @@ def main_prefill(args, dev, rank, local, world):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+MKC_KS = (16, 32, 64, 128, 256, 512)
+MKC_WORKSPACE = 4 << 30     # scores of 8 heads per pass (512 MiB per head)
+
+
+class _CalInputs:
+    """The calibration sequences of a prefill workload, as PrefillState draws them."""
+
+    def __init__(self, wl, dev):
+        self.wl, self.dev = wl, dev
+        self.ch = synth.outlier_channels(synth.seed_of(wl.name, "channels"), wl.Hkv, wl.d)
+
+    inputs = PrefillState.inputs
+
+
+def main_mkc(args, dev, rank, local, world):
+    """--workload mkc: one layer of multi-k cumulative calibration (App. D,
+    Algorithm 2) on the calibration shape of the LLaMA-3-8B prefill workload:
+    8 causal sequences of 4096 rows, 32/8 heads, d = 128, bf16; the tables of
+    every k in MKC_KS come from one call.  value = pooled calibration scores
+    (sequences x heads x causal elements) per second, pre-softmax."""
+    wl = workloads.CFG3
+    from calibrated_thresholding_gb300 import build
+    build.build()
+    topt.lib()
+    src = _CalInputs(wl, dev)
+    Qs, Ks = zip(*[src.inputs(synth.seed_of(wl.name, "cal", s_), 1)[:2] for s_ in range(wl.n_cal)])
+    Q, K = torch.cat(Qs).contiguous(), torch.cat(Ks).contiguous()
+    del Qs, Ks
+    row_len = torch.arange(1, wl.S + 1, device=dev, dtype=torch.int32)
+    ks = torch.tensor(MKC_KS, device=dev, dtype=torch.int32)
+    theta = torch.empty((len(MKC_KS), wl.Hq, wl.S), device=dev, dtype=torch.float32)
+    status = torch.zeros(1, device=dev, dtype=torch.int32)
+    ws = torch.empty(MKC_WORKSPACE + (64 << 20), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    pooled = wl.n_cal * wl.Hq * wl.S * (wl.S + 1) // 2
+    per_head = wl.n_cal * wl.S * wl.S * 4
+    heads_per_pass = min(wl.Hq, (ws.numel() - (16 << 20)) // per_head)
+    passes = -(-wl.Hq // heads_per_pass)
+    res = {}
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    t0 = time.time()
+    for name, mode in (("pre", 0), ("post", 1)):
+        for _ in range(args.warmup):
+            topt.calibrate_multik(Q, K, row_len, ks, mode, wl.S, theta=theta, status=status, workspace=ws)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            ev[2 * i].record(stream)
+            topt.calibrate_multik(Q, K, row_len, ks, mode, wl.S, theta=theta, status=status, workspace=ws)
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+        if int(status.item()) != 0:
+            raise RuntimeError(f"topt_calibrate_multik status {int(status.item())}")
+        res[name] = float(np.mean(ms))
+    clk = clocks.stop(t0, time.time())
+    launches_pre = 1 + passes * 2 + 1
+    launches_post = launches_pre + passes
+    line = {
+        "metric": "multi-k cumulative calibration: pooled calibration scores per second",
+        "value": pooled / (res["pre"] / 1e3), "unit": "scores/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["pre"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
+                   "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS),
+                   "heads_per_pass": int(heads_per_pass),
+                   "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call"},
+        "ms_per_call": res, "pooled_scores": pooled,
+        "post_scores_per_s": pooled / (res["post"] / 1e3),
+        "gpu_launches": args.steps * (launches_pre + launches_post),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def prefill_e2e(st, args, dev, world):

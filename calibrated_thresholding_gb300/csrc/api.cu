@@ -61,6 +61,22 @@ topt_status check_calib_shape(const topt_calib_args* a) {
   return TOPT_OK;
 }
 
+topt_status check_mkc_shape(const topt_mkc_args* a) {
+  if (!a) return TOPT_EINVAL;
+  if (a->n_seqs < 1 || a->n_q_heads < 1 || a->n_kv_heads < 1 || a->n_rows < 1 || a->n_keys < 1 ||
+      a->theta_len < 1)
+    return TOPT_ESHAPE;
+  if (!dim_ok(a->head_dim)) return TOPT_ESHAPE;
+  if (a->n_q_heads % a->n_kv_heads != 0 || a->n_q_heads > 65535) return TOPT_ESHAPE;
+  if (a->dtype != TOPT_BF16 && a->dtype != TOPT_F32) return TOPT_EDTYPE;
+  if (a->mode != TOPT_PRE && a->mode != TOPT_POST) return TOPT_EINVAL;
+  if (a->n_k < 1 || a->n_k > 65535) return TOPT_EINVAL;
+  // pooled counts of one (head, length) group stay below 2^32
+  if (a->n_keys >= (1 << 20)) return TOPT_ESHAPE;
+  if ((size_t)a->n_seqs * a->n_q_heads * a->n_rows > 0x7fffffffu) return TOPT_ESHAPE;
+  return TOPT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -184,6 +200,30 @@ topt_status topt_calibrate(const topt_calib_args* a, topt_stream stream) {
     if (!a->workspace || a->workspace_bytes < minimum) return TOPT_EWORKSPACE;
   }
   return cuda_status(calibrate_launch(*a, (cudaStream_t)stream));
+}
+
+topt_status topt_calibrate_multik_workspace(const topt_mkc_args* a, size_t* bytes) {
+  topt_status st = check_mkc_shape(a);
+  if (st != TOPT_OK) return st;
+  if (!bytes) return TOPT_EINVAL;
+  const size_t fixed = calibrate_multik_fixed_bytes(*a), head = calibrate_multik_head_bytes(*a);
+  const size_t minimum = fixed + head;
+  size_t want = fixed + head * (size_t)a->n_q_heads;
+  const size_t cap = (size_t)1 << 30;
+  if (want > cap) want = cap > minimum ? cap : minimum;
+  *bytes = want;
+  return TOPT_OK;
+}
+
+topt_status topt_calibrate_multik(const topt_mkc_args* a, topt_stream stream) {
+  topt_status st = check_mkc_shape(a);
+  if (st != TOPT_OK) return st;
+  if (!a->q || !a->keys || !a->row_len || !a->ks || !a->theta) return TOPT_EINVAL;
+  if (!aligned16(a->q) || !aligned16(a->keys)) return TOPT_EINVAL;
+  const size_t minimum = calibrate_multik_fixed_bytes(*a) + calibrate_multik_head_bytes(*a);
+  if (!a->workspace || a->workspace_bytes < minimum || (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
+    return TOPT_EWORKSPACE;
+  return cuda_status(calibrate_multik_launch(*a, (cudaStream_t)stream));
 }
 
 topt_status topt_select_kth(const float* x, int32_t rows, int32_t row_stride, const int32_t* row_len,

@@ -16,6 +16,9 @@
 //                         count at [head][L-1]
 //   calib_finalize_kernel one CTA per head: mean + alpha*std, dense rows,
 //                         nearest calibrated row id for the rest.
+// The second half of the file is multi-k cumulative calibration
+// [TopTheta App. D, Algorithm 2]: every threshold table theta(k) of a list of
+// targets k from one pass over the calibration rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,6 +29,7 @@ constexpr int kScoreKeys = 128;  // keys per score CTA (one per thread)
 constexpr int kScoreRows = 8;    // query rows per score CTA
 constexpr int kSelThreads = 256;
 constexpr int kFinThreads = 1024;
+constexpr long kMaxPassRows = 65535L * kScoreRows;  // grid.y limit of the score kernel
 
 // Order-preserving map float -> uint32 (-0.0 is folded onto +0.0).
 __device__ __forceinline__ uint32_t f2key(float f) {
@@ -43,20 +47,21 @@ struct SelectSmem {
   float red[kSelThreads / kWarp];
 };
 
-// Exact k-th largest (1-based, 1 <= k <= L) of row[0..L-1], computed by the
-// whole CTA with four 8-bit digit passes from the most significant digit.
-__device__ float cta_select_kth(const float* __restrict__ row, int L, int k, SelectSmem& sm) {
+// Key of the k-th largest (1-based, 1 <= k <= count) of the elements that
+// `visit` hands out, computed by the whole CTA with four 8-bit digit passes
+// from the most significant digit.  visit(f) calls f(key) once for every
+// element of this thread's share; it runs once per pass.
+template <class Visit>
+__device__ uint32_t cta_select_key(const Visit& visit, unsigned kk, SelectSmem& sm) {
   uint32_t prefix = 0u, pmask = 0u;
-  unsigned kk = (unsigned)k;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kSelThreads) sm.hist[i] = 0u;
+    for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0u;
     __syncthreads();
-    for (int j = tid; j < L; j += kSelThreads) {
-      const uint32_t key = f2key(row[j]);
+    visit([&](uint32_t key) {
       if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
-    }
+    });
     __syncthreads();
     if (tid < kWarp) {
       // Lane l owns bins 255-8l down to 248-8l (descending order of value).
@@ -92,7 +97,15 @@ __device__ float cta_select_kth(const float* __restrict__ row, int L, int k, Sel
     pmask |= 0xffu << shift;
     kk = sm.sel[1];
   }
-  return key2f(prefix);
+  return prefix;
+}
+
+// Exact k-th largest (1-based, 1 <= k <= L) of row[0..L-1].
+__device__ float cta_select_kth(const float* __restrict__ row, int L, int k, SelectSmem& sm) {
+  const auto visit = [&](auto&& f) {
+    for (int j = threadIdx.x; j < L; j += blockDim.x) f(f2key(row[j]));
+  };
+  return key2f(cta_select_key(visit, (unsigned)k, sm));
 }
 
 __device__ float cta_reduce_max(float v, SelectSmem& sm) {
@@ -131,6 +144,7 @@ __device__ __forceinline__ void load8(const float* src, float f[8]) {
 
 struct CalibParams {
   int N, Hq, Hkv, R, Nk, Lmax, mode, k;
+  int h0, Hp;  // the score kernel covers query heads h0 .. h0+Hp-1
   float alpha, sm_scale;
   const void* q;
   const void* keys;
@@ -141,37 +155,41 @@ struct CalibParams {
   int32_t* status;
 };
 
-// Scores of rows [it0, it0 + nrows) of the flattened (seq, head, row) index.
+// Scores of rows [it0, it0 + nrows) of the flattened (seq, head, row) index
+// over the heads h0 .. h0+Hp-1; row it0 + r goes to ws row r.
 template <typename T, int D>
 __global__ void __launch_bounds__(kScoreKeys) calib_scores_kernel(const CalibParams p, long it0,
                                                                   int nrows, float* __restrict__ ws) {
   __shared__ float qs[kScoreRows][D];
   __shared__ int s_L[kScoreRows];
   __shared__ long s_kofs[kScoreRows];
+  __shared__ long s_qofs[kScoreRows];
   const int r0 = blockIdx.y * kScoreRows;
   const T* Q = static_cast<const T*>(p.q);
   const T* K = static_cast<const T*>(p.keys);
-  for (int idx = threadIdx.x; idx < kScoreRows * D; idx += kScoreKeys) {
-    const int r = idx / D, dd = idx - r * D;
-    const long it = it0 + r0 + r;
-    qs[r][dd] = (r0 + r < nrows) ? to_f32<T>(Q[it * D + dd]) : 0.f;
-  }
   if (threadIdx.x < kScoreRows) {
     const int r = threadIdx.x;
     const long it = it0 + r0 + r;
     int L = 0;
-    long kofs = 0;
+    long kofs = 0, qofs = -1;
     if (r0 + r < nrows) {
       const long i = it % p.R;
       const long nh = it / p.R;
-      const long h = nh % p.Hq;
-      const long n = nh / p.Hq;
+      const long h = p.h0 + nh % p.Hp;
+      const long n = nh / p.Hp;
       L = p.row_len[i];
       if (L < 1 || L > p.Nk) L = 0;
       kofs = ((n * p.Hkv) + h / (p.Hq / p.Hkv)) * (long)p.Nk * D;
+      qofs = ((n * p.Hq + h) * p.R + i) * D;
     }
     s_L[r] = L;
     s_kofs[r] = kofs;
+    s_qofs[r] = qofs;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kScoreRows * D; idx += kScoreKeys) {
+    const int r = idx / D, dd = idx - r * D;
+    qs[r][dd] = s_qofs[r] >= 0 ? to_f32<T>(Q[s_qofs[r] + dd]) : 0.f;
   }
   __syncthreads();
   const int j = blockIdx.x * kScoreKeys + threadIdx.x;
@@ -265,20 +283,22 @@ __device__ __forceinline__ float calib_value(const CalibParams& p, size_t cell) 
   return (float)(mean + (double)p.alpha * sd);
 }
 
-// One CTA per head.  Segment-wise forward/backward sweeps find, for every row
-// id, the nearest calibrated row below and above.
-__global__ void __launch_bounds__(kFinThreads) calib_finalize_kernel(const CalibParams p) {
+// One head's row of a threshold table, written by one CTA of kFinThreads:
+// has(i) says whether row id L = i+1 was calibrated, val(i) its value.
+// Rows with L <= k are dense (-inf); any other row takes the nearest
+// calibrated row id (ties: the shorter row); no calibrated row: dense.
+// Segment-wise forward/backward sweeps find, for every row id, the nearest
+// calibrated row below and above; out[] holds the forward result as int bits
+// in between.
+template <class Has, class Val>
+__device__ void fill_nearest_rows(int Lmax, int k, const Has& has, const Val& val, float* out) {
   __shared__ int s_last[kFinThreads], s_first[kFinThreads];
-  const int h = blockIdx.x;
-  const int Lmax = p.Lmax;
   const int seg = (Lmax + kFinThreads - 1) / kFinThreads;
-  const int lo = min(threadIdx.x * seg, Lmax);
+  const int lo = min((int)threadIdx.x * seg, Lmax);
   const int hi = min(lo + seg, Lmax);
-  const int32_t* cnt = p.count + (size_t)h * Lmax;
-  float* th = p.theta + (size_t)h * Lmax;
   int last = -1, first = -1;
   for (int i = lo; i < hi; ++i)
-    if (cnt[i] > 0) {
+    if (has(i)) {
       last = i;
       if (first < 0) first = i;
     }
@@ -291,28 +311,38 @@ __global__ void __launch_bounds__(kFinThreads) calib_finalize_kernel(const Calib
     if (s_first[u] >= 0) next = s_first[u];
   // forward: nearest calibrated index at or below i, stored as int bits
   for (int i = lo; i < hi; ++i) {
-    if (cnt[i] > 0) prev = i;
-    th[i] = __int_as_float(prev);
+    if (has(i)) prev = i;
+    out[i] = __int_as_float(prev);
   }
   // backward: nearest at or above, then decide
   for (int i = hi - 1; i >= lo; --i) {
-    if (cnt[i] > 0) next = i;
-    const int below = __float_as_int(th[i]);
+    const bool hit = has(i);
+    if (hit) next = i;
+    const int below = __float_as_int(out[i]);
     const int L = i + 1;
     float v;
-    if (cnt[i] > 0) {
-      v = calib_value(p, (size_t)h * Lmax + i);
-    } else if (L <= p.k || (below < 0 && next < 0)) {
+    if (hit) {
+      v = val(i);
+    } else if (L <= k || (below < 0 && next < 0)) {
       v = -CUDART_INF_F;
     } else {
       int pick;
       if (below < 0) pick = next;
       else if (next < 0) pick = below;
       else pick = (i - below <= next - i) ? below : next;
-      v = calib_value(p, (size_t)h * Lmax + pick);
+      v = val(pick);
     }
-    th[i] = v;
+    out[i] = v;
   }
+}
+
+// One CTA per head.
+__global__ void __launch_bounds__(kFinThreads) calib_finalize_kernel(const CalibParams p) {
+  const int h = blockIdx.x;
+  const int32_t* cnt = p.count + (size_t)h * p.Lmax;
+  const auto has = [&](int i) { return cnt[i] > 0; };
+  const auto val = [&](int i) { return calib_value(p, (size_t)h * p.Lmax + i); };
+  fill_nearest_rows(p.Lmax, p.k, has, val, p.theta + (size_t)h * p.Lmax);
 }
 
 template <typename T, int D>
@@ -323,6 +353,310 @@ cudaError_t calib_pass(const CalibParams& p, long it0, int nrows, float* ws, cud
   if (e != cudaSuccess) return e;
   calib_select_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Multi-k cumulative calibration [TopTheta App. D, Algorithm 2, Eq. 8].
+//
+// For the calibration rows of one head and one length r (N_r rows, pooled
+// values x), Eq. 8 averages the effective k of the rows whose [min, max)
+// holds theta.  With B(theta) = #{rows whose maximum is > theta},
+// A(theta) = #{rows whose minimum is > theta} and P(theta) = #{x > theta}:
+//   k_bar(theta) >= k  <=>  B - A > 0  and  P >= k B + (r - k) A,
+// because every row with min <= theta < max has #{its x > theta} elements
+// above theta, a row with min > theta has all r and a row with max <= theta
+// none.  B and A change only at row maxima and minima ("events"); between
+// two consecutive events the condition is monotone in theta.  So
+// theta(k) = sup{theta : k_bar(theta) >= k} is found from the highest event
+// e that starts a valid stretch [e, u) (u the next event above e):
+//   theta(k) = min(u, the T-th largest x),  T = k B(e) + (r - k) A(e).
+// The kernel sorts the events in shared memory, counts P at every event
+// with two histograms of the pooled values, and makes one radix select per
+// target k.
+// ---------------------------------------------------------------------------
+constexpr int kMkcMaxSamples = 4096;  // calibration rows of one head and length per call
+constexpr int kMkcThreads = kSelThreads;
+constexpr int kIdxThreads = 1024;
+
+struct MkcSmem {
+  uint32_t mx[kMkcMaxSamples];      // row maxima (keys), sorted descending
+  uint32_t mn[kMkcMaxSamples];      // row minima (keys), sorted descending
+  uint32_t px[kMkcMaxSamples + 1];  // px[c] = #{x : #{mx >= x} <= c} after the scan
+  uint32_t pn[kMkcMaxSamples + 1];  // same against the minima
+};
+
+struct MkcParams {
+  int N, Hq, R, Nk, Lmax, n_k, h0, Hp, mode;
+  const int32_t* ks;         // [n_k] target k values
+  const int32_t* row_len;    // [R]
+  int32_t* len_cnt;          // [Lmax + 1] rows of a sequence with L keys
+  int32_t* len_start;        // [Lmax + 1] first slot of length L in `order`
+  int32_t* order;            // [R] row ids grouped by length
+  float* ws;                 // scores (log-softmax for POST) [N][Hp][R][Nk] of the pass
+  float* gval;               // [n_k][Hq][Lmax] theta_L(k) of the calibrated lengths
+  int32_t* status;
+};
+
+// Rows grouped by length: counting sort of row_len (one CTA).
+__global__ void __launch_bounds__(kIdxThreads) mkc_index_kernel(const MkcParams p, int32_t* cur) {
+  __shared__ int tot[kIdxThreads];
+  int32_t* cnt = p.len_cnt;
+  int32_t* start = p.len_start;
+  int32_t* order = p.order;
+  const int n = p.Lmax + 1;
+  for (int i = threadIdx.x; i < n; i += kIdxThreads) cnt[i] = 0;
+  for (int i = threadIdx.x; i < p.n_k; i += kIdxThreads)
+    if (p.ks[i] < 1) set_status(p.status, TOPT_EINVAL);
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.R; i += kIdxThreads) {
+    const int L = p.row_len[i];
+    if (L < 1 || L > p.Nk || L > p.Lmax) set_status(p.status, TOPT_EINVAL);
+    else atomicAdd(&cnt[L], 1);
+  }
+  __syncthreads();
+  const int seg = (n + kIdxThreads - 1) / kIdxThreads;
+  const int lo = min((int)threadIdx.x * seg, n), hi = min(lo + seg, n);
+  int t = 0;
+  for (int i = lo; i < hi; ++i) t += cnt[i];
+  tot[threadIdx.x] = t;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int u = 0; u < kIdxThreads; ++u) {
+      const int v = tot[u];
+      tot[u] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  int run = tot[threadIdx.x];
+  for (int i = lo; i < hi; ++i) {
+    start[i] = run;
+    cur[i] = run;
+    run += cnt[i];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.R; i += kIdxThreads) {
+    const int L = p.row_len[i];
+    if (L >= 1 && L <= p.Nk && L <= p.Lmax) order[atomicAdd(&cur[L], 1)] = i;
+  }
+}
+
+// POST: every score row of the pass becomes its log-softmax a - m - ln Z, in
+// place.  It orders the pooled values as the softmax values do (exp is
+// increasing) without the fp32 underflow of small probabilities to one tied
+// zero; the selected threshold is exponentiated at the end.
+__global__ void __launch_bounds__(kSelThreads) mkc_softmax_kernel(const MkcParams p) {
+  __shared__ SelectSmem sm;
+  const long lr = blockIdx.x;
+  const int L = p.row_len[lr % p.R];
+  if (L < 1 || L > p.Nk || L > p.Lmax) return;
+  float* row = p.ws + lr * p.Nk;
+  float m = -CUDART_INF_F;
+  for (int j = threadIdx.x; j < L; j += kSelThreads) m = fmaxf(m, row[j]);
+  m = cta_reduce_max(m, sm);
+  float z = 0.f;
+  for (int j = threadIdx.x; j < L; j += kSelThreads) z += expf(row[j] - m);
+  z = cta_reduce_sum(z, sm);
+  const float lz = logf(z);
+  for (int j = threadIdx.x; j < L; j += kSelThreads) row[j] = (row[j] - m) - lz;
+}
+
+// Entries of a[0..n) (sorted descending) that are > key, or >= key.
+__device__ __forceinline__ int count_gt(const uint32_t* a, int n, uint32_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] > key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+__device__ __forceinline__ int count_ge(const uint32_t* a, int n, uint32_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] >= key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Inclusive prefix sums of a[0..n) and b[0..n) by the whole CTA.
+__device__ void cta_scan2(uint32_t* a, uint32_t* b, int n) {
+  __shared__ uint32_t ta[kMkcThreads], tb[kMkcThreads];
+  const int seg = (n + kMkcThreads - 1) / kMkcThreads;
+  const int lo = min((int)threadIdx.x * seg, n), hi = min(lo + seg, n);
+  uint32_t sa = 0u, sb = 0u;
+  for (int i = lo; i < hi; ++i) {
+    sa += a[i];
+    sb += b[i];
+  }
+  ta[threadIdx.x] = sa;
+  tb[threadIdx.x] = sb;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t ra = 0u, rb = 0u;
+    for (int u = 0; u < kMkcThreads; ++u) {
+      const uint32_t va = ta[u], vb = tb[u];
+      ta[u] = ra;
+      tb[u] = rb;
+      ra += va;
+      rb += vb;
+    }
+  }
+  __syncthreads();
+  uint32_t ra = ta[threadIdx.x], rb = tb[threadIdx.x];
+  for (int i = lo; i < hi; ++i) {
+    ra += a[i];
+    rb += b[i];
+    a[i] = ra;
+    b[i] = rb;
+  }
+  __syncthreads();
+}
+
+// One CTA per (row length L, head of the pass).
+__global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams p) {
+  extern __shared__ __align__(16) unsigned char mkc_raw[];
+  MkcSmem& sh = *reinterpret_cast<MkcSmem*>(mkc_raw);
+  __shared__ SelectSmem sm;
+  __shared__ uint32_t s_best[kMkcThreads / kWarp];
+  const int L = blockIdx.x + 1;
+  const int hl = blockIdx.y;
+  const int c = p.len_cnt[L];
+  if (c == 0 || L < 2) return;  // a row of one key has no interval
+  bool wanted = false;
+  for (int ki = 0; ki < p.n_k; ++ki) wanted |= (p.ks[ki] >= 1 && p.ks[ki] < L);
+  if (!wanted) return;  // row id L <= k is dense for every target
+  const long nr_l = (long)p.N * c;
+  if (nr_l > kMkcMaxSamples) {
+    if (threadIdx.x == 0) set_status(p.status, TOPT_EINVAL);
+    return;
+  }
+  const int Nr = (int)nr_l;
+  int cap = 1;
+  while (cap < Nr) cap <<= 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int nw = kMkcThreads / kWarp;
+  const int base = p.len_start[L];
+  const auto rowp = [&](int s) -> const float* {
+    const int n = s / c, idx = s - n * c;
+    const int i = p.order[base + idx];
+    return p.ws + (((long)n * p.Hp + hl) * p.R + i) * p.Nk;
+  };
+  // 1. maximum and minimum of every row; padding (key 0) sorts last
+  for (int s = warp; s < cap; s += nw) {
+    uint32_t hi_k = 0u, lo_k = 0u;
+    if (s < Nr) {
+      const float* row = rowp(s);
+      lo_k = 0xffffffffu;
+      for (int j = lane; j < L; j += kWarp) {
+        const uint32_t key = f2key(row[j]);
+        hi_k = max(hi_k, key);
+        lo_k = min(lo_k, key);
+      }
+      hi_k = __reduce_max_sync(0xffffffffu, hi_k);
+      lo_k = __reduce_min_sync(0xffffffffu, lo_k);
+    }
+    if (lane == 0) {
+      sh.mx[s] = hi_k;
+      sh.mn[s] = lo_k;
+    }
+  }
+  __syncthreads();
+  // 2. bitonic sort of both event arrays, descending
+  for (int size = 2; size <= cap; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < cap / 2; t += kMkcThreads) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        uint32_t a = sh.mx[lo], b = sh.mx[hi];
+        if ((a < b) == desc) {
+          sh.mx[lo] = b;
+          sh.mx[hi] = a;
+        }
+        a = sh.mn[lo];
+        b = sh.mn[hi];
+        if ((a < b) == desc) {
+          sh.mn[lo] = b;
+          sh.mn[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // 3. P at every event: x > e <=> #{events >= x} <= #{events > e}
+  for (int i = tid; i <= Nr; i += kMkcThreads) {
+    sh.px[i] = 0u;
+    sh.pn[i] = 0u;
+  }
+  __syncthreads();
+  for (int s = warp; s < Nr; s += nw) {
+    const float* row = rowp(s);
+    for (int j = lane; j < L; j += kWarp) {
+      const uint32_t key = f2key(row[j]);
+      atomicAdd(&sh.px[count_ge(sh.mx, Nr, key)], 1u);
+      atomicAdd(&sh.pn[count_ge(sh.mn, Nr, key)], 1u);
+    }
+  }
+  __syncthreads();
+  cta_scan2(sh.px, sh.pn, Nr + 1);
+  // 4. every target k
+  const auto visit = [&](auto&& f) {
+    for (int s = warp; s < Nr; s += nw) {
+      const float* row = rowp(s);
+      for (int j = lane; j < L; j += kWarp) f(f2key(row[j]));
+    }
+  };
+  for (int ki = 0; ki < p.n_k; ++ki) {
+    const int k = p.ks[ki];
+    if (k < 1 || k >= L) continue;  // uniform over the CTA
+    uint32_t best = 0u;
+    for (int t = tid; t < 2 * Nr; t += kMkcThreads) {
+      const bool from_max = t < Nr;
+      const uint32_t e = from_max ? sh.mx[t] : sh.mn[t - Nr];
+      const int bx = count_gt(sh.mx, Nr, e);
+      const int a = count_gt(sh.mn, Nr, e);
+      if (bx - a <= 0) continue;
+      const uint32_t P = from_max ? sh.px[bx] : sh.pn[a];
+      const long T = (long)k * bx + (long)(L - k) * a;
+      if ((long)P >= T) best = max(best, e);
+    }
+    best = __reduce_max_sync(0xffffffffu, best);
+    __syncthreads();
+    if (lane == 0) s_best[warp] = best;
+    __syncthreads();
+    best = 0u;
+#pragma unroll
+    for (int w = 0; w < nw; ++w) best = max(best, s_best[w]);
+    const size_t cell = ((size_t)ki * p.Hq + p.h0 + hl) * p.Lmax + (L - 1);
+    if (best == 0u) {  // no stretch reaches k
+      if (tid == 0) p.gval[cell] = -CUDART_INF_F;
+      continue;
+    }
+    const int bx = count_gt(sh.mx, Nr, best);
+    const int a = count_gt(sh.mn, Nr, best);
+    uint32_t u = sh.mx[bx - 1];  // bx >= 1: a valid stretch has a maximum above it
+    if (a > 0) u = min(u, sh.mn[a - 1]);
+    const unsigned T = (unsigned)((long)k * bx + (long)(L - k) * a);
+    const uint32_t y = cta_select_key(visit, T, sm);
+    if (tid == 0) {
+      const float v = key2f(min(y, u));
+      p.gval[cell] = p.mode == TOPT_POST ? expf(v) : v;
+    }
+  }
+}
+
+// One CTA per (head, target k): the table of that k.
+__global__ void __launch_bounds__(kFinThreads) mkc_finalize_kernel(const MkcParams p, float* theta) {
+  const int h = blockIdx.x, ki = blockIdx.y;
+  const int k = p.ks[ki];
+  const size_t off = ((size_t)ki * p.Hq + h) * p.Lmax;
+  const auto has = [&](int i) { return i + 1 > k && p.len_cnt[i + 1] > 0; };
+  const auto val = [&](int i) { return p.gval[off + i]; };
+  fill_nearest_rows(p.Lmax, k, has, val, theta + off);
 }
 
 }  // namespace
@@ -343,6 +677,8 @@ cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s) {
   p.Lmax = a.theta_len;
   p.mode = a.mode;
   p.k = a.k;
+  p.h0 = 0;
+  p.Hp = a.n_q_heads;
   p.alpha = a.alpha;
   p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
   p.q = a.q;
@@ -364,7 +700,7 @@ cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s) {
     size_t per_row = (size_t)a.n_keys * sizeof(float);
     long rows_per_pass = (long)(a.workspace_bytes / per_row);
     rows_per_pass = rows_per_pass / kScoreRows * kScoreRows;
-    if (rows_per_pass > (1L << 20)) rows_per_pass = 1L << 20;
+    if (rows_per_pass > kMaxPassRows) rows_per_pass = kMaxPassRows;
     if (rows_per_pass < kScoreRows) return cudaErrorInvalidValue;
     float* ws = static_cast<float*>(a.workspace);
     for (long it0 = 0; it0 < total; it0 += rows_per_pass) {
@@ -384,6 +720,107 @@ cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Workspace of multi-k calibration: row index, per-k values, then the scores
+// of as many heads as fit.
+size_t calibrate_multik_fixed_bytes(const topt_mkc_args& a) {
+  return 3 * align256((size_t)(a.theta_len + 1) * sizeof(int32_t)) +
+         align256((size_t)a.n_rows * sizeof(int32_t)) +
+         align256((size_t)a.n_k * a.n_q_heads * a.theta_len * sizeof(float));
+}
+size_t calibrate_multik_head_bytes(const topt_mkc_args& a) {
+  return align256((size_t)a.n_seqs * a.n_rows * a.n_keys * sizeof(float));
+}
+int calibrate_multik_max_samples() { return kMkcMaxSamples; }
+
+template <typename T, int D>
+cudaError_t mkc_scores(const CalibParams& cp, long total, float* ws, cudaStream_t s) {
+  for (long it0 = 0; it0 < total; it0 += kMaxPassRows) {
+    const int nrows = (int)((total - it0) < kMaxPassRows ? (total - it0) : kMaxPassRows);
+    dim3 g((cp.Nk + kScoreKeys - 1) / kScoreKeys, (nrows + kScoreRows - 1) / kScoreRows);
+    calib_scores_kernel<T, D><<<g, kScoreKeys, 0, s>>>(cp, it0, nrows, ws + it0 * (long)cp.Nk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t calibrate_multik_launch(const topt_mkc_args& a, cudaStream_t s) {
+  static bool attr_set = false;
+  cudaError_t e;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(mkc_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(MkcSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  char* w = static_cast<char*>(a.workspace);
+  const size_t lb = align256((size_t)(a.theta_len + 1) * sizeof(int32_t));
+  MkcParams p;
+  p.N = a.n_seqs;
+  p.Hq = a.n_q_heads;
+  p.R = a.n_rows;
+  p.Nk = a.n_keys;
+  p.Lmax = a.theta_len;
+  p.n_k = a.n_k;
+  p.mode = a.mode;
+  p.ks = a.ks;
+  p.row_len = a.row_len;
+  p.len_cnt = reinterpret_cast<int32_t*>(w);
+  p.len_start = reinterpret_cast<int32_t*>(w + lb);
+  int32_t* cur = reinterpret_cast<int32_t*>(w + 2 * lb);
+  p.order = reinterpret_cast<int32_t*>(w + 3 * lb);
+  p.gval = reinterpret_cast<float*>(w + 3 * lb + align256((size_t)a.n_rows * sizeof(int32_t)));
+  p.status = a.status;
+  float* ws = reinterpret_cast<float*>(w + calibrate_multik_fixed_bytes(a));
+  const size_t per_head = calibrate_multik_head_bytes(a);
+  size_t fit = (a.workspace_bytes - calibrate_multik_fixed_bytes(a)) / per_head;
+  const int Hp = fit < (size_t)a.n_q_heads ? (int)fit : a.n_q_heads;
+  if (Hp < 1) return cudaErrorInvalidValue;
+  p.ws = ws;
+
+  mkc_index_kernel<<<1, kIdxThreads, 0, s>>>(p, cur);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  CalibParams cp;
+  cp.N = a.n_seqs;
+  cp.Hq = a.n_q_heads;
+  cp.Hkv = a.n_kv_heads;
+  cp.R = a.n_rows;
+  cp.Nk = a.n_keys;
+  cp.Lmax = a.theta_len;
+  cp.mode = a.mode;
+  cp.k = 1;
+  cp.alpha = 0.f;
+  cp.sm_scale = 1.0f / sqrtf((float)a.head_dim);
+  cp.q = a.q;
+  cp.keys = a.keys;
+  cp.row_len = a.row_len;
+  cp.acc = nullptr;
+  cp.count = nullptr;
+  cp.theta = nullptr;
+  cp.status = a.status;
+  for (int h0 = 0; h0 < a.n_q_heads; h0 += Hp) {
+    const int hp = (a.n_q_heads - h0) < Hp ? (a.n_q_heads - h0) : Hp;
+    cp.h0 = p.h0 = h0;
+    cp.Hp = p.Hp = hp;
+    const long total = (long)a.n_seqs * hp * a.n_rows;
+    if (a.dtype == TOPT_BF16) {
+      e = a.head_dim == 128 ? mkc_scores<__nv_bfloat16, 128>(cp, total, ws, s)
+                            : mkc_scores<__nv_bfloat16, 64>(cp, total, ws, s);
+    } else {
+      e = a.head_dim == 128 ? mkc_scores<float, 128>(cp, total, ws, s) : mkc_scores<float, 64>(cp, total, ws, s);
+    }
+    if (e != cudaSuccess) return e;
+    if (a.mode == TOPT_POST) {
+      mkc_softmax_kernel<<<(unsigned)total, kSelThreads, 0, s>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    mkc_group_kernel<<<dim3((unsigned)a.theta_len, (unsigned)hp), kMkcThreads, sizeof(MkcSmem), s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  mkc_finalize_kernel<<<dim3((unsigned)a.n_q_heads, (unsigned)a.n_k), kFinThreads, 0, s>>>(p, a.theta);
+  return cudaGetLastError();
 }
 
 cudaError_t select_kth_launch(const float* x, int32_t rows, int32_t stride, const int32_t* row_len,

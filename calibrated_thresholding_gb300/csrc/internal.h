@@ -36,6 +36,11 @@ cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax
 size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);
 size_t calibrate_min_rows_per_pass();
 cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s);
+// multi-k cumulative calibration: fixed workspace + one head's scores per head
+size_t calibrate_multik_fixed_bytes(const topt_mkc_args& a);
+size_t calibrate_multik_head_bytes(const topt_mkc_args& a);
+int calibrate_multik_max_samples();
+cudaError_t calibrate_multik_launch(const topt_mkc_args& a, cudaStream_t s);
 cudaError_t select_kth_launch(const float* x, int32_t rows, int32_t stride,
                               const int32_t* row_len, int32_t k, float* out,
                               int32_t* status, cudaStream_t s);

@@ -58,6 +58,14 @@ class CalibArgs(ctypes.Structure):
                 ("status", vp), ("workspace", vp), ("workspace_bytes", sz)]
 
 
+class MkcArgs(ctypes.Structure):
+    _fields_ = [("n_seqs", i32), ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
+                ("n_rows", i32), ("n_keys", i32), ("theta_len", i32), ("dtype", i32),
+                ("mode", i32), ("n_k", i32), ("ks", vp), ("q", vp), ("keys", vp),
+                ("row_len", vp), ("theta", vp), ("status", vp), ("workspace", vp),
+                ("workspace_bytes", sz)]
+
+
 class VmeanArgs(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_kv_heads", i32), ("head_dim", i32), ("cache_len", i32),
                 ("dtype", i32), ("n_new", i32), ("v_cache", vp), ("n_old", vp), ("mu", vp),
@@ -69,7 +77,7 @@ _lock = threading.Lock()
 
 SYMBOLS = ["topt_decode_workspace", "topt_decode", "topt_decode_noalloc", "topt_prefill_workspace",
            "topt_prefill_tile_shape", "topt_prefill", "topt_prefill_test_timeout", "topt_calibrate_workspace",
-           "topt_calibrate", "topt_select_kth", "topt_vmean_update", "topt_version",
+           "topt_calibrate", "topt_calibrate_multik_workspace", "topt_calibrate_multik", "topt_select_kth", "topt_vmean_update", "topt_version",
            "topt_status_string"]
 
 
@@ -338,6 +346,38 @@ class Calibrator:
         a = self._args(None, None, None, CALIB_FINALIZE, status)
         _check("topt_calibrate", lib().topt_calibrate(ctypes.byref(a), _stream(stream)))
         return self.theta
+
+
+def calibrate_multik(q, keys, row_len, ks, mode, theta_len, theta=None, status=None,
+                     workspace=None, stream=None):
+    """Multi-k cumulative calibration of one layer [TopTheta App. D, Algorithm 2].
+
+    q [N][Hq][R][d] and keys [N][Hkv][Nk][d] on the GPU, row_len [R] int32,
+    ks [n_k] int32 target k values.  Returns theta [n_k][Hq][theta_len]:
+    theta[ki] is the table for ks[ki] (topt_calibrate_multik).
+    """
+    N, Hq, R, d = q.shape
+    ks = _dev(ks, "ks", torch.int32)
+    n_k = ks.numel()
+    if theta is None:
+        theta = torch.empty((n_k, Hq, theta_len), device=q.device, dtype=torch.float32)
+    a = MkcArgs()
+    a.n_seqs, a.n_q_heads, a.n_kv_heads, a.head_dim = N, Hq, keys.shape[1], d
+    a.n_rows, a.n_keys, a.theta_len = R, keys.shape[2], int(theta_len)
+    a.dtype, a.mode, a.n_k = _dtype_code(q), int(mode), n_k
+    a.ks, a.q, a.keys = _ptr(ks), _ptr(_dev(q, "q")), _ptr(_dev(keys, "keys"))
+    a.row_len = _ptr(_dev(row_len, "row_len", torch.int32))
+    a.theta = _ptr(_dev(theta, "theta", torch.float32))
+    a.status = _ptr(_dev(status, "status", torch.int32))
+    if workspace is None:
+        n = sz(0)
+        _check("topt_calibrate_multik_workspace",
+               lib().topt_calibrate_multik_workspace(ctypes.byref(a), ctypes.byref(n)))
+        workspace = torch.empty(n.value, device=q.device, dtype=torch.uint8)
+    a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
+    a.workspace_bytes = workspace.numel()
+    _check("topt_calibrate_multik", lib().topt_calibrate_multik(ctypes.byref(a), _stream(stream)))
+    return theta
 
 
 def select_kth(x, row_len, k, out=None, status=None, stream=None):

@@ -220,6 +220,59 @@ topt_status topt_calibrate_workspace(const topt_calib_args* args, size_t* bytes)
  *                     -INFINITY if the head has no calibrated row.          */
 topt_status topt_calibrate(const topt_calib_args* args, topt_stream stream);
 
+/* ------------------------------------------------------------------------ */
+/* Multi-k cumulative calibration (MKC) [TopTheta App. D, Algorithm 2,      */
+/* Eq. 8], one layer per call: the threshold tables of several target k     */
+/* from one pass over the calibration rows, so that k can be chosen when    */
+/* serving by offsetting the theta pointer by ki * Hq * Lmax.                */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_seqs;       /* N >= 1 calibration sequences */
+  int32_t n_q_heads;    /* Hq (<= 65535) */
+  int32_t n_kv_heads;   /* Hkv */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t n_rows;       /* R query rows per sequence */
+  int32_t n_keys;       /* Nk keys per sequence, < 2^20 */
+  int32_t theta_len;    /* Lmax */
+  int32_t dtype;        /* topt_dtype of q and keys */
+  int32_t mode;         /* topt_mode: intervals of a (PRE) or of softmax(a) (POST) */
+  int32_t n_k;          /* number of target k values, 1..65535 */
+  const int32_t* ks;    /* [n_k] device, each >= 1 (any order, repeats allowed) */
+  const void* q;        /* [N][Hq][R][d] device, 16-byte aligned */
+  const void* keys;     /* [N][Hkv][Nk][d] device, 16-byte aligned */
+  const int32_t* row_len; /* [R] device: keys seen by each query row, 1..min(Nk, Lmax) */
+  float* theta;         /* [n_k][Hq][Lmax] device, written */
+  int32_t* status;      /* device int32 or NULL; set to TOPT_EINVAL on a bad row_len
+                           or k, or when more than 4096 rows (N times the rows of
+                           one length) share a head and a length; theta is then
+                           undefined */
+  void* workspace;      /* device, 256-byte aligned, caller-owned */
+  size_t workspace_bytes;
+} topt_mkc_args;
+
+/* Minimum workspace: the row index, n_k*Hq*Lmax floats and the scores of one
+ * head (N*R*Nk floats); every further head's scores let one pass cover more
+ * heads.  *bytes covers all heads at once, capped at 1 GiB (but not below
+ * the minimum). */
+topt_status topt_calibrate_multik_workspace(const topt_mkc_args* args, size_t* bytes);
+
+/* For every head h and row length r that some row has, the calibration rows
+ * of length r of all N sequences give the function k_bar_r(theta) of Eq. 8:
+ * the mean, over the rows whose [min, max) holds theta, of the number of
+ * their scores (PRE) or softmax values (POST) above theta.  Then, per target
+ * k (index ki):
+ *   theta[ki][h][r-1] = sup{theta : k_bar_r(theta) >= k}, one of the
+ *                       calibration values (the paper leaves the inverse of
+ *                       k_bar open; this is the largest threshold up to
+ *                       which the rows keep at least k on average), or
+ *                       -INFINITY when no theta reaches k;
+ *   L <= k            -INFINITY (the row is kept whole);
+ *   other L           the value of the nearest calibrated r > k (ties:
+ *                     smaller r); -INFINITY if there is none.
+ * For N = 1 and a row whose k-th largest value exceeds its minimum, the
+ * result is that k-th largest value, as Algorithm 1 gives with alpha = 0. */
+topt_status topt_calibrate_multik(const topt_mkc_args* args, topt_stream stream);
+
 /* Building block of calibration, exposed for testing: out[r] = the k-th
  * largest of x[r][0 .. row_len[r]-1] (x is [rows][row_stride] fp32 on the
  * device; -0.0 counts as +0.0; -INFINITY if row_len[r] < k).  Exact: the

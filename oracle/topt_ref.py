@@ -41,7 +41,6 @@ reason in the design notes of the repository):
 """
 from __future__ import annotations
 
-import bisect
 import math
 
 import numpy as np
@@ -211,20 +210,27 @@ def merge_intervals(seqs):
     out: k_bar is undefined there.  Returns (lo, hi, sum_t0, n_intervals)
     with the mean kept as an exact ratio of integers.
     """
-    ends = sorted({e for seq in seqs for (_, lo, hi) in seq for e in (lo, hi)})
-    starts = [[a for (_, a, _) in seq] for seq in seqs]
-    pieces = []
-    for lo, hi in zip(ends[:-1], ends[1:]):
-        tot = cnt = 0
-        for seq, st in zip(seqs, starts):
-            # the last interval starting at or below lo is the only candidate
-            j = bisect.bisect_right(st, lo) - 1
-            if j >= 0 and lo < seq[j][2]:
-                tot += seq[j][0]
-                cnt += 1
-        if cnt:
-            pieces.append((lo, hi, tot, cnt))
-    return pieces
+    ends = np.unique(np.array([e for seq in seqs for (_, lo, hi) in seq for e in (lo, hi)],
+                              dtype=np.float64))
+    lo, hi = ends[:-1], ends[1:]
+    tot = np.zeros(lo.shape[0], dtype=np.int64)
+    cnt = np.zeros(lo.shape[0], dtype=np.int64)
+    for seq in seqs:
+        if not seq:
+            continue
+        t0 = np.array([t for (t, _, _) in seq], dtype=np.int64)
+        a = np.array([x for (_, x, _) in seq], dtype=np.float64)
+        b = np.array([x for (_, _, x) in seq], dtype=np.float64)
+        # the last interval of the sequence starting at or below lo is the only
+        # one that can contain the piece
+        j = np.searchsorted(a, lo, side="right") - 1
+        jj = np.maximum(j, 0)
+        inside = (j >= 0) & (lo < b[jj])
+        tot += np.where(inside, t0[jj], 0)
+        cnt += inside
+    keep = cnt > 0
+    return [(float(l), float(h), int(t), int(c))
+            for l, h, t, c in zip(lo[keep], hi[keep], tot[keep], cnt[keep])]
 
 
 def mkc_theta(pieces, k):
