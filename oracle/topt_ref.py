@@ -38,6 +38,12 @@ reason in the design notes of the repository):
 * c17 MKC: theta_r(k) = sup{theta : k_bar_r(theta) >= k} (App. D leaves the
       inverse of a fractional, not always monotone k_bar open); Eq. 8 averages
       only over the intervals that contain theta, as printed.
+* c18 offline-calibrated E~ (estimator 1 of §3.2.1) is the mean, over the
+      calibration rows of a row id, of the exact discarded sum E of each row
+      under the inference thresholds, in the max-shifted units of reading c8;
+      rows with theta = -inf get 0; row ids without samples take the nearest
+      sampled one (reading c5), none at all 0.  At inference it is used as
+      it is, whatever the row itself keeps.
 """
 from __future__ import annotations
 
@@ -46,7 +52,7 @@ import math
 import numpy as np
 
 PRE, POST = 0, 1
-SDC_NONE, SDC_EXACT, SDC_EXPTH = 0, 1, 2
+SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
 GAMMA = 0.05          # [TopTheta §3.2.1, exp-threshold estimator]
 BAND_REL = 1e-3       # decisions within this relative distance of theta are not compared
 
@@ -160,6 +166,60 @@ def calibrate_ref(Qc, Kc, row_len, k, mode, alpha, Lmax):
     """Algorithm 1 for one layer: returns (theta [Hq][Lmax], sets)."""
     sets = collect_thresholds(Qc, Kc, row_len, k, mode)
     return finalize_thresholds(sets, Qc.shape[1], Lmax, k, alpha), sets
+
+
+# ---------------------------------------------------------------------------
+# §3.2.1 estimator 1: offline-calibrated discarded sum E~.
+# ---------------------------------------------------------------------------
+def discarded_sum(a, theta):
+    """E of one pre-softmax row under theta: the exponent sum of the keys that
+    are not kept, in the units of Eq. 4 (row maximum subtracted, reading c8)."""
+    a = np.asarray(a, dtype=np.float64)
+    m = float(np.max(a))
+    return float(np.exp(a[a < theta] - m).sum())
+
+
+def collect_discarded(Qc, Kc, row_len, theta, sets=None):
+    """Observed E of every calibration row under the (pre-softmax) threshold
+    table theta [Hq][Lmax], keyed by (head, L); rows whose threshold is -inf
+    keep everything and give no sample.  Indexing as in ``collect_thresholds``."""
+    Qc = np.asarray(Qc, dtype=np.float64)
+    Kc = np.asarray(Kc, dtype=np.float64)
+    N, Hq, R, _ = Qc.shape
+    g = Hq // Kc.shape[1]
+    if sets is None:
+        sets = {}
+    for n in range(N):
+        for h in range(Hq):
+            for i in range(R):
+                L = int(row_len[i])
+                th = theta_for_row(theta[h], L)
+                if not np.isfinite(th):
+                    continue
+                a = row_scores(Qc[n, h, i], Kc[n, h // g], L)
+                sets.setdefault((h, L), []).append(discarded_sum(a, th))
+    return sets
+
+
+def finalize_discarded(sets, theta):
+    """E~ [Hq][Lmax]: the mean of each sampled row id, the nearest sampled row
+    id elsewhere (reading c5), 0 where theta is -inf or nothing was sampled
+    (reading c18)."""
+    Hq, Lmax = theta.shape
+    et = np.zeros((Hq, Lmax))
+    for h in range(Hq):
+        value = {L: float(np.mean(v)) for (hh, L), v in sets.items() if hh == h and L <= Lmax}
+        row = fill_row_ids(value, Lmax, 0)
+        row[~np.isfinite(row)] = 0.0
+        row[~np.isfinite(theta[h])] = 0.0
+        et[h] = row
+    return et
+
+
+def calibrate_discarded_ref(Qc, Kc, row_len, theta):
+    """Offline E~ table beside a pre-softmax theta table: (E~ [Hq][Lmax], sets)."""
+    sets = collect_discarded(Qc, Kc, row_len, theta)
+    return finalize_discarded(sets, np.asarray(theta, dtype=np.float64)), sets
 
 
 # ---------------------------------------------------------------------------
@@ -285,7 +345,7 @@ def theta_for_row(theta_row, L):
 # Inference on one attention row: threshold, SDC, VMC.
 # ---------------------------------------------------------------------------
 def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
-               gamma=GAMMA, decide=None):
+               gamma=GAMMA, decide=None, e_tilde=0.0):
     """Top-theta attention of one row.
 
     a      scores of the L visible keys (Eq. 1)
@@ -293,6 +353,7 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     theta  the row's calibrated threshold (pre: on a, post: on s)
     decide optional bool [L]; inside the band |x - theta| <= 1e-3 |theta| the
            oracle adopts these decisions instead of its own.
+    e_tilde the row's offline-calibrated estimate (SDC_OFFLINE, reading c18)
 
     Returns a dict with out [d], keep [L], kept (k~), band [L], m, Z, R, E, beta.
     """
@@ -325,6 +386,8 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     else:
         if sdc == SDC_EXACT:                # [TopTheta §3.2.1, estimator 3]
             E_est = E
+        elif sdc == SDC_OFFLINE:            # [TopTheta §3.2.1, estimator 1], reading c18
+            E_est = float(e_tilde)
         else:                               # [TopTheta §3.2.1, estimator 2], reading c8
             E_est = gamma * (L - kt) * math.exp(theta - m) if L > kt else 0.0
         # Eq. 4: softmax(a~)_i * R/(R + E~) = e_i / (R + E~)
@@ -356,11 +419,12 @@ def vmean_update_ref(mu, n_old, new_rows):
 # Decode and prefill drivers (loops over rows, heads and batches).
 # ---------------------------------------------------------------------------
 def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
-               mu=None, gamma=GAMMA, decide=None, heads=None):
+               mu=None, gamma=GAMMA, decide=None, heads=None, e_tilde=None):
     """One generated token per sequence ([TopTheta §2.2, generative decoding]).
 
     q [B][Hq][d]; Kc, Vc [B][Hkv][Nmax][d]; seq_len [B] (keys incl. the current
-    token); theta [Hq][Lmax]; mu [B][Hkv][d] (when vmc).  ``decide`` is an
+    token); theta [Hq][Lmax]; mu [B][Hkv][d] (when vmc); e_tilde [Hq][Lmax]
+    (SDC_OFFLINE, looked up like theta).  ``decide`` is an
     optional bool [B][Hq][Nmax] of decisions adopted inside the band.
     ``heads`` optionally restricts the work to a list of (b, h) pairs.
 
@@ -379,8 +443,9 @@ def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
         a = row_scores(q[b, h], Kc[b, kv], L)
         th = theta_for_row(theta[h], L)
         dec = None if decide is None else decide[b, h, :L]
+        et = 0.0 if e_tilde is None else theta_for_row(e_tilde[h], L)
         res[(b, h)] = attend_row(a, Vc[b, kv, :L], th, mode, sdc, vmc,
-                                 None if mu is None else mu[b, kv], gamma, dec)
+                                 None if mu is None else mu[b, kv], gamma, dec, et)
     union = {}
     for (b, h), r in res.items():
         key = (b, h // g)
@@ -391,12 +456,13 @@ def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
 
 
 def prefill_ref(Q, K, V, theta, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA,
-                decide=None, rows=None):
+                decide=None, rows=None, e_tilde=None):
     """Causal prefill ([TopTheta §2.2, prefill phase]); row i sees keys 0..i.
 
     Q [B][Hq][S][d]; K, V [B][Hkv][S][d]; theta [Hq][Lmax].  mu for row i is
     the mean of V rows 0..i (reading c11).  ``rows`` optionally restricts the
-    work to a list of (b, h, i).  Returns a dict keyed by (b, h, i).
+    work to a list of (b, h, i).  e_tilde [Hq][Lmax] as in ``decode_ref``.
+    Returns a dict keyed by (b, h, i).
     """
     B, Hq, S, _ = Q.shape
     Hkv = K.shape[1]
@@ -411,8 +477,9 @@ def prefill_ref(Q, K, V, theta, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA,
         th = theta_for_row(theta[h], L)
         mu = vmean_ref(V[b, kv, :L]) if vmc else None
         dec = None if decide is None else decide[b, h, i, :L]
+        et = 0.0 if e_tilde is None else theta_for_row(e_tilde[h], L)
         res[(b, h, i)] = attend_row(a, V[b, kv, :L], th, mode, sdc, vmc, mu,
-                                    gamma, dec)
+                                    gamma, dec, et)
     return res
 
 

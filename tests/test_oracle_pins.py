@@ -308,6 +308,70 @@ def test_output_error_metric():
 
 
 # ---------------------------------------------------------------------------
+# Offline-calibrated SDC (§3.2.1 estimator 1) by hand and by identities.
+# ---------------------------------------------------------------------------
+def check_golden_offline_sdc(golden_dir):
+    g = _load(golden_dir, "sdc_offline_two_samples.json")
+    d, k, L, Lmax = g["d"], g["k"], g["L"], g["Lmax"]
+    S = g["sample_scores"]
+    Qc = np.zeros((len(S), 1, 1, d))
+    Kc = np.zeros((len(S), 1, L, d))
+    for n in range(len(S)):
+        Qc[n, 0, 0] = g["q"]
+        Kc[n, 0, :, 0] = S[n]
+    theta, _ = ref.calibrate_ref(Qc, Kc, [L], k, ref.PRE, 0.0, Lmax)
+    et, sets = ref.calibrate_discarded_ref(Qc, Kc, [L], theta)
+    assert len(sets[(0, L)]) == len(S)
+    np.testing.assert_allclose(et[0], g["e_tilde"], rtol=1e-14, atol=1e-15)
+    a = ref.row_scores(Qc[0, 0, 0], Kc[0, 0], L)
+    r = ref.attend_row(a, np.eye(L), ref.theta_for_row(theta[0], L), ref.PRE, ref.SDC_OFFLINE,
+                       e_tilde=ref.theta_for_row(et[0], L))
+    np.testing.assert_allclose(r["out"], g["row1_out"], rtol=1e-14, atol=1e-15)
+    assert abs(r["beta"] - g["row1_beta"]) < 1e-14
+
+
+def test_golden_offline_sdc(golden_dir):
+    check_golden_offline_sdc(golden_dir)
+
+
+def test_offline_sdc_identities():
+    """E~ = the row's own E is exact SDC; E~ = 0 is plain pre-softmax."""
+    rng = np.random.default_rng(8)
+    for _ in range(200):
+        L = int(rng.integers(2, 20))
+        a = rng.normal(size=L) * 2
+        V = rng.normal(size=(L, 5))
+        mu = V.mean(axis=0)
+        th = float(np.sort(a)[rng.integers(0, L)])
+        ex = ref.attend_row(a, V, th, ref.PRE, ref.SDC_EXACT, True, mu)
+        off = ref.attend_row(a, V, th, ref.PRE, ref.SDC_OFFLINE, True, mu, e_tilde=ex["E"])
+        np.testing.assert_allclose(off["out"], ex["out"], rtol=1e-13, atol=1e-15)
+        assert abs(off["beta"] - ex["beta"]) < 1e-13
+        none = ref.attend_row(a, V, th, ref.PRE, ref.SDC_NONE, True, mu)
+        zero = ref.attend_row(a, V, th, ref.PRE, ref.SDC_OFFLINE, True, mu, e_tilde=0.0)
+        np.testing.assert_allclose(zero["out"], none["out"], rtol=1e-13, atol=1e-15)
+        assert none["beta"] == 0.0 and abs(zero["beta"]) < 1e-13
+
+
+def test_offline_sdc_one_row_calibration_is_exact_on_that_row():
+    """E~ calibrated on one decode row, applied to the same row, reproduces
+    exact SDC: the only sample is that row's own E."""
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        L, d = int(rng.integers(4, 30)), 8
+        k = int(rng.integers(1, L))
+        Kc = rng.normal(size=(1, 1, L, d))
+        q = rng.normal(size=(1, 1, d)) * 2
+        V = rng.normal(size=(1, 1, L, d))
+        theta, _ = ref.calibrate_ref(q[:, :, None, :], Kc, [L], k, ref.PRE, 0.0, L)
+        et, _ = ref.calibrate_discarded_ref(q[:, :, None, :], Kc, [L], theta)
+        ex, _ = ref.decode_ref(q, Kc, V, [L], theta, ref.PRE, ref.SDC_EXACT, True, V.mean(axis=2))
+        off, _ = ref.decode_ref(q, Kc, V, [L], theta, ref.PRE, ref.SDC_OFFLINE, True, V.mean(axis=2),
+                                e_tilde=et)
+        np.testing.assert_allclose(off[(0, 0)]["out"], ex[(0, 0)]["out"], rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
 # Multi-k cumulative calibration (App. D, Algorithm 2, Eq. 8).
 # ---------------------------------------------------------------------------
 def _mkc_inputs(rows, d=4):
@@ -478,6 +542,11 @@ def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
         return th
     _planted(monkeypatch, "finalize_thresholds", first_row,
              lambda: check_golden_nearest_row(golden_dir))
+
+    # offline E~ summed without subtracting the row maximum
+    _planted(monkeypatch, "discarded_sum",
+             lambda a, th: float(np.exp(np.asarray(a, float)[np.asarray(a, float) < th]).sum()),
+             lambda: check_golden_offline_sdc(golden_dir))
 
     # MKC: Eq. 8 averaged over all rows instead of the rows holding theta
     def merge_all_rows(seqs):
