@@ -58,11 +58,11 @@ NOMINAL_HBM_GBS = 8000.0
 # null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
-                  "source_sha256": "493ab46e4573be8a0fc8cc15c4a76447fb21a36d812d94aeb9e4dec0f110bf55",
-                  "bytes_per_launch": 268611072 + 13505792}   # decode_scores_kernel, one layer call
+                  "source_sha256": "6d2feadb355c09b0b466979e7b9c42f193a615d2070dfdd109cd8cc8dead5159",
+                  "bytes_per_launch": 268609792 + 13152256}   # decode_scores_kernel, one layer call
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "cb97c76275b0130056a5a5fc96f981626a4f10449d80b0e75ae92031b64498c0",
-                   "bytes_per_launch": 59533568 + 23594496}   # prefill_tc_kernel, post-softmax + VMC
+                   "source_sha256": "f0bd74c0af7559c1a0d66f264efb8004ccea2b5a967d0127d663594ba6fa74e6",
+                   "bytes_per_launch": 59525120 + 22531584}   # prefill_tc_kernel, post-softmax + VMC
 
 
 def parse():
@@ -648,6 +648,9 @@ def run_reference(args):
     if args.workload == "cfg3":
         run_reference_prefill(args, workloads.CFG3)
         return
+    if args.workload == "mkc":
+        run_reference_mkc(args, workloads.CFG3)
+        return
     wl = WORKLOADS[args.workload]
     layers_total = args.layers or wl.layers
     cores = host_cores()
@@ -952,6 +955,83 @@ class _CalInputs:
     inputs = PrefillState.inputs
 
 
+def host_mkc_sample(wl, heads=2):
+    """One KV group of the calibration sequences of `wl` on the host, float64."""
+    ch = synth.outlier_channels(synth.seed_of(wl.name, "channels"), wl.Hkv, wl.d)[:1]
+    gen = synth.generator(synth.seed_of(wl.name, "host", 7), "cpu")
+    Kc = synth.keys(gen, wl.n_cal, 1, wl.S, wl.d, ch)
+    Qc = synth.prefill_queries(gen, Kc, heads)
+    return synth.as_f64(Qc), synth.as_f64(Kc)
+
+
+def oracle_mkc_seconds(sample, groups, mode, cores):
+    """Wall-clock seconds of the oracle's Algorithm 2 on (head, row length)
+    groups: scores of the group's rows, interval sequences, MergeIntervals and
+    the inverse for every k of MKC_KS; returns (seconds, pooled scores)."""
+    import oracle.topt_ref as ref
+    Q, K = sample
+
+    def one(group):
+        h, L = group
+        rows = []
+        for n in range(Q.shape[0]):
+            a = ref.row_scores(Q[n, h, L - 1], K[n, 0], L)
+            rows.append(a if mode == 0 else ref.row_softmax(a))
+        pieces = ref.merge_intervals([ref.mkc_interval_sequence(r) for r in rows])
+        return [ref.mkc_theta(pieces, k) for k in MKC_KS if L > k]
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(one, groups))
+    return time.perf_counter() - t0, sum(Q.shape[0] * L for _, L in groups)
+
+
+def mkc_groups_sample(wl, n, heads=2, seed=0):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(heads)), int(L)) for L in rng.integers(1, wl.S + 1, n)]
+
+
+def mkc_cpu_baseline(wl, seconds):
+    cores = host_cores()
+    sample = host_mkc_sample(wl)
+    done, spent, pooled = 0, 0.0, 0
+    while spent < seconds:
+        groups = mkc_groups_sample(wl, 2 * cores, seed=done)
+        dt, n = oracle_mkc_seconds(sample, groups, 0, cores)
+        spent += dt
+        pooled += n
+        done += len(groups)
+    return {"value": pooled / spent, "unit": "scores/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} (head, row length) groups, length uniform in 1..{wl.S}, "
+                      f"{wl.n_cal} rows each, pre-softmax, all {len(MKC_KS)} k; float64 numpy, "
+                      f"{cores} threads"}
+
+
+def run_reference_mkc(args, wl):
+    cores = host_cores()
+    sample = host_mkc_sample(wl)
+    per_step = 2 * cores
+    for i in range(args.warmup):
+        oracle_mkc_seconds(sample, mkc_groups_sample(wl, per_step, seed=i), 0, cores)
+    runs = [oracle_mkc_seconds(sample, mkc_groups_sample(wl, per_step, seed=args.warmup + i), 0, cores)
+            for i in range(args.steps)]
+    value = sum(r[1] for r in runs) / sum(r[0] for r in runs)
+    pooled = wl.n_cal * wl.Hq * wl.S * (wl.S + 1) // 2
+    line = {"impl": "reference",
+            "metric": "multi-k cumulative calibration: pooled calibration scores per second",
+            "value": value, "unit": "scores/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": pooled / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
+                       "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS)},
+            "cpu_baseline": {"value": value, "unit": "scores/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} (head, row length) groups per step, "
+                                       "float64 numpy oracle, pre-softmax"},
+            "e2e": {"value": value, "unit": "scores/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main_mkc(args, dev, rank, local, world):
     """--workload mkc: one layer of multi-k cumulative calibration (App. D,
     Algorithm 2) on the calibration shape of the LLaMA-3-8B prefill workload:
@@ -959,6 +1039,9 @@ def main_mkc(args, dev, rank, local, world):
     every k in MKC_KS come from one call.  value = pooled calibration scores
     (sequences x heads x causal elements) per second, pre-softmax."""
     wl = workloads.CFG3
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = mkc_cpu_baseline(wl, args.cpu_seconds)
     from calibrated_thresholding_gb300 import build
     build.build()
     topt.lib()
@@ -994,9 +1077,29 @@ def main_mkc(args, dev, rank, local, world):
         if int(status.item()) != 0:
             raise RuntimeError(f"topt_calibrate_multik status {int(status.item())}")
         res[name] = float(np.mean(ms))
+    # offline SDC estimate E~ beside the k = 64 pre-softmax table, same rows
+    ki64 = MKC_KS.index(64)
+    topt.calibrate_multik(Q, K, row_len, ks, 0, wl.S, theta=theta, status=status, workspace=ws)
+    th64 = theta[ki64].clone()
+    sdc_cal = topt.SdcCalibrator(th64, device=dev)
+    sdc_ws = ws[:1 << 30]
+    for _ in range(args.warmup):
+        sdc_cal.add(Q, K, row_len, reset=True, workspace=sdc_ws)
+        sdc_cal.finalize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        sdc_cal.add(Q, K, row_len, reset=True, workspace=sdc_ws)
+        sdc_cal.finalize()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    sdc_ms = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]))
     clk = clocks.stop(t0, time.time())
     launches_pre = 1 + passes * 2 + 1
     launches_post = launches_pre + passes
+    rows_total = wl.n_cal * wl.Hq * wl.S
+    sdc_passes = -(-rows_total // min((1 << 30) // (wl.S * 4) // 8 * 8, 65535 * 8))
     line = {
         "metric": "multi-k cumulative calibration: pooled calibration scores per second",
         "value": pooled / (res["pre"] / 1e3), "unit": "scores/s", "n_gpus": 1, "steps": args.steps,
@@ -1008,9 +1111,13 @@ def main_mkc(args, dev, rank, local, world):
                    "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call"},
         "ms_per_call": res, "pooled_scores": pooled,
         "post_scores_per_s": pooled / (res["post"] / 1e3),
-        "gpu_launches": args.steps * (launches_pre + launches_post),
+        "sdc_offline_calibration": {"ms_per_call": sdc_ms, "table": "k = 64 pre-softmax theta",
+                                    "rows": rows_total, "scores_per_s": pooled / (sdc_ms / 1e3)},
+        "gpu_launches": args.steps * (launches_pre + launches_post + 2 * sdc_passes + 2),
         "clocks": clk,
     }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
 

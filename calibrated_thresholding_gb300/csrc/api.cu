@@ -17,7 +17,7 @@ topt_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TOPT_OK : TOP
 
 topt_status check_common_mode(int mode, int sdc) {
   if (mode != TOPT_PRE && mode != TOPT_POST) return TOPT_EINVAL;
-  if (sdc < TOPT_SDC_NONE || sdc > TOPT_SDC_EXPTH) return TOPT_EINVAL;
+  if (sdc < TOPT_SDC_NONE || sdc > TOPT_SDC_OFFLINE) return TOPT_EINVAL;
   return TOPT_OK;
 }
 
@@ -112,6 +112,7 @@ topt_status topt_decode(const topt_decode_args* a, topt_stream stream) {
   if (a->vmc && !a->mu) return TOPT_EINVAL;
   if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache)) return TOPT_EINVAL;
   if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
+  if (a->mode == TOPT_PRE && a->sdc == TOPT_SDC_OFFLINE && !a->e_tilde) return TOPT_EINVAL;
   const size_t need = decode_workspace_bytes(*a);
   if (!a->workspace || a->workspace_bytes < need || (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
     return TOPT_EWORKSPACE;
@@ -125,6 +126,7 @@ topt_status topt_decode_noalloc(const topt_decode_args* a, topt_stream stream) {
   if (a->vmc && !a->mu) return TOPT_EINVAL;
   if (!aligned16(a->q) || !aligned16(a->k_cache) || !aligned16(a->v_cache)) return TOPT_EINVAL;
   if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
+  if (a->mode == TOPT_PRE && a->sdc == TOPT_SDC_OFFLINE && !a->e_tilde) return TOPT_EINVAL;
   if (decode_workspace_bytes(*a) > decode_noalloc_capacity()) return TOPT_EWORKSPACE;
   return cuda_status(decode_noalloc_launch(*a, (cudaStream_t)stream));
 }
@@ -153,6 +155,7 @@ topt_status topt_prefill(const topt_prefill_args* a, topt_stream stream) {
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
     return TOPT_EINVAL;
   if (a->sdc == TOPT_SDC_EXPTH && !(a->gamma >= 0.f && std::isfinite(a->gamma))) return TOPT_EINVAL;
+  if (a->mode == TOPT_PRE && a->sdc == TOPT_SDC_OFFLINE && !a->e_tilde) return TOPT_EINVAL;
   const size_t need = prefill_workspace_bytes(*a);
   if (need > 0 && (!a->workspace || a->workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(a->workspace) & 255u)))
@@ -165,6 +168,7 @@ topt_status topt_prefill_test_timeout(const topt_prefill_args* a, topt_stream st
   if (st != TOPT_OK) return st;
   if (a->dtype != TOPT_BF16 || !a->status) return TOPT_EINVAL;
   if (!a->q || !a->k || !a->v || !a->theta || !a->out) return TOPT_EINVAL;
+  if (a->mode == TOPT_PRE && a->sdc == TOPT_SDC_OFFLINE && !a->e_tilde) return TOPT_EINVAL;
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out))
     return TOPT_EINVAL;
   const size_t need = prefill_workspace_bytes(*a);
@@ -200,6 +204,44 @@ topt_status topt_calibrate(const topt_calib_args* a, topt_stream stream) {
     if (!a->workspace || a->workspace_bytes < minimum) return TOPT_EWORKSPACE;
   }
   return cuda_status(calibrate_launch(*a, (cudaStream_t)stream));
+}
+
+static topt_status check_sdc_calib_shape(const topt_sdc_calib_args* a) {
+  if (!a) return TOPT_EINVAL;
+  if (a->n_seqs < 0 || a->n_q_heads < 1 || a->n_kv_heads < 1 || a->theta_len < 1) return TOPT_ESHAPE;
+  if (a->n_seqs > 0 && (a->n_rows < 1 || a->n_keys < 1)) return TOPT_ESHAPE;
+  if (!dim_ok(a->head_dim)) return TOPT_ESHAPE;
+  if (a->n_q_heads % a->n_kv_heads != 0) return TOPT_ESHAPE;
+  if (a->dtype != TOPT_BF16 && a->dtype != TOPT_F32) return TOPT_EDTYPE;
+  if (a->flags & ~(TOPT_CALIB_RESET | TOPT_CALIB_FINALIZE)) return TOPT_EINVAL;
+  return TOPT_OK;
+}
+
+topt_status topt_calibrate_sdc_workspace(const topt_sdc_calib_args* a, size_t* bytes) {
+  topt_status st = check_sdc_calib_shape(a);
+  if (st != TOPT_OK) return st;
+  if (!bytes) return TOPT_EINVAL;
+  const size_t rows = (size_t)a->n_seqs * a->n_q_heads * a->n_rows;
+  size_t want = calibrate_sdc_workspace_bytes(*a, rows > 0 ? rows : 1);
+  const size_t cap = (size_t)1 << 30;
+  const size_t minimum = calibrate_sdc_workspace_bytes(*a, calibrate_min_rows_per_pass());
+  if (want > cap) want = cap > minimum ? cap : minimum;
+  *bytes = want;
+  return TOPT_OK;
+}
+
+topt_status topt_calibrate_sdc(const topt_sdc_calib_args* a, topt_stream stream) {
+  topt_status st = check_sdc_calib_shape(a);
+  if (st != TOPT_OK) return st;
+  if (!a->acc || !a->count || !a->theta) return TOPT_EINVAL;
+  if ((a->flags & TOPT_CALIB_FINALIZE) && !a->e_tilde) return TOPT_EINVAL;
+  if (a->n_seqs > 0) {
+    if (!a->q || !a->keys || !a->row_len) return TOPT_EINVAL;
+    if (!aligned16(a->q) || !aligned16(a->keys)) return TOPT_EINVAL;
+    const size_t minimum = calibrate_sdc_workspace_bytes(*a, calibrate_min_rows_per_pass());
+    if (!a->workspace || a->workspace_bytes < minimum) return TOPT_EWORKSPACE;
+  }
+  return cuda_status(calibrate_sdc_launch(*a, (cudaStream_t)stream));
 }
 
 topt_status topt_calibrate_multik_workspace(const topt_mkc_args* a, size_t* bytes) {

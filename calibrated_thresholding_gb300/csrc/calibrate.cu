@@ -345,13 +345,73 @@ __global__ void __launch_bounds__(kFinThreads) calib_finalize_kernel(const Calib
   fill_nearest_rows(p.Lmax, p.k, has, val, p.theta + (size_t)h * p.Lmax);
 }
 
-template <typename T, int D>
+// ---------------------------------------------------------------------------
+// Offline-calibrated SDC estimate [TopTheta §3.2.1, estimator 1]: the mean,
+// per (head, row id), of each calibration row's discarded exponent sum
+// E = sum_{a_j < theta} exp(a_j - m) under a pre-softmax threshold table.
+// The same score passes as Algorithm 1; acc holds one sum per cell.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSelThreads) calib_e_kernel(const CalibParams p, long it0,
+                                                              const float* __restrict__ ws) {
+  __shared__ SelectSmem sm;
+  const long it = it0 + blockIdx.x;
+  const long i = it % p.R;
+  const long h = (it / p.R) % p.Hq;
+  const int L = p.row_len[i];
+  if (L < 1 || L > p.Nk || L > p.Lmax) {
+    if (threadIdx.x == 0) set_status(p.status, TOPT_EINVAL);
+    return;
+  }
+  const float th = p.theta[(size_t)h * p.Lmax + (L - 1)];
+  if (!(th > -CUDART_INF_F)) return;  // the row is kept whole: no sample
+  const float* row = ws + (long)blockIdx.x * p.Nk;
+  float m = -CUDART_INF_F;
+  for (int j = threadIdx.x; j < L; j += kSelThreads) m = fmaxf(m, row[j]);
+  m = cta_reduce_max(m, sm);
+  float e = 0.f;
+  for (int j = threadIdx.x; j < L; j += kSelThreads) {
+    const float x = row[j];
+    if (x < th) e += expf(x - m);
+  }
+  e = cta_reduce_sum(e, sm);
+  if (threadIdx.x == 0) {
+    const size_t cell = (size_t)h * p.Lmax + (L - 1);
+    atomicAdd(p.acc + cell, (double)e);
+    atomicAdd(p.count + cell, 1);
+  }
+}
+
+__global__ void calib_e_zero_kernel(double* acc, int32_t* count, size_t cells) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < cells; i += (size_t)gridDim.x * blockDim.x) {
+    acc[i] = 0.0;
+    count[i] = 0;
+  }
+}
+
+// One CTA per head: sample means, nearest sampled row id elsewhere, 0 where
+// theta is -inf or the head has no sample.
+__global__ void __launch_bounds__(kFinThreads) calib_e_finalize_kernel(const CalibParams p, float* e_tilde) {
+  const int h = blockIdx.x;
+  const size_t off = (size_t)h * p.Lmax;
+  const float* th = p.theta + off;
+  const auto has = [&](int i) { return p.count[off + i] > 0 && th[i] > -CUDART_INF_F; };
+  const auto val = [&](int i) { return (float)(p.acc[off + i] / (double)p.count[off + i]); };
+  fill_nearest_rows(p.Lmax, 0, has, val, e_tilde + off);
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.Lmax; i += kFinThreads) {
+    const float v = e_tilde[off + i];
+    e_tilde[off + i] = (th[i] > -CUDART_INF_F && v > -CUDART_INF_F) ? v : 0.f;
+  }
+}
+
+template <typename T, int D, bool kSdc = false>
 cudaError_t calib_pass(const CalibParams& p, long it0, int nrows, float* ws, cudaStream_t s) {
   dim3 g1((p.Nk + kScoreKeys - 1) / kScoreKeys, (nrows + kScoreRows - 1) / kScoreRows);
   calib_scores_kernel<T, D><<<g1, kScoreKeys, 0, s>>>(p, it0, nrows, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  calib_select_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
+  if (kSdc) calib_e_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
+  else calib_select_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
   return cudaGetLastError();
 }
 
@@ -717,6 +777,64 @@ cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s) {
   }
   if (a.flags & TOPT_CALIB_FINALIZE) {
     calib_finalize_kernel<<<a.n_q_heads, kFinThreads, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+size_t calibrate_sdc_workspace_bytes(const topt_sdc_calib_args& a, size_t rows_per_pass) {
+  return align256(rows_per_pass * (size_t)a.n_keys * sizeof(float));
+}
+
+cudaError_t calibrate_sdc_launch(const topt_sdc_calib_args& a, cudaStream_t s) {
+  CalibParams p;
+  p.N = a.n_seqs;
+  p.Hq = a.n_q_heads;
+  p.Hkv = a.n_kv_heads;
+  p.R = a.n_rows;
+  p.Nk = a.n_keys;
+  p.Lmax = a.theta_len;
+  p.mode = TOPT_PRE;
+  p.k = 1;
+  p.h0 = 0;
+  p.Hp = a.n_q_heads;
+  p.alpha = 0.f;
+  p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
+  p.q = a.q;
+  p.keys = a.keys;
+  p.row_len = a.row_len;
+  p.acc = a.acc;
+  p.count = a.count;
+  p.theta = const_cast<float*>(a.theta);  // read only here
+  p.status = a.status;
+  const size_t cells = (size_t)a.n_q_heads * a.theta_len;
+  cudaError_t e;
+  if (a.flags & TOPT_CALIB_RESET) {
+    calib_e_zero_kernel<<<(unsigned)((cells + 255) / 256 < 4096 ? (cells + 255) / 256 : 4096), 256, 0, s>>>(
+        a.acc, a.count, cells);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const long total = (long)a.n_seqs * a.n_q_heads * a.n_rows;
+  if (total > 0) {
+    long rows_per_pass = (long)(a.workspace_bytes / ((size_t)a.n_keys * sizeof(float)));
+    rows_per_pass = rows_per_pass / kScoreRows * kScoreRows;
+    if (rows_per_pass > kMaxPassRows) rows_per_pass = kMaxPassRows;
+    if (rows_per_pass < kScoreRows) return cudaErrorInvalidValue;
+    float* ws = static_cast<float*>(a.workspace);
+    for (long it0 = 0; it0 < total; it0 += rows_per_pass) {
+      const int nrows = (int)((total - it0) < rows_per_pass ? (total - it0) : rows_per_pass);
+      if (a.dtype == TOPT_BF16) {
+        e = a.head_dim == 128 ? calib_pass<__nv_bfloat16, 128, true>(p, it0, nrows, ws, s)
+                              : calib_pass<__nv_bfloat16, 64, true>(p, it0, nrows, ws, s);
+      } else {
+        e = a.head_dim == 128 ? calib_pass<float, 128, true>(p, it0, nrows, ws, s)
+                              : calib_pass<float, 64, true>(p, it0, nrows, ws, s);
+      }
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (a.flags & TOPT_CALIB_FINALIZE) {
+    calib_e_finalize_kernel<<<a.n_q_heads, kFinThreads, 0, s>>>(p, a.e_tilde);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -141,11 +141,12 @@ __device__ __forceinline__ float score_bound(int mode, float theta, float m, flo
 }
 
 // Normalisation of one output row [TopTheta §3.2.1 Eq. 4, §3.2.2 Eq. 6-7].
-// num = sum_{kept} exp(a_j - m) v_j, R = sum_{kept} exp(a_j - m), Z = all.
+// num = sum_{kept} exp(a_j - m) v_j, R = sum_{kept} exp(a_j - m), Z = all;
+// e_off is the row's offline-calibrated E~ (TOPT_SDC_OFFLINE).
 // Writes scale (multiplies num) and beta (multiplies mu when VMC is on).
 __device__ __forceinline__ void out_scale_beta(int mode, int sdc, float gamma, float theta,
                                                float m, float Z, float R, int L, int kept,
-                                               float& scale, float& beta) {
+                                               float e_off, float& scale, float& beta) {
   if (mode == TOPT_POST) {
     scale = 1.f / Z;
     beta = 1.f - R / Z;
@@ -159,6 +160,8 @@ __device__ __forceinline__ void out_scale_beta(int mode, int sdc, float gamma, f
   float E;
   if (sdc == TOPT_SDC_EXACT) {
     E = fmaxf(Z - R, 0.f);
+  } else if (sdc == TOPT_SDC_OFFLINE) {
+    E = e_off;
   } else {
     E = (L > kept) ? gamma * (float)(L - kept) * __expf(theta - m) : 0.f;
   }

@@ -76,6 +76,7 @@ struct DecodeParams {
   const __nv_bfloat16* v;
   const int32_t* seq_len;
   const float* theta;
+  const float* e_tilde;  // offline E~ [Hq][Lmax] (pre-softmax, TOPT_SDC_OFFLINE)
   const float* mu;
   float* out;
   int32_t* kept;
@@ -678,7 +679,10 @@ __global__ void __launch_bounds__(kThreads, select_min_blocks<G>()) decode_selec
       ktot += __ldcg(p.part_kt + q * G + h);
     }
     float scl, beta;
-    out_scale_beta(p.mode, p.sdc, p.gamma, sm.th[h], sm.M[h], sm.Z[h], R, L, ktot, scl, beta);
+    const float e_off = (p.mode == TOPT_PRE && p.sdc == TOPT_SDC_OFFLINE)
+                            ? p.e_tilde[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)]
+                            : 0.f;
+    out_scale_beta(p.mode, p.sdc, p.gamma, sm.th[h], sm.M[h], sm.Z[h], R, L, ktot, e_off, scl, beta);
     float o = num * scl;
     if (p.vmc) o = fmaf(beta, p.mu[(size_t)pair * D + dd], o);
     const size_t row = (size_t)b * p.Hq + kvh * G + h;
@@ -853,6 +857,7 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.v = static_cast<const __nv_bfloat16*>(a.v_cache);
   p.seq_len = a.seq_len;
   p.theta = a.theta;
+  p.e_tilde = a.e_tilde;
   p.mu = a.mu;
   p.out = a.out;
   p.kept = a.kept;

@@ -36,6 +36,9 @@ cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax
 size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);
 size_t calibrate_min_rows_per_pass();
 cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s);
+// offline-calibrated SDC estimate E~, calibrated beside a pre-softmax theta
+size_t calibrate_sdc_workspace_bytes(const topt_sdc_calib_args& a, size_t rows_per_pass);
+cudaError_t calibrate_sdc_launch(const topt_sdc_calib_args& a, cudaStream_t s);
 // multi-k cumulative calibration: fixed workspace + one head's scores per head
 size_t calibrate_multik_fixed_bytes(const topt_mkc_args& a);
 size_t calibrate_multik_head_bytes(const topt_mkc_args& a);

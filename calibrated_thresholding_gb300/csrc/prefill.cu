@@ -32,6 +32,7 @@ struct PrefillParams {
   const void* k;
   const void* v;
   const float* theta;
+  const float* e_tilde;  // offline E~ [Hq][Lmax] (pre-softmax, TOPT_SDC_OFFLINE)
   float* out;
   int32_t* kept;
   uint32_t* mask;
@@ -192,7 +193,10 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillPar
   }
   if (row_ok) {
     float sc, beta;
-    out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, L, kt_cnt, sc, beta);
+    const float e_off = (p.mode == TOPT_PRE && p.sdc == TOPT_SDC_OFFLINE)
+                            ? p.e_tilde[(size_t)h * p.Lmax + (min(L, p.Lmax) - 1)]
+                            : 0.f;
+    out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, L, kt_cnt, e_off, sc, beta);
     const size_t orow = ((size_t)b * p.Hq + h) * p.S + i_row;
     const float* mu = p.vmc ? p.mu + (((size_t)b * p.Hkv + kvh) * p.S + i_row) * D : nullptr;
 #pragma unroll
@@ -282,6 +286,7 @@ cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s, int withh
   p.k = a.k;
   p.v = a.v;
   p.theta = a.theta;
+  p.e_tilde = a.e_tilde;
   p.out = a.out;
   p.kept = a.kept;
   p.mask = a.mask;

@@ -106,6 +106,7 @@ struct TcParams {
   int B, Hq, Hkv, S, Lmax, mode, sdc, vmc, mask_words, nqb;
   float gamma, sm_scale;
   const float* theta;
+  const float* e_tilde;  // offline E~ [Hq][Lmax] (pre-softmax, TOPT_SDC_OFFLINE)
   float* out;
   int32_t* kept;
   uint32_t* mask;
@@ -507,7 +508,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const bool have_o = *o_written != 0;
       float sc = 0.f, beta = 0.f;
-      if (row_ok) out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, Lrow, cnt, sc, beta);
+      if (row_ok) {
+        const float e_off = (p.mode == TOPT_PRE && p.sdc == TOPT_SDC_OFFLINE)
+                                ? p.e_tilde[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)]
+                                : 0.f;
+        out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, Lrow, cnt, e_off, sc, beta);
+      }
       const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
       constexpr int OC = D / kParts;  // output columns of this thread
       const int c0 = OC * part;
@@ -796,6 +802,7 @@ cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax
   p.gamma = a.gamma;
   p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
   p.theta = a.theta;
+  p.e_tilde = a.e_tilde;
   p.out = a.out;
   p.kept = a.kept;
   p.mask = a.mask;

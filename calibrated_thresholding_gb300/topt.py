@@ -16,7 +16,7 @@ import torch
 from . import build as _build
 
 PRE, POST = 0, 1
-SDC_NONE, SDC_EXACT, SDC_EXPTH = 0, 1, 2
+SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
 BF16, F32 = 0, 1
 CALIB_RESET, CALIB_FINALIZE = 1, 2
 GAMMA = 0.05
@@ -38,7 +38,7 @@ class DecodeArgs(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
                 ("cache_len", i32), ("theta_len", i32), ("mode", i32), ("sdc", i32), ("vmc", i32),
                 ("gamma", f32), ("q", vp), ("k_cache", vp), ("v_cache", vp), ("seq_len", vp),
-                ("theta", vp), ("mu", vp), ("out", vp), ("kept", vp), ("vrows", vp), ("mask", vp),
+                ("theta", vp), ("e_tilde", vp), ("mu", vp), ("out", vp), ("kept", vp), ("vrows", vp), ("mask", vp),
                 ("status", vp), ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 3)]
 
 
@@ -46,7 +46,7 @@ class PrefillArgs(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
                 ("seq", i32), ("theta_len", i32), ("dtype", i32), ("mode", i32), ("sdc", i32),
                 ("vmc", i32), ("gamma", f32), ("q", vp), ("k", vp), ("v", vp), ("theta", vp),
-                ("out", vp), ("kept", vp), ("mask", vp), ("tiles", vp), ("status", vp),
+                ("e_tilde", vp), ("out", vp), ("kept", vp), ("mask", vp), ("tiles", vp), ("status", vp),
                 ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 2)]
 
 
@@ -56,6 +56,14 @@ class CalibArgs(ctypes.Structure):
                 ("mode", i32), ("k", i32), ("alpha", f32), ("flags", i32), ("q", vp),
                 ("keys", vp), ("row_len", vp), ("acc", vp), ("count", vp), ("theta", vp),
                 ("status", vp), ("workspace", vp), ("workspace_bytes", sz)]
+
+
+class SdcCalibArgs(ctypes.Structure):
+    _fields_ = [("n_seqs", i32), ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
+                ("n_rows", i32), ("n_keys", i32), ("theta_len", i32), ("dtype", i32),
+                ("flags", i32), ("q", vp), ("keys", vp), ("row_len", vp), ("theta", vp),
+                ("acc", vp), ("count", vp), ("e_tilde", vp), ("status", vp), ("workspace", vp),
+                ("workspace_bytes", sz)]
 
 
 class MkcArgs(ctypes.Structure):
@@ -77,7 +85,8 @@ _lock = threading.Lock()
 
 SYMBOLS = ["topt_decode_workspace", "topt_decode", "topt_decode_noalloc", "topt_prefill_workspace",
            "topt_prefill_tile_shape", "topt_prefill", "topt_prefill_test_timeout", "topt_calibrate_workspace",
-           "topt_calibrate", "topt_calibrate_multik_workspace", "topt_calibrate_multik", "topt_select_kth", "topt_vmean_update", "topt_version",
+           "topt_calibrate", "topt_calibrate_sdc_workspace", "topt_calibrate_sdc",
+           "topt_calibrate_multik_workspace", "topt_calibrate_multik", "topt_select_kth", "topt_vmean_update", "topt_version",
            "topt_status_string"]
 
 
@@ -155,7 +164,7 @@ def _dtype_code(t):
 # ---------------------------------------------------------------------------
 def decode_args(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
                 gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-                workspace=None):
+                workspace=None, e_tilde=None):
     B, Hq, d = q.shape
     _, Hkv, Nmax, _ = k_cache.shape
     a = DecodeArgs()
@@ -167,6 +176,7 @@ def decode_args(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=
     a.v_cache = _ptr(_dev(v_cache, "v_cache", torch.bfloat16))
     a.seq_len = _ptr(_dev(seq_len, "seq_len", torch.int32))
     a.theta = _ptr(_dev(theta, "theta", torch.float32))
+    a.e_tilde = _ptr(_dev(e_tilde, "e_tilde", torch.float32))
     a.mu = _ptr(_dev(mu, "mu", torch.float32))
     a.out = _ptr(_dev(out, "out", torch.float32))
     a.kept = _ptr(_dev(kept, "kept", torch.int32))
@@ -192,7 +202,7 @@ def decode_workspace(a: DecodeArgs, device) -> torch.Tensor:
 
 def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
            gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-           workspace=None, stream=None):
+           workspace=None, stream=None, e_tilde=None):
     """Top-theta decode through ``topt_decode``; see include/topt.h for shapes.
 
     Allocates (with torch) the outputs and the workspace that are not given.
@@ -208,7 +218,8 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
     if vrows is None:
         vrows = torch.empty((B, Hkv), device=dev, dtype=torch.int32)
     a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
-                    gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status)
+                    gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status,
+                    e_tilde=e_tilde)
     if workspace is None:
         workspace = decode_workspace(a, dev)
     a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
@@ -219,7 +230,7 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
 
 def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
                    gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-                   stream=None):
+                   stream=None, e_tilde=None):
     """Top-theta decode through ``topt_decode_noalloc`` (library-held scratch).
 
     For callers that must not allocate device scratch; see include/topt.h for
@@ -236,7 +247,8 @@ def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, v
     if vrows is None:
         vrows = torch.empty((B, Hkv), device=dev, dtype=torch.int32)
     a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
-                    gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status)
+                    gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status,
+                    e_tilde=e_tilde)
     _check("topt_decode_noalloc", lib().topt_decode_noalloc(ctypes.byref(a), _stream(stream)))
     return dict(out=out, kept=kept, vrows=vrows, mask=mask)
 
@@ -245,7 +257,7 @@ def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, v
 # prefill
 # ---------------------------------------------------------------------------
 def prefill_args(q, k, v, theta, *, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA, out=None,
-                 kept=None, mask=None, tiles=None, status=None):
+                 kept=None, mask=None, tiles=None, status=None, e_tilde=None):
     B, Hq, S, d = q.shape
     Hkv = k.shape[1]
     if k.dtype != q.dtype or v.dtype != q.dtype:
@@ -256,6 +268,7 @@ def prefill_args(q, k, v, theta, *, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA, 
     a.mode, a.sdc, a.vmc, a.gamma = int(mode), int(sdc), int(bool(vmc)), float(gamma)
     a.q, a.k, a.v = _ptr(_dev(q, "q")), _ptr(_dev(k, "k")), _ptr(_dev(v, "v"))
     a.theta = _ptr(_dev(theta, "theta", torch.float32))
+    a.e_tilde = _ptr(_dev(e_tilde, "e_tilde", torch.float32))
     a.out = _ptr(_dev(out, "out", torch.float32))
     a.kept = _ptr(_dev(kept, "kept", torch.int32))
     a.mask = _ptr(_dev(mask, "mask", torch.int32))
@@ -278,7 +291,7 @@ def prefill_tile_shape(a: PrefillArgs):
 
 
 def prefill(q, k, v, theta, *, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA, out=None, kept=None,
-            mask=None, tiles=None, status=None, workspace=None, stream=None):
+            mask=None, tiles=None, status=None, workspace=None, stream=None, e_tilde=None):
     """Causal Top-theta prefill through ``topt_prefill``."""
     B, Hq, S, d = q.shape
     dev = q.device
@@ -287,7 +300,7 @@ def prefill(q, k, v, theta, *, mode, sdc=SDC_NONE, vmc=False, gamma=GAMMA, out=N
     if kept is None:
         kept = torch.empty((B, Hq, S), device=dev, dtype=torch.int32)
     a = prefill_args(q, k, v, theta, mode=mode, sdc=sdc, vmc=vmc, gamma=gamma, out=out, kept=kept,
-                     mask=mask, tiles=tiles, status=status)
+                     mask=mask, tiles=tiles, status=status, e_tilde=e_tilde)
     need = prefill_workspace_bytes(a)
     if workspace is None and need > 0:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
@@ -346,6 +359,54 @@ class Calibrator:
         a = self._args(None, None, None, CALIB_FINALIZE, status)
         _check("topt_calibrate", lib().topt_calibrate(ctypes.byref(a), _stream(stream)))
         return self.theta
+
+
+class SdcCalibrator:
+    """Offline E~ of one layer beside a pre-softmax theta [TopTheta §3.2.1, estimator 1].
+
+    ``add`` runs topt_calibrate_sdc on a batch of calibration sequences;
+    ``finalize`` writes and returns E~ [Hq][Lmax] (pass it as ``e_tilde``
+    with ``sdc=SDC_OFFLINE``).
+    """
+
+    def __init__(self, theta, device="cuda"):
+        self.theta = _dev(theta, "theta", torch.float32)
+        self.Hq, self.Lmax = theta.shape
+        self.acc = torch.zeros((self.Hq, self.Lmax), device=device, dtype=torch.float64)
+        self.count = torch.zeros((self.Hq, self.Lmax), device=device, dtype=torch.int32)
+        self.e_tilde = torch.empty((self.Hq, self.Lmax), device=device, dtype=torch.float32)
+
+    def _args(self, q, keys, row_len, flags, status):
+        a = SdcCalibArgs()
+        a.n_q_heads, a.theta_len, a.flags = self.Hq, self.Lmax, int(flags)
+        a.theta, a.acc, a.count = _ptr(self.theta), _ptr(self.acc), _ptr(self.count)
+        a.e_tilde = _ptr(self.e_tilde)
+        a.status = _ptr(_dev(status, "status", torch.int32))
+        if q is None:
+            a.n_seqs, a.n_kv_heads, a.head_dim, a.dtype = 0, self.Hq, 128, BF16
+            return a
+        N, Hq, R, d = q.shape
+        a.n_seqs, a.n_kv_heads, a.head_dim, a.n_rows, a.n_keys = N, keys.shape[1], d, R, keys.shape[2]
+        a.dtype = _dtype_code(q)
+        a.q, a.keys = _ptr(_dev(q, "q")), _ptr(_dev(keys, "keys"))
+        a.row_len = _ptr(_dev(row_len, "row_len", torch.int32))
+        return a
+
+    def add(self, q, keys, row_len, reset=False, status=None, workspace=None, stream=None):
+        a = self._args(q, keys, row_len, CALIB_RESET if reset else 0, status)
+        if workspace is None:
+            n = sz(0)
+            _check("topt_calibrate_sdc_workspace",
+                   lib().topt_calibrate_sdc_workspace(ctypes.byref(a), ctypes.byref(n)))
+            workspace = torch.empty(n.value, device=q.device, dtype=torch.uint8)
+        a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
+        a.workspace_bytes = workspace.numel()
+        _check("topt_calibrate_sdc", lib().topt_calibrate_sdc(ctypes.byref(a), _stream(stream)))
+
+    def finalize(self, status=None, stream=None):
+        a = self._args(None, None, None, CALIB_FINALIZE, status)
+        _check("topt_calibrate_sdc", lib().topt_calibrate_sdc(ctypes.byref(a), _stream(stream)))
+        return self.e_tilde
 
 
 def calibrate_multik(q, keys, row_len, ks, mode, theta_len, theta=None, status=None,

@@ -56,10 +56,19 @@ typedef enum {
 typedef enum { TOPT_PRE = 0, TOPT_POST = 1 } topt_mode;
 
 /* Estimators of the discarded exponent sum E~ [TopTheta §3.2.1]:
- *   EXACT  E~ = sum over discarded keys of exp(a_j - m)
- *   EXPTH  E~ = gamma * (L - k~) * exp(theta - m)   (gamma: 0.05 in the paper)
- * SDC applies to pre-softmax only; post-softmax ignores the field. */
-typedef enum { TOPT_SDC_NONE = 0, TOPT_SDC_EXACT = 1, TOPT_SDC_EXPTH = 2 } topt_sdc;
+ *   EXACT    E~ = sum over discarded keys of exp(a_j - m)
+ *   EXPTH    E~ = gamma * (L - k~) * exp(theta - m)   (gamma: 0.05 in the paper)
+ *   OFFLINE  E~ = e_tilde[h][L-1], a static table calibrated beside theta by
+ *            topt_calibrate_sdc (looked up like theta); used as it is,
+ *            whatever the row itself keeps
+ * m is the row maximum.  SDC applies to pre-softmax only; post-softmax ignores
+ * the field. */
+typedef enum {
+  TOPT_SDC_NONE = 0,
+  TOPT_SDC_EXACT = 1,
+  TOPT_SDC_EXPTH = 2,
+  TOPT_SDC_OFFLINE = 3
+} topt_sdc;
 
 typedef enum { TOPT_BF16 = 0, TOPT_F32 = 1 } topt_dtype;
 
@@ -83,6 +92,8 @@ typedef struct {
   const void* v_cache;  /* [B][Hkv][Nmax][d] bf16 */
   const int32_t* seq_len; /* [B] keys per sequence incl. the current token, 1..Nmax */
   const float* theta;   /* [Hq][Lmax] fp32, the layer's slice of the table */
+  const float* e_tilde; /* [Hq][Lmax] fp32 offline E~; required for TOPT_SDC_OFFLINE
+                           with TOPT_PRE, else ignored (may be NULL) */
   const float* mu;      /* [B][Hkv][d] fp32 mean V row; required when vmc != 0 */
   float* out;           /* [B][Hq][d] fp32 */
   int32_t* kept;        /* [B][Hq] k~ per head, or NULL */
@@ -148,6 +159,7 @@ typedef struct {
   const void* k;        /* [B][Hkv][S][d] */
   const void* v;        /* [B][Hkv][S][d] */
   const float* theta;   /* [Hq][Lmax] */
+  const float* e_tilde; /* [Hq][Lmax] offline E~ (TOPT_SDC_OFFLINE with TOPT_PRE), else NULL */
   float* out;           /* [B][Hq][S][d] fp32, 16-byte aligned; VMC uses the prefix mean of
                            V rows 0..i.  q, k, v are 16-byte aligned too. */
   int32_t* kept;        /* [B][Hq][S] k~ per row, or NULL */
@@ -219,6 +231,45 @@ topt_status topt_calibrate_workspace(const topt_calib_args* args, size_t* bytes)
  *   otherwise         the value of the nearest calibrated L (ties: smaller L);
  *                     -INFINITY if the head has no calibrated row.          */
 topt_status topt_calibrate(const topt_calib_args* args, topt_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Offline-calibrated SDC [TopTheta §3.2.1, estimator 1], one layer per      */
+/* call: a static E~ per (head, row) calibrated beside a pre-softmax theta.  */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t n_seqs;       /* N >= 0 calibration sequences in this call */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t n_rows;       /* R query rows per sequence */
+  int32_t n_keys;       /* Nk keys per sequence */
+  int32_t theta_len;    /* Lmax */
+  int32_t dtype;        /* topt_dtype of q and keys */
+  int32_t flags;        /* TOPT_CALIB_RESET / TOPT_CALIB_FINALIZE, as topt_calibrate */
+  const void* q;        /* [N][Hq][R][d] */
+  const void* keys;     /* [N][Hkv][Nk][d] */
+  const int32_t* row_len; /* [R] keys seen by each query row, 1..min(Nk, Lmax) */
+  const float* theta;   /* [Hq][Lmax] pre-softmax thresholds the table is for (input) */
+  double* acc;          /* [Hq][Lmax] running sum of E samples */
+  int32_t* count;       /* [Hq][Lmax] number of samples */
+  float* e_tilde;       /* [Hq][Lmax] written on FINALIZE */
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+} topt_sdc_calib_args;
+
+/* Same workspace rule as topt_calibrate_workspace. */
+topt_status topt_calibrate_sdc_workspace(const topt_sdc_calib_args* args, size_t* bytes);
+
+/* For every sequence, head h and row i with L = row_len[i] and a finite
+ * theta[h][L-1]: adds E = sum over keys j < L with a_j < theta of
+ * exp(a_j - m) (m the row maximum) to the accumulators at [h][L-1].
+ * FINALIZE then writes, per head and L:
+ *   theta = -INFINITY  0 (the row is kept whole)
+ *   count > 0          the mean of the samples
+ *   otherwise          the mean of the nearest sampled L (ties: smaller L);
+ *                      0 if the head has no sample. */
+topt_status topt_calibrate_sdc(const topt_sdc_calib_args* args, topt_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Multi-k cumulative calibration (MKC) [TopTheta App. D, Algorithm 2,      */

@@ -23,7 +23,7 @@ def unpack_mask(words, L):
 
 
 def check_decode(q, Kc, Vc, seq_len, theta, mode, sdc, vmc, mu, res, gamma=ref.GAMMA, heads=None,
-                 out_tol=OUT_TOL):
+                 out_tol=OUT_TOL, e_tilde=None):
     """Compare topt.decode results (dict of tensors incl. mask) with decode_ref.
 
     Returns (n_rows_checked, n_band_elements, max_rel_err).
@@ -34,6 +34,7 @@ def check_decode(q, Kc, Vc, seq_len, theta, mode, sdc, vmc, mu, res, gamma=ref.G
     g = Hq // Hkv
     sl = seq_len.cpu().numpy()
     th = theta.cpu().double().numpy()
+    et = None if e_tilde is None else e_tilde.cpu().double().numpy()
     mun = None if mu is None else mu.cpu().double().numpy()
     out = res["out"].cpu().double().numpy()
     kept = res["kept"].cpu().numpy()
@@ -54,15 +55,17 @@ def check_decode(q, Kc, Vc, seq_len, theta, mode, sdc, vmc, mu, res, gamma=ref.G
         for h in hs:
             a = ref.row_scores(qn[b, h], Kn, L)
             gpu_keep = unpack_mask(mask[b, h], L)
+            e_off = 0.0 if et is None else ref.theta_for_row(et[h], L)
             r0 = ref.attend_row(a, Vn, ref.theta_for_row(th[h], L), mode, sdc, vmc,
-                                None if mun is None else mun[b, kv], gamma)
+                                None if mun is None else mun[b, kv], gamma, e_tilde=e_off)
             band = r0["band"]
             n_band += int(band.sum())
             mism = (gpu_keep != r0["keep"]) & ~band
             assert not mism.any(), f"mask mismatch (b={b}, h={h}) at {np.flatnonzero(mism)[:10]}"
             assert not unpack_mask(mask[b, h], mask.shape[-1] * 32)[L:].any(), "bits beyond L"
             r = ref.attend_row(a, Vn, ref.theta_for_row(th[h], L), mode, sdc, vmc,
-                               None if mun is None else mun[b, kv], gamma, decide=gpu_keep)
+                               None if mun is None else mun[b, kv], gamma, decide=gpu_keep,
+                               e_tilde=e_off)
             assert kept[b, h] == r["kept"], (b, h, kept[b, h], r["kept"])
             err = ref.output_rel_error(out[b, h], r["out"])
             worst = max(worst, err)
@@ -73,12 +76,14 @@ def check_decode(q, Kc, Vc, seq_len, theta, mode, sdc, vmc, mu, res, gamma=ref.G
     return len(heads), n_band, worst
 
 
-def check_prefill(Q, K, V, theta, mode, sdc, vmc, res, rows=None, gamma=ref.GAMMA, out_tol=OUT_TOL):
+def check_prefill(Q, K, V, theta, mode, sdc, vmc, res, rows=None, gamma=ref.GAMMA, out_tol=OUT_TOL,
+                  e_tilde=None):
     """Compare topt.prefill results (with mask) with prefill_ref on the given rows."""
     Qn, Kn, Vn = synth.as_f64(Q), synth.as_f64(K), synth.as_f64(V)
     B, Hq, S, _ = Qn.shape
     g = Hq // Kn.shape[1]
     th = theta.cpu().double().numpy()
+    et = None if e_tilde is None else e_tilde.cpu().double().numpy()
     out = res["out"].cpu().double().numpy()
     kept = res["kept"].cpu().numpy()
     mask = res["mask"].cpu().numpy()
@@ -93,14 +98,16 @@ def check_prefill(Q, K, V, theta, mode, sdc, vmc, res, rows=None, gamma=ref.GAMM
         a = ref.row_scores(Qn[b, h, i], Kn[b, kv], L)
         mu = ref.vmean_ref(Vn[b, kv, :L]) if vmc else None
         gk = unpack_mask(mask[b, h, i], L)
-        r0 = ref.attend_row(a, Vn[b, kv, :L], ref.theta_for_row(th[h], L), mode, sdc, vmc, mu, gamma)
+        e_off = 0.0 if et is None else ref.theta_for_row(et[h], L)
+        r0 = ref.attend_row(a, Vn[b, kv, :L], ref.theta_for_row(th[h], L), mode, sdc, vmc, mu, gamma,
+                            e_tilde=e_off)
         band = r0["band"]
         n_band += int(band.sum())
         mism = (gk != r0["keep"]) & ~band
         assert not mism.any(), f"mask mismatch (b={b}, h={h}, i={i}) at {np.flatnonzero(mism)[:10]}"
         assert not unpack_mask(mask[b, h, i], mask.shape[-1] * 32)[L:].any(), "bits beyond row"
         r = ref.attend_row(a, Vn[b, kv, :L], ref.theta_for_row(th[h], L), mode, sdc, vmc, mu,
-                           gamma, decide=gk)
+                           gamma, decide=gk, e_tilde=e_off)
         assert kept[b, h, i] == r["kept"], (b, h, i)
         err = ref.output_rel_error(out[b, h, i], r["out"])
         worst = max(worst, err)

@@ -64,7 +64,9 @@ def test_decode_validation_rejects_on_host(L):
     for kw in bad:
         assert L.topt_decode_workspace(ctypes.byref(_decode_args(**kw)), ctypes.byref(n)) == 3, kw
     assert L.topt_decode_workspace(ctypes.byref(_decode_args(mode=7)), ctypes.byref(n)) == 1
-    assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=3)), ctypes.byref(n)) == 1
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=4)), ctypes.byref(n)) == 1
+    # the offline estimator is a valid mode; its table is checked at the call
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=3)), ctypes.byref(n)) == 0
     # NULL tensors: rejected before any launch
     assert L.topt_decode(ctypes.byref(_decode_args()), None) == 1
 
@@ -92,6 +94,26 @@ def test_prefill_and_calibrate_validation(L):
     c.flags = 8
     assert L.topt_calibrate(ctypes.byref(c), None) == 1
     assert L.topt_select_kth(None, 3, 4, None, 1, None, None, None) == 1
+
+    e = topt.SdcCalibArgs()
+    e.n_seqs, e.n_q_heads, e.n_kv_heads, e.head_dim, e.n_rows, e.n_keys = 2, 4, 2, 64, 10, 10
+    e.theta_len, e.dtype = 10, topt.BF16
+    assert L.topt_calibrate_sdc_workspace(ctypes.byref(e), ctypes.byref(n)) == 0
+    assert n.value >= 2 * 4 * 10 * 10 * 4
+    assert L.topt_calibrate_sdc(ctypes.byref(e), None) == 1    # NULL theta / accumulators
+    e.n_kv_heads = 3
+    assert L.topt_calibrate_sdc_workspace(ctypes.byref(e), ctypes.byref(n)) == 3
+
+    m = topt.MkcArgs()
+    m.n_seqs, m.n_q_heads, m.n_kv_heads, m.head_dim, m.n_rows, m.n_keys = 2, 4, 2, 64, 10, 10
+    m.theta_len, m.dtype, m.mode, m.n_k = 10, topt.BF16, topt.PRE, 3
+    assert L.topt_calibrate_multik_workspace(ctypes.byref(m), ctypes.byref(n)) == 0
+    assert n.value >= 2 * 10 * 10 * 4 + 3 * 4 * 10 * 4
+    assert L.topt_calibrate_multik(ctypes.byref(m), None) == 1  # NULL tensors
+    m.n_k = 0
+    assert L.topt_calibrate_multik_workspace(ctypes.byref(m), ctypes.byref(n)) == 1
+    m.n_k, m.n_keys = 3, 1 << 20
+    assert L.topt_calibrate_multik_workspace(ctypes.byref(m), ctypes.byref(n)) == 3
 
     v = topt.VmeanArgs()
     v.batch, v.n_kv_heads, v.head_dim, v.cache_len, v.dtype, v.n_new = 1, 1, 64, 8, topt.BF16, 9
