@@ -35,10 +35,10 @@ reason in the design notes of the repository):
 * c12 an empty selection gives num = 0 and R = 0 (pre without SDC: out = 0).
 * c13 std uses ddof = 1; a single sample has std 0.
 * c16 post-softmax with SDC is post-softmax (SDC maps pre onto post).
-* c17 MKC: theta_r(k) = sup{theta : k_bar_r(theta) >= k} (App. D leaves the
+* c19 MKC: theta_r(k) = sup{theta : k_bar_r(theta) >= k} (App. D leaves the
       inverse of a fractional, not always monotone k_bar open); Eq. 8 averages
       only over the intervals that contain theta, as printed.
-* c18 offline-calibrated E~ (estimator 1 of §3.2.1) is the mean, over the
+* c20 offline-calibrated E~ (estimator 1 of §3.2.1) is the mean, over the
       calibration rows of a row id, of the exact discarded sum E of each row
       under the inference thresholds, in the max-shifted units of reading c8;
       rows with theta = -inf get 0; row ids without samples take the nearest
@@ -204,7 +204,7 @@ def collect_discarded(Qc, Kc, row_len, theta, sets=None):
 def finalize_discarded(sets, theta):
     """E~ [Hq][Lmax]: the mean of each sampled row id, the nearest sampled row
     id elsewhere (reading c5), 0 where theta is -inf or nothing was sampled
-    (reading c18)."""
+    (reading c20)."""
     Hq, Lmax = theta.shape
     et = np.zeros((Hq, Lmax))
     for h in range(Hq):
@@ -294,7 +294,7 @@ def merge_intervals(seqs):
 
 
 def mkc_theta(pieces, k):
-    """theta_r(k), the inverse of k_bar_r at k (reading c17).
+    """theta_r(k), the inverse of k_bar_r at k (reading c19).
 
     The largest threshold up to which the calibration rows keep at least k
     elements on average: sup{theta : k_bar(theta) >= k}, the upper end of the
@@ -353,7 +353,7 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     theta  the row's calibrated threshold (pre: on a, post: on s)
     decide optional bool [L]; inside the band |x - theta| <= 1e-3 |theta| the
            oracle adopts these decisions instead of its own.
-    e_tilde the row's offline-calibrated estimate (SDC_OFFLINE, reading c18)
+    e_tilde the row's offline-calibrated estimate (SDC_OFFLINE, reading c20)
 
     Returns a dict with out [d], keep [L], kept (k~), band [L], m, Z, R, E, beta.
     """
@@ -386,7 +386,7 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     else:
         if sdc == SDC_EXACT:                # [TopTheta §3.2.1, estimator 3]
             E_est = E
-        elif sdc == SDC_OFFLINE:            # [TopTheta §3.2.1, estimator 1], reading c18
+        elif sdc == SDC_OFFLINE:            # [TopTheta §3.2.1, estimator 1], reading c20
             E_est = float(e_tilde)
         else:                               # [TopTheta §3.2.1, estimator 2], reading c8
             E_est = gamma * (L - kt) * math.exp(theta - m) if L > kt else 0.0
