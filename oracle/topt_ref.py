@@ -44,6 +44,10 @@ reason in the design notes of the repository):
       rows with theta = -inf get 0; row ids without samples take the nearest
       sampled one (reading c5), none at all 0.  At inference it is used as
       it is, whatever the row itself keeps.
+* c21 GQA group policies (§4.6, the two alternatives): UNION gives every head
+      of a group the union of the group's kept sets; VOTE keeps a key for a
+      head only if the head keeps it and at least t heads of the group do.
+      Each head then normalises over its final set (R, k~, SDC, beta).
 """
 from __future__ import annotations
 
@@ -53,6 +57,7 @@ import numpy as np
 
 PRE, POST = 0, 1
 SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
+GQA_OWN, GQA_UNION, GQA_VOTE = 0, 1, 2
 GAMMA = 0.05          # [TopTheta §3.2.1, exp-threshold estimator]
 BAND_REL = 1e-3       # decisions within this relative distance of theta are not compared
 
@@ -345,7 +350,7 @@ def theta_for_row(theta_row, L):
 # Inference on one attention row: threshold, SDC, VMC.
 # ---------------------------------------------------------------------------
 def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
-               gamma=GAMMA, decide=None, e_tilde=0.0):
+               gamma=GAMMA, decide=None, e_tilde=0.0, keep=None):
     """Top-theta attention of one row.
 
     a      scores of the L visible keys (Eq. 1)
@@ -354,6 +359,8 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     decide optional bool [L]; inside the band |x - theta| <= 1e-3 |theta| the
            oracle adopts these decisions instead of its own.
     e_tilde the row's offline-calibrated estimate (SDC_OFFLINE, reading c20)
+    keep   optional bool [L]: the final kept set, replacing the comparison with
+           theta (a GQA group policy decided it, reading c21)
 
     Returns a dict with out [d], keep [L], kept (k~), band [L], m, Z, R, E, beta.
     """
@@ -365,6 +372,7 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
     Z = float(e.sum())
     s = e / Z                               # Eq. 2
     x = a if mode == PRE else s
+    forced = keep
     keep = x >= theta                       # reading c1
     if np.isfinite(theta):
         band = np.abs(x - theta) <= BAND_REL * abs(theta)
@@ -372,6 +380,8 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
         band = np.zeros(L, dtype=bool)
     if decide is not None:
         keep = np.where(band, np.asarray(decide, dtype=bool), keep)
+    if forced is not None:
+        keep = np.asarray(forced, dtype=bool).copy()
     kt = int(keep.sum())
     R = float(e[keep].sum())                # Eq. 4: selected exponent sum
     E = Z - R                               # Eq. 4: discarded exponent sum
@@ -418,13 +428,33 @@ def vmean_update_ref(mu, n_old, new_rows):
 # ---------------------------------------------------------------------------
 # Decode and prefill drivers (loops over rows, heads and batches).
 # ---------------------------------------------------------------------------
+def group_policy(keeps, policy, min_heads=1):
+    """Final kept sets of the g heads of one GQA group ([TopTheta §4.6]).
+
+    keeps [g][L] are the heads' own threshold decisions.  GQA_OWN keeps them
+    (the paper's experiments); GQA_UNION gives every head the union, "to
+    leverage V rows already loaded for the group"; GQA_VOTE discards keys
+    requested by fewer than ``min_heads`` heads (reading c21).
+    """
+    K = np.asarray(keeps, dtype=bool)
+    if policy == GQA_OWN:
+        return K.copy()
+    if policy == GQA_UNION:
+        return np.repeat(K.any(axis=0)[None, :], K.shape[0], axis=0)
+    votes = K.sum(axis=0)
+    return K & (votes >= min_heads)[None, :]
+
+
 def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
-               mu=None, gamma=GAMMA, decide=None, heads=None, e_tilde=None):
+               mu=None, gamma=GAMMA, decide=None, heads=None, e_tilde=None,
+               gqa=GQA_OWN, gqa_min_heads=1):
     """One generated token per sequence ([TopTheta §2.2, generative decoding]).
 
     q [B][Hq][d]; Kc, Vc [B][Hkv][Nmax][d]; seq_len [B] (keys incl. the current
     token); theta [Hq][Lmax]; mu [B][Hkv][d] (when vmc); e_tilde [Hq][Lmax]
-    (SDC_OFFLINE, looked up like theta).  ``decide`` is an
+    (SDC_OFFLINE, looked up like theta); gqa / gqa_min_heads the group policy
+    (``group_policy``; a policy other than GQA_OWN computes whole groups).
+    ``decide`` is an
     optional bool [B][Hq][Nmax] of decisions adopted inside the band.
     ``heads`` optionally restricts the work to a list of (b, h) pairs.
 
@@ -437,6 +467,9 @@ def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
     res = {}
     if heads is None:
         heads = [(b, h) for b in range(B) for h in range(Hq)]
+    if gqa != GQA_OWN:
+        groups = sorted({(b, h // g) for (b, h) in heads})
+        heads = [(b, kv * g + i) for (b, kv) in groups for i in range(g)]
     for (b, h) in heads:
         L = int(seq_len[b])
         kv = h // g
@@ -446,6 +479,18 @@ def decode_ref(q, Kc, Vc, seq_len, theta, mode, sdc=SDC_NONE, vmc=False,
         et = 0.0 if e_tilde is None else theta_for_row(e_tilde[h], L)
         res[(b, h)] = attend_row(a, Vc[b, kv, :L], th, mode, sdc, vmc,
                                  None if mu is None else mu[b, kv], gamma, dec, et)
+    if gqa != GQA_OWN:
+        for (b, kv) in groups:
+            L = int(seq_len[b])
+            hs = [kv * g + i for i in range(g)]
+            final = group_policy([res[(b, h)]["keep"] for h in hs], gqa, gqa_min_heads)
+            for i, h in enumerate(hs):
+                a = row_scores(q[b, h], Kc[b, kv], L)
+                th = theta_for_row(theta[h], L)
+                et = 0.0 if e_tilde is None else theta_for_row(e_tilde[h], L)
+                res[(b, h)] = attend_row(a, Vc[b, kv, :L], th, mode, sdc, vmc,
+                                         None if mu is None else mu[b, kv], gamma, None, et,
+                                         keep=final[i])
     union = {}
     for (b, h), r in res.items():
         key = (b, h // g)

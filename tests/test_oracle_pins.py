@@ -372,6 +372,67 @@ def test_offline_sdc_one_row_calibration_is_exact_on_that_row():
 
 
 # ---------------------------------------------------------------------------
+# GQA group policies (§4.6): set invariants against the heads' own decisions.
+# ---------------------------------------------------------------------------
+def _gqa_case(seed, same_q=False):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, d, Nmax = 2, 8, 2, 16, 40
+    K = rng.normal(size=(B, Hkv, Nmax, d))
+    V = rng.normal(size=(B, Hkv, Nmax, d))
+    q = rng.normal(size=(B, Hq, d)) * 2
+    if same_q:
+        q[:, 1:4] = q[:, :1]
+        q[:, 5:8] = q[:, 4:5]
+    seq = [40, 23]
+    theta = rng.normal(size=(Hq, Nmax)) * 0.5 + 0.8
+    if same_q:                    # identical heads: same query and same thresholds
+        theta[1:4] = theta[:1]
+        theta[5:8] = theta[4:5]
+    mu = V.mean(axis=2)
+    return q, K, V, seq, theta, mu
+
+
+def check_gqa_policies(seed=10):
+    g = 4
+    for same_q in (False, True):
+        q, K, V, seq, theta, mu = _gqa_case(seed, same_q)
+        for mode, sdc in ((ref.PRE, ref.SDC_NONE), (ref.PRE, ref.SDC_EXACT), (ref.POST, ref.SDC_NONE)):
+            own, v_own = ref.decode_ref(q, K, V, seq, theta, mode, sdc, True, mu)
+            uni, v_uni = ref.decode_ref(q, K, V, seq, theta, mode, sdc, True, mu, gqa=ref.GQA_UNION)
+            assert v_uni == v_own                       # the union reads the same V rows
+            for (b, h), r in own.items():
+                grp = np.any([own[(b, (h // g) * g + i)]["keep"] for i in range(g)], axis=0)
+                assert np.array_equal(uni[(b, h)]["keep"], grp)
+                assert np.all(uni[(b, h)]["keep"] >= r["keep"])
+                if same_q:                              # identical heads: the union is each own set
+                    np.testing.assert_allclose(uni[(b, h)]["out"], r["out"], rtol=1e-13, atol=1e-15)
+            one, v_one = ref.decode_ref(q, K, V, seq, theta, mode, sdc, True, mu, gqa=ref.GQA_VOTE,
+                                        gqa_min_heads=1)
+            assert v_one == v_own
+            for key in own:
+                np.testing.assert_allclose(one[key]["out"], own[key]["out"], rtol=1e-13, atol=1e-15)
+            prev = one
+            for t in range(2, g + 2):
+                vt, v_vt = ref.decode_ref(q, K, V, seq, theta, mode, sdc, True, mu, gqa=ref.GQA_VOTE,
+                                          gqa_min_heads=t)
+                for (b, kv), n in v_vt.items():
+                    votes = np.zeros(seq[b], dtype=int)
+                    for i in range(g):
+                        votes += own[(b, kv * g + i)]["keep"]
+                    assert n == int((votes >= t).sum())  # brute-force vote count
+                for key, r in vt.items():
+                    assert np.all(r["keep"] <= prev[key]["keep"])
+                    assert np.all(r["keep"] <= own[key]["keep"])
+                    if t > g:
+                        assert r["kept"] == 0
+                prev = vt
+
+
+def test_gqa_policies_invariants():
+    check_gqa_policies()
+
+
+# ---------------------------------------------------------------------------
 # Multi-k cumulative calibration (App. D, Algorithm 2, Eq. 8).
 # ---------------------------------------------------------------------------
 def _mkc_inputs(rows, d=4):
@@ -542,6 +603,23 @@ def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
         return th
     _planted(monkeypatch, "finalize_thresholds", first_row,
              lambda: check_golden_nearest_row(golden_dir))
+
+    # GQA: intersection instead of union, and votes compared with > instead of >=
+    orig_pol = ref.group_policy
+
+    def wrong_union(keeps, policy, min_heads=1):
+        if policy == ref.GQA_UNION:
+            K = np.asarray(keeps, dtype=bool)
+            return np.repeat(K.all(axis=0)[None, :], K.shape[0], axis=0)
+        return orig_pol(keeps, policy, min_heads)
+    _planted(monkeypatch, "group_policy", wrong_union, check_gqa_policies)
+
+    def strict_vote(keeps, policy, min_heads=1):
+        if policy == ref.GQA_VOTE:
+            K = np.asarray(keeps, dtype=bool)
+            return K & (K.sum(axis=0) > min_heads)[None, :]
+        return orig_pol(keeps, policy, min_heads)
+    _planted(monkeypatch, "group_policy", strict_vote, check_gqa_policies)
 
     # offline E~ summed without subtracting the row maximum
     _planted(monkeypatch, "discarded_sum",
