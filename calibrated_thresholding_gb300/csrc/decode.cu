@@ -84,6 +84,7 @@ struct DecodeParams {
   uint32_t* mask;
   int32_t* status;
   int mask_words, spp, ipp, slice_len, lstride, score_warps;
+  int gqa_min;        // TOPT_GQA_VOTE: heads of the group that must keep a key
   // workspace
   float* logits;      // [pairs][lstride][score_cols(G)]
   float2* stats;      // [pairs][spp][G]: a warp run's partial at the run's first tile
@@ -427,7 +428,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_scores_kernel(const Decode
 // ----------------------------------------------------------------------------
 // Select: one slice of one pair per CTA.
 // ----------------------------------------------------------------------------
-template <int D, int G>
+// POL is the GQA group policy [TopTheta §4.6]: TOPT_GQA_OWN (each head its own
+// selection), TOPT_GQA_UNION (every head the group's union) or TOPT_GQA_VOTE
+// (a key survives for a head that keeps it only if p.gqa_min heads keep it).
+template <int D, int G, int POL>
 __global__ void __launch_bounds__(kThreads, select_min_blocks<G>()) decode_select_kernel(const DecodeParams p) {
   constexpr int SK = slice_keys<G>();
   constexpr int NGRP = SK / kThreads;     // 32-key groups per warp
@@ -537,16 +541,42 @@ __global__ void __launch_bounds__(kThreads, select_min_blocks<G>()) decode_selec
     const bool in_slice = gi * kThreads < SL;  // warp-uniform
     const bool valid = in_slice && s0 + jl < L;
     unsigned un = 0u;
+    if constexpr (POL == TOPT_GQA_OWN) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float a = valid ? sm.u.sc[jl * GC + h] : -CUDART_INF_F;
-      const bool keep = valid && (a >= T[h]);
-      wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
-      Rl[h] += wv[gi][h];
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      kt[h] += __popc(bal);
-      un |= bal;
-      if (mrow && lane == 0 && in_slice && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      for (int h = 0; h < G; ++h) {
+        const float a = valid ? sm.u.sc[jl * GC + h] : -CUDART_INF_F;
+        const bool keep = valid && (a >= T[h]);
+        wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
+        Rl[h] += wv[gi][h];
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        kt[h] += __popc(bal);
+        un |= bal;
+        if (mrow && lane == 0 && in_slice && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      }
+    } else {
+      // the heads' own decisions for this lane's key, then the group policy
+      unsigned kb = 0u;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float a = valid ? sm.u.sc[jl * GC + h] : -CUDART_INF_F;
+        if (valid && a >= T[h]) kb |= 1u << h;
+      }
+      if constexpr (POL == TOPT_GQA_UNION) {
+        if (kb) kb = (1u << G) - 1u;
+      } else {
+        if (__popc(kb) < p.gqa_min) kb = 0u;
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const bool keep = (kb >> h) & 1u;
+        const float a = keep ? sm.u.sc[jl * GC + h] : 0.f;
+        wv[gi][h] = keep ? __expf(a - M[h]) : 0.f;
+        Rl[h] += wv[gi][h];
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        kt[h] += __popc(bal);
+        un |= bal;
+        if (mrow && lane == 0 && in_slice && j0 < p.mask_words * 32) mrow[(size_t)h * p.mask_words + (j0 >> 5)] = bal;
+      }
     }
     uni[gi] = un;
     wcount += __popc(un);
@@ -710,8 +740,17 @@ cudaError_t grid_of(int& grid) {
     if ((e = cudaFuncSetAttribute(decode_scores_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)smem)) != cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)sizeof(SelectSmem<D, G>))) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G, TOPT_GQA_OWN>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelectSmem<D, G>))) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G, TOPT_GQA_UNION>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelectSmem<D, G>))) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(decode_select_kernel<D, G, TOPT_GQA_VOTE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelectSmem<D, G>))) !=
+        cudaSuccess)
       return e;
     int per_sm = 0, sms = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_scores_kernel<D, G>, kThreads, smem)) !=
@@ -777,7 +816,10 @@ cudaError_t launch_dg(DecodeParams p, const topt_decode_args& a, cudaStream_t s)
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if ((e = record_event(a.events[1], s)) != cudaSuccess) return e;
-  if ((e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G>, p)) != cudaSuccess) return e;
+  if (a.gqa_policy == TOPT_GQA_UNION) e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G, TOPT_GQA_UNION>, p);
+  else if (a.gqa_policy == TOPT_GQA_VOTE) e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G, TOPT_GQA_VOTE>, p);
+  else e = cudaLaunchKernelEx(&cfg, decode_select_kernel<D, G, TOPT_GQA_OWN>, p);
+  if (e != cudaSuccess) return e;
   return record_event(a.events[2], s);
 }
 
@@ -865,6 +907,7 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.mask = a.mask;
   p.status = a.status;
   p.mask_words = (a.cache_len + 31) / 32;
+  p.gqa_min = a.gqa_min_heads;
   p.spp = (a.cache_len + kTile - 1) / kTile + 1;
   p.lstride = logit_stride(a.cache_len);
   p.ipp = 1;

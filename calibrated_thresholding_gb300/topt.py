@@ -17,6 +17,7 @@ from . import build as _build
 
 PRE, POST = 0, 1
 SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
+GQA_OWN, GQA_UNION, GQA_VOTE = 0, 1, 2
 BF16, F32 = 0, 1
 CALIB_RESET, CALIB_FINALIZE = 1, 2
 GAMMA = 0.05
@@ -39,7 +40,8 @@ class DecodeArgs(ctypes.Structure):
                 ("cache_len", i32), ("theta_len", i32), ("mode", i32), ("sdc", i32), ("vmc", i32),
                 ("gamma", f32), ("q", vp), ("k_cache", vp), ("v_cache", vp), ("seq_len", vp),
                 ("theta", vp), ("e_tilde", vp), ("mu", vp), ("out", vp), ("kept", vp), ("vrows", vp), ("mask", vp),
-                ("status", vp), ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 3)]
+                ("status", vp), ("workspace", vp), ("workspace_bytes", sz), ("events", vp * 3),
+                ("gqa_policy", i32), ("gqa_min_heads", i32)]
 
 
 class PrefillArgs(ctypes.Structure):
@@ -164,13 +166,14 @@ def _dtype_code(t):
 # ---------------------------------------------------------------------------
 def decode_args(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
                 gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-                workspace=None, e_tilde=None):
+                workspace=None, e_tilde=None, gqa=GQA_OWN, gqa_min_heads=1):
     B, Hq, d = q.shape
     _, Hkv, Nmax, _ = k_cache.shape
     a = DecodeArgs()
     a.batch, a.n_q_heads, a.n_kv_heads, a.head_dim = B, Hq, Hkv, d
     a.cache_len, a.theta_len = Nmax, theta.shape[-1]
     a.mode, a.sdc, a.vmc, a.gamma = int(mode), int(sdc), int(bool(vmc)), float(gamma)
+    a.gqa_policy, a.gqa_min_heads = int(gqa), int(gqa_min_heads)
     a.q = _ptr(_dev(q, "q", torch.bfloat16))
     a.k_cache = _ptr(_dev(k_cache, "k_cache", torch.bfloat16))
     a.v_cache = _ptr(_dev(v_cache, "v_cache", torch.bfloat16))
@@ -202,7 +205,7 @@ def decode_workspace(a: DecodeArgs, device) -> torch.Tensor:
 
 def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
            gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-           workspace=None, stream=None, e_tilde=None):
+           workspace=None, stream=None, e_tilde=None, gqa=GQA_OWN, gqa_min_heads=1):
     """Top-theta decode through ``topt_decode``; see include/topt.h for shapes.
 
     Allocates (with torch) the outputs and the workspace that are not given.
@@ -219,7 +222,7 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
         vrows = torch.empty((B, Hkv), device=dev, dtype=torch.int32)
     a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
                     gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status,
-                    e_tilde=e_tilde)
+                    e_tilde=e_tilde, gqa=gqa, gqa_min_heads=gqa_min_heads)
     if workspace is None:
         workspace = decode_workspace(a, dev)
     a.workspace = _ptr(_dev(workspace, "workspace", torch.uint8))
@@ -230,7 +233,7 @@ def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False
 
 def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,
                    gamma=GAMMA, out=None, kept=None, vrows=None, mask=None, status=None,
-                   stream=None, e_tilde=None):
+                   stream=None, e_tilde=None, gqa=GQA_OWN, gqa_min_heads=1):
     """Top-theta decode through ``topt_decode_noalloc`` (library-held scratch).
 
     For callers that must not allocate device scratch; see include/topt.h for
@@ -248,7 +251,7 @@ def decode_noalloc(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, v
         vrows = torch.empty((B, Hkv), device=dev, dtype=torch.int32)
     a = decode_args(q, k_cache, v_cache, seq_len, theta, mode=mode, sdc=sdc, vmc=vmc, mu=mu,
                     gamma=gamma, out=out, kept=kept, vrows=vrows, mask=mask, status=status,
-                    e_tilde=e_tilde)
+                    e_tilde=e_tilde, gqa=gqa, gqa_min_heads=gqa_min_heads)
     _check("topt_decode_noalloc", lib().topt_decode_noalloc(ctypes.byref(a), _stream(stream)))
     return dict(out=out, kept=kept, vrows=vrows, mask=mask)
 

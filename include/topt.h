@@ -72,9 +72,20 @@ typedef enum {
 
 typedef enum { TOPT_BF16 = 0, TOPT_F32 = 1 } topt_dtype;
 
+/* GQA group policies of decode [TopTheta §4.6, the two alternatives to each
+ * head using only its own selection]:
+ *   OWN    each head keeps its own selection (the paper's experiments)
+ *   UNION  every head of a group uses the union of the group's selections,
+ *          which reads no extra V row
+ *   VOTE   a key a head keeps survives only if at least gqa_min_heads heads
+ *          of the group keep it; V rows requested by fewer heads are not read
+ * Each head then normalises over its final set (R, k~, SDC, beta).  kept,
+ * vrows and mask report the final sets. */
+typedef enum { TOPT_GQA_OWN = 0, TOPT_GQA_UNION = 1, TOPT_GQA_VOTE = 2 } topt_gqa_policy;
+
 /* ------------------------------------------------------------------------ */
 /* Decode: one query token per sequence against its KV cache.               */
-/* [TopTheta §2.2 "generative decoding", Fig. 1, §3.2, §4.6 (GQA)]          */
+/* [TopTheta §2.2 (generative decoding), Fig. 1, §3.2, §4.6 (GQA)]          */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t batch;        /* B, 1 .. 256 */
@@ -112,6 +123,8 @@ typedef struct {
    * kernels keeps the select kernel from being scheduled early, so leave [1]
    * NULL unless the split is wanted. */
   void* events[3];
+  int32_t gqa_policy;     /* topt_gqa_policy; 0 (OWN) when zero-initialised */
+  int32_t gqa_min_heads;  /* TOPT_GQA_VOTE: t >= 1 heads (t = 1 is OWN); else ignored */
 } topt_decode_args;
 
 /* Bytes of workspace topt_decode needs for these shapes (pointers unused). */
@@ -143,7 +156,7 @@ topt_status topt_decode_noalloc(const topt_decode_args* args, topt_stream stream
 
 /* ------------------------------------------------------------------------ */
 /* Prefill: causal attention of S query rows; row i sees keys 0..i.         */
-/* [TopTheta §2.2 "prefill phase", §3, §3.2]                                 */
+/* [TopTheta §2.2 (prefill phase), §3, §3.2]                                 */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t batch;        /* B */
@@ -333,8 +346,8 @@ topt_status topt_select_kth(const float* x, int32_t rows, int32_t row_stride,
                             int32_t* status, topt_stream stream);
 
 /* ------------------------------------------------------------------------ */
-/* Running mean of V rows [TopTheta §3.2.2: "mu can be maintained as a       */
-/* running mean during generative decoding"]                                 */
+/* Running mean of V rows [TopTheta §3.2.2: in decode, mu is updated with    */
+/* each new row instead of being recomputed]                                  */
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t batch, n_kv_heads, head_dim, cache_len;

@@ -432,9 +432,9 @@ def group_policy(keeps, policy, min_heads=1):
     """Final kept sets of the g heads of one GQA group ([TopTheta §4.6]).
 
     keeps [g][L] are the heads' own threshold decisions.  GQA_OWN keeps them
-    (the paper's experiments); GQA_UNION gives every head the union, "to
-    leverage V rows already loaded for the group"; GQA_VOTE discards keys
-    requested by fewer than ``min_heads`` heads (reading c21).
+    (the paper's experiments); GQA_UNION gives every head the union, so the
+    heads use V rows the group loads anyway; GQA_VOTE drops keys that fewer
+    than ``min_heads`` heads keep (reading c21).
     """
     K = np.asarray(keeps, dtype=bool)
     if policy == GQA_OWN:

@@ -67,6 +67,11 @@ def test_decode_validation_rejects_on_host(L):
     assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=4)), ctypes.byref(n)) == 1
     # the offline estimator is a valid mode; its table is checked at the call
     assert L.topt_decode_workspace(ctypes.byref(_decode_args(sdc=3)), ctypes.byref(n)) == 0
+    # GQA policies: unknown policy and VOTE without a head count are refused
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(gqa_policy=3)), ctypes.byref(n)) == 1
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(gqa_policy=2)), ctypes.byref(n)) == 1
+    assert L.topt_decode_workspace(ctypes.byref(_decode_args(gqa_policy=2, gqa_min_heads=2)),
+                                   ctypes.byref(n)) == 0
     # NULL tensors: rejected before any launch
     assert L.topt_decode(ctypes.byref(_decode_args()), None) == 1
 
