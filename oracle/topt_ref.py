@@ -44,6 +44,11 @@ reason in the design notes of the repository):
       rows with theta = -inf get 0; row ids without samples take the nearest
       sampled one (reading c5), none at all 0.  At inference it is used as
       it is, whatever the row itself keeps.
+* c22 fitted theta(L): the pages mention a function of the sequence length
+      fitted to the calibrated thresholds without its form; here a least-
+      squares polynomial of degree min(2, n - 1) in ln L through the n
+      calibrated row ids L > k, fitted to theta (pre) or to ln theta (post,
+      positive values only), and used for every row id L > k.
 * c21 GQA group policies (§4.6, the two alternatives): UNION gives every head
       of a group the union of the group's kept sets; VOTE keeps a key for a
       head only if the head keeps it and at least t heads of the group do.
@@ -167,9 +172,53 @@ def fill_row_ids(value, Lmax, k):
     return row
 
 
-def calibrate_ref(Qc, Kc, row_len, k, mode, alpha, Lmax):
-    """Algorithm 1 for one layer: returns (theta [Hq][Lmax], sets)."""
+def fit_row_ids(value, Lmax, k, mode):
+    """One head's row of the table from a function of ln L fitted to the
+    calibrated row ids ``value`` (L -> theta), reading c22.
+
+    y = theta (PRE) or ln theta (POST, theta > 0 only) is fitted by least
+    squares with a polynomial of degree min(2, n - 1) in x = ln L over the n
+    usable row ids; every L > k takes the fitted value (exp of it for POST),
+    L <= k stays dense, and a head without usable row ids is dense.
+    """
+    row = np.full(Lmax, -np.inf)
+    pts = [(L, v) for L, v in sorted(value.items()) if L > k and (mode == PRE or v > 0)]
+    if not pts:
+        return row
+    x = np.log(np.array([L for L, _ in pts], dtype=np.float64))
+    y = np.array([v for _, v in pts], dtype=np.float64)
+    if mode == POST:
+        y = np.log(y)
+    deg = min(2, len(pts) - 1)
+    coef = np.polynomial.polynomial.polyfit(x, y, deg)
+    Ls = np.arange(k + 1, Lmax + 1, dtype=np.float64)
+    fitted = np.polynomial.polynomial.polyval(np.log(Ls), coef)
+    row[k:] = np.exp(fitted) if mode == POST else fitted
+    return row
+
+
+def finalize_fitted(sets, Hq, Lmax, k, alpha, mode):
+    """theta [Hq][Lmax] from the fitted function of ln L (reading c22); the
+    calibrated values are the Algorithm 1 statistics of ``finalize_thresholds``."""
+    theta = np.full((Hq, Lmax), -np.inf)
+    for h in range(Hq):
+        value = {}
+        for (hh, L), obs in sets.items():
+            if hh != h or L > Lmax:
+                continue
+            obs = np.asarray(obs, dtype=np.float64)
+            std = float(np.std(obs, ddof=1)) if obs.size > 1 else 0.0
+            value[L] = float(np.mean(obs)) + alpha * std
+        theta[h] = fit_row_ids(value, Lmax, k, mode)
+    return theta
+
+
+def calibrate_ref(Qc, Kc, row_len, k, mode, alpha, Lmax, fit=False):
+    """Algorithm 1 for one layer: returns (theta [Hq][Lmax], sets); ``fit``
+    replaces the nearest-row fill with the fitted function of ln L."""
     sets = collect_thresholds(Qc, Kc, row_len, k, mode)
+    if fit:
+        return finalize_fitted(sets, Qc.shape[1], Lmax, k, alpha, mode), sets
     return finalize_thresholds(sets, Qc.shape[1], Lmax, k, alpha), sets
 
 

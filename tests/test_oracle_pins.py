@@ -372,6 +372,59 @@ def test_offline_sdc_one_row_calibration_is_exact_on_that_row():
 
 
 # ---------------------------------------------------------------------------
+# Fitted theta(L) (reading c22): exact recovery of functions of ln L.
+# ---------------------------------------------------------------------------
+def check_fitted_theta():
+    k, Lmax = 3, 200
+    c = (0.7, 0.45, -0.04)
+    f = lambda L: c[0] + c[1] * math.log(L) + c[2] * math.log(L) ** 2
+    # one calibration row per length, its k-th largest score set to f(L)
+    for L in (5, 9, 17, 33, 64, 90):
+        row = np.concatenate([f(L) + 1.0 + np.arange(k - 1), [f(L)], f(L) - 1.0 - np.arange(L - k)])
+        Qc, Kc = _mkc_inputs([row])
+        th, _ = ref.calibrate_ref(Qc, Kc, [L], k, ref.PRE, 0.0, Lmax, fit=False)
+        assert th[0, L - 1] == f(L)
+    sets = {(0, L): [f(L)] for L in (5, 9, 17, 33, 64, 90)}
+    theta = ref.finalize_fitted(sets, 1, Lmax, k, 0.0, ref.PRE)
+    want = np.array([f(L) for L in range(1, Lmax + 1)])
+    assert np.all(np.isneginf(theta[0, :k]))
+    np.testing.assert_allclose(theta[0, k:], want[k:], rtol=0, atol=1e-12)
+    # end to end through Algorithm 1 on the rows built above
+    Ls = (5, 9, 17, 33)
+    rows = [np.concatenate([f(L) + 1.0 + np.arange(k - 1), [f(L)], f(L) - 1.0 - np.arange(L - k)])
+            for L in Ls]
+    Nk = max(Ls)
+    # each row sees its own keys: put row i at keys 0..L_i-1 of its own sequence
+    Qs = np.zeros((len(Ls), 1, 1, 4))
+    Ks = np.zeros((len(Ls), 1, Nk, 4))
+    for i, (L, r) in enumerate(zip(Ls, rows)):
+        Qs[i, 0, 0, 0] = 2.0
+        Ks[i, 0, :L, 0] = r
+    sets = {}
+    for i, L in enumerate(Ls):
+        ref.collect_thresholds(Qs[i:i + 1], Ks[i:i + 1], [L], k, ref.PRE, sets)
+    th = ref.finalize_fitted(sets, 1, 120, k, 0.0, ref.PRE)
+    np.testing.assert_allclose(th[0, k:], want[k:120], rtol=0, atol=1e-12)
+    # post-softmax: a power law in L is a line in ln L after the log
+    sets = {(0, L): [0.3 * L ** -1.2] for L in (6, 20, 70)}
+    th = ref.finalize_fitted(sets, 1, Lmax, k, 0.0, ref.POST)
+    Lr = np.arange(k + 1, Lmax + 1)
+    np.testing.assert_allclose(th[0, k:], 0.3 * Lr ** -1.2, rtol=1e-12, atol=0)
+    # two calibrated lengths: the line through both points in ln L
+    th = ref.finalize_fitted({(0, 10): [1.0], (0, 40): [2.0]}, 1, 80, k, 0.0, ref.PRE)
+    assert abs(th[0, 9] - 1.0) < 1e-13 and abs(th[0, 39] - 2.0) < 1e-13
+    assert abs(th[0, 19] - 1.5) < 1e-13              # ln 20 is halfway between ln 10 and ln 40
+    # one length: a constant; none: dense
+    th = ref.finalize_fitted({(0, 10): [1.5]}, 1, 30, k, 0.0, ref.PRE)
+    assert np.all(th[0, k:] == 1.5)
+    assert np.all(np.isneginf(ref.finalize_fitted({}, 1, 30, k, 0.0, ref.PRE)))
+
+
+def test_fitted_theta_recovers_functions_of_log_length():
+    check_fitted_theta()
+
+
+# ---------------------------------------------------------------------------
 # GQA group policies (§4.6): set invariants against the heads' own decisions.
 # ---------------------------------------------------------------------------
 def _gqa_case(seed, same_q=False):
@@ -603,6 +656,21 @@ def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
         return th
     _planted(monkeypatch, "finalize_thresholds", first_row,
              lambda: check_golden_nearest_row(golden_dir))
+
+    # fitted theta(L) taken in L instead of ln L
+    orig_fit = ref.fit_row_ids
+
+    def fit_in_L(value, Lmax, k, mode):
+        pts = [(L, v) for L, v in sorted(value.items()) if L > k]
+        row = np.full(Lmax, -np.inf)
+        if not pts:
+            return row
+        x = np.array([L for L, _ in pts], float)
+        coef = np.polynomial.polynomial.polyfit(x, [v for _, v in pts], min(2, len(pts) - 1))
+        row[k:] = np.polynomial.polynomial.polyval(np.arange(k + 1, Lmax + 1, dtype=float), coef)
+        return row
+    _planted(monkeypatch, "fit_row_ids", fit_in_L, check_fitted_theta)
+    assert ref.fit_row_ids is orig_fit
 
     # GQA: intersection instead of union, and votes compared with > instead of >=
     orig_pol = ref.group_policy
