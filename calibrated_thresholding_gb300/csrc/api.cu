@@ -59,7 +59,7 @@ topt_status check_calib_shape(const topt_calib_args* a) {
   if (a->mode != TOPT_PRE && a->mode != TOPT_POST) return TOPT_EINVAL;
   if (a->k < 1) return TOPT_EINVAL;
   if (!std::isfinite(a->alpha)) return TOPT_EINVAL;
-  if (a->flags & ~(TOPT_CALIB_RESET | TOPT_CALIB_FINALIZE)) return TOPT_EINVAL;
+  if (a->flags & ~(TOPT_CALIB_RESET | TOPT_CALIB_FINALIZE | TOPT_CALIB_FIT)) return TOPT_EINVAL;
   return TOPT_OK;
 }
 

@@ -145,6 +145,7 @@ __device__ __forceinline__ void load8(const float* src, float f[8]) {
 struct CalibParams {
   int N, Hq, Hkv, R, Nk, Lmax, mode, k;
   int h0, Hp;  // the score kernel covers query heads h0 .. h0+Hp-1
+  int fit;     // FINALIZE writes the fitted function of ln L (TOPT_CALIB_FIT)
   float alpha, sm_scale;
   const void* q;
   const void* keys;
@@ -336,13 +337,110 @@ __device__ void fill_nearest_rows(int Lmax, int k, const Has& has, const Val& va
   }
 }
 
+// One head's row of a threshold table from a least-squares polynomial of
+// degree min(2, n - 1) in x = ln L through the n usable calibrated row ids
+// L > k: y = theta (PRE) or ln theta (POST, theta > 0 only).  Every L > k
+// takes the fitted value (exp of it for POST); L <= k and a head without
+// usable row ids are dense.  The pages mention a fitted function of the
+// sequence length without its form; this is the plainest such fit.  fp64
+// normal equations, solved by one thread (at most 3 x 3).
+template <class Has, class Val>
+__device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& val, float* out) {
+  constexpr int kW = kFinThreads / kWarp;
+  __shared__ double red[8][kW];
+  __shared__ double S[8];      // the reduced sums
+  __shared__ double A[3][4];   // normal equations | right-hand side
+  __shared__ double coef[3];
+  __shared__ int s_deg;
+  double m[8];  // sums of x^0..x^4, then of y x^0..y x^2
+#pragma unroll
+  for (int q = 0; q < 8; ++q) m[q] = 0.0;
+  for (int i = threadIdx.x; i < Lmax; i += kFinThreads) {
+    const int L = i + 1;
+    if (L <= k || !has(i)) continue;
+    double y = (double)val(i);
+    if (mode == TOPT_POST) {
+      if (!(y > 0.0)) continue;
+      y = log(y);
+    }
+    const double x = log((double)L);
+    double xp = 1.0;
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      m[q] += xp;
+      if (q < 3) m[5 + q] += xp * y;
+      xp *= x;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    double v = m[q];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) red[q][warp] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < 8; ++q) {
+      S[q] = 0.0;
+      for (int w = 0; w < kW; ++w) S[q] += red[q][w];
+    }
+    const int n = (int)(S[0] + 0.5);
+    const int deg = n < 3 ? n - 1 : 2;
+    if (deg >= 0) {
+      // A c = t with A[r][c] = sum x^(r+c), t[r] = sum y x^r; partial pivoting
+      const int sz = deg + 1;
+      for (int r = 0; r < sz; ++r) {
+        for (int c = 0; c < sz; ++c) A[r][c] = S[r + c];
+        A[r][3] = S[5 + r];
+      }
+      for (int c = 0; c < sz; ++c) {
+        int piv = c;
+        for (int r = c + 1; r < sz; ++r)
+          if (fabs(A[r][c]) > fabs(A[piv][c])) piv = r;
+        if (piv != c)
+          for (int e = 0; e < 4; ++e) {
+            const double t = A[c][e];
+            A[c][e] = A[piv][e];
+            A[piv][e] = t;
+          }
+        for (int r = c + 1; r < sz; ++r) {
+          const double f = A[r][c] / A[c][c];
+          for (int e = c; e < 4; ++e) A[r][e] -= f * A[c][e];
+        }
+      }
+      coef[0] = coef[1] = coef[2] = 0.0;
+      for (int r = sz - 1; r >= 0; --r) {
+        double v = A[r][3];
+        for (int e = r + 1; e < sz; ++e) v -= A[r][e] * coef[e];
+        coef[r] = v / A[r][r];
+      }
+    }
+    s_deg = deg;
+  }
+  __syncthreads();
+  const int deg = s_deg;
+  for (int i = threadIdx.x; i < Lmax; i += kFinThreads) {
+    const int L = i + 1;
+    if (L <= k || deg < 0) {
+      out[i] = -CUDART_INF_F;
+      continue;
+    }
+    const double x = log((double)L);
+    const double y = coef[0] + x * (coef[1] + x * coef[2]);
+    out[i] = (float)(mode == TOPT_POST ? exp(y) : y);
+  }
+}
+
 // One CTA per head.
 __global__ void __launch_bounds__(kFinThreads) calib_finalize_kernel(const CalibParams p) {
   const int h = blockIdx.x;
   const int32_t* cnt = p.count + (size_t)h * p.Lmax;
   const auto has = [&](int i) { return cnt[i] > 0; };
   const auto val = [&](int i) { return calib_value(p, (size_t)h * p.Lmax + i); };
-  fill_nearest_rows(p.Lmax, p.k, has, val, p.theta + (size_t)h * p.Lmax);
+  if (p.fit) fit_rows(p.Lmax, p.k, p.mode, has, val, p.theta + (size_t)h * p.Lmax);
+  else fill_nearest_rows(p.Lmax, p.k, has, val, p.theta + (size_t)h * p.Lmax);
 }
 
 // ---------------------------------------------------------------------------
@@ -739,6 +837,7 @@ cudaError_t calibrate_launch(const topt_calib_args& a, cudaStream_t s) {
   p.k = a.k;
   p.h0 = 0;
   p.Hp = a.n_q_heads;
+  p.fit = (a.flags & TOPT_CALIB_FIT) != 0;
   p.alpha = a.alpha;
   p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
   p.q = a.q;
@@ -798,6 +897,7 @@ cudaError_t calibrate_sdc_launch(const topt_sdc_calib_args& a, cudaStream_t s) {
   p.k = 1;
   p.h0 = 0;
   p.Hp = a.n_q_heads;
+  p.fit = 0;
   p.alpha = 0.f;
   p.sm_scale = 1.0f / sqrtf((float)a.head_dim);
   p.q = a.q;
@@ -909,6 +1009,7 @@ cudaError_t calibrate_multik_launch(const topt_mkc_args& a, cudaStream_t s) {
   cp.Lmax = a.theta_len;
   cp.mode = a.mode;
   cp.k = 1;
+  cp.fit = 0;
   cp.alpha = 0.f;
   cp.sm_scale = 1.0f / sqrtf((float)a.head_dim);
   cp.q = a.q;

@@ -19,7 +19,7 @@ PRE, POST = 0, 1
 SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
 GQA_OWN, GQA_UNION, GQA_VOTE = 0, 1, 2
 BF16, F32 = 0, 1
-CALIB_RESET, CALIB_FINALIZE = 1, 2
+CALIB_RESET, CALIB_FINALIZE, CALIB_FIT = 1, 2, 4
 GAMMA = 0.05
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported dtype", 3: "unsupported shape",
@@ -321,11 +321,13 @@ class Calibrator:
     """Accumulators of one layer's calibration [TopTheta §3.1, Algorithm 1].
 
     ``add`` runs topt_calibrate on a batch of calibration sequences; ``finalize``
-    writes and returns theta [Hq][Lmax].
+    writes and returns theta [Hq][Lmax].  ``fit`` makes finalize write the
+    fitted function of ln L (TOPT_CALIB_FIT) instead of the nearest-row fill.
     """
 
-    def __init__(self, n_q_heads, theta_len, k, mode, alpha=0.0, device="cuda"):
+    def __init__(self, n_q_heads, theta_len, k, mode, alpha=0.0, device="cuda", fit=False):
         self.Hq, self.Lmax, self.k, self.mode, self.alpha = n_q_heads, theta_len, k, mode, alpha
+        self.fit = bool(fit)
         self.acc = torch.zeros((2, n_q_heads, theta_len), device=device, dtype=torch.float64)
         self.count = torch.zeros((n_q_heads, theta_len), device=device, dtype=torch.int32)
         self.theta = torch.empty((n_q_heads, theta_len), device=device, dtype=torch.float32)
@@ -359,7 +361,7 @@ class Calibrator:
         _check("topt_calibrate", lib().topt_calibrate(ctypes.byref(a), _stream(stream)))
 
     def finalize(self, status=None, stream=None):
-        a = self._args(None, None, None, CALIB_FINALIZE, status)
+        a = self._args(None, None, None, CALIB_FINALIZE | (CALIB_FIT if self.fit else 0), status)
         _check("topt_calibrate", lib().topt_calibrate(ctypes.byref(a), _stream(stream)))
         return self.theta
 

@@ -204,7 +204,7 @@ topt_status topt_prefill_test_timeout(const topt_prefill_args* args, topt_stream
 /* ------------------------------------------------------------------------ */
 /* Calibration [TopTheta §3.1, Algorithm 1], one layer per call.            */
 /* ------------------------------------------------------------------------ */
-enum { TOPT_CALIB_RESET = 1, TOPT_CALIB_FINALIZE = 2 };
+enum { TOPT_CALIB_RESET = 1, TOPT_CALIB_FINALIZE = 2, TOPT_CALIB_FIT = 4 };
 
 typedef struct {
   int32_t n_seqs;       /* N >= 0 calibration sequences in this call */
@@ -219,7 +219,10 @@ typedef struct {
   int32_t k;            /* target kept elements per row, >= 1 */
   float alpha;          /* offset in standard deviations */
   int32_t flags;        /* TOPT_CALIB_RESET: zero the accumulators first;
-                           TOPT_CALIB_FINALIZE: write theta after accumulating */
+                           TOPT_CALIB_FINALIZE: write theta after accumulating;
+                           TOPT_CALIB_FIT (with FINALIZE): write the fitted
+                           function of ln L described below instead of the
+                           nearest-row fill */
   const void* q;        /* [N][Hq][R][d] */
   const void* keys;     /* [N][Hkv][Nk][d] */
   const int32_t* row_len; /* [R] keys seen by each query row, 1..Nk (causal prefill: r+1) */
@@ -242,7 +245,12 @@ topt_status topt_calibrate_workspace(const topt_calib_args* args, size_t* bytes)
  *   count > 0         mean + alpha * std (std with ddof 1; 0 for one sample)
  *   L <= k            -INFINITY (the row is kept whole)
  *   otherwise         the value of the nearest calibrated L (ties: smaller L);
- *                     -INFINITY if the head has no calibrated row.          */
+ *                     -INFINITY if the head has no calibrated row.
+ * With TOPT_CALIB_FIT every L > k instead takes a least-squares polynomial
+ * of degree min(2, n-1) in ln L through the n calibrated values (PRE), or
+ * exp of one through their logarithms (POST, positive values only); a head
+ * with no usable value is dense.  The paper mentions fitting thresholds as a
+ * function of the sequence length without giving the form. */
 topt_status topt_calibrate(const topt_calib_args* args, topt_stream stream);
 
 /* ------------------------------------------------------------------------ */
