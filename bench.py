@@ -96,6 +96,16 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def max_over_ranks(x, world, dev):
+    """The largest x over the ranks of the job (the slowest replica's time);
+    x itself when the job has one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([float(x)], device=dev, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def source_sha(names):
     h = hashlib.sha256()
     for n in names:
@@ -786,11 +796,7 @@ def main():
     t1 = time.time()
     state.clear_events()
     clk = clocks.stop(t0, t1)
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     if args.eager:
         score_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
         kern_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][2]) for s_ in range(args.steps) for l_ in range(layers)]
@@ -894,11 +900,7 @@ def main_prefill(args, dev, rank, local, world):
     call_s, kern_s, tiles = time_prefill(L, st, stream, args.steps, args.warmup)
     t1 = time.time()
     clk = clocks.stop(t0, t1)
-    ms = float(np.sum(call_s)) * 1e3
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.sum(call_s)) * 1e3, world, dev)
     call = ms / 1e3 / args.steps
     kept_total = float(st.kept.double().sum().item())
     value = kept_elem_flops(wl, kept_total) * world / call / 1e12
@@ -1067,6 +1069,8 @@ def main_mkc(args, dev, rank, local, world):
         for _ in range(args.warmup):
             topt.calibrate_multik(Q, K, row_len, ks, mode, wl.S, theta=theta, status=status, workspace=ws)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize(dev)
         for i in range(args.steps):
             ev[2 * i].record(stream)
@@ -1076,7 +1080,7 @@ def main_mkc(args, dev, rank, local, world):
         ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
         if int(status.item()) != 0:
             raise RuntimeError(f"topt_calibrate_multik status {int(status.item())}")
-        res[name] = float(np.mean(ms))
+        res[name] = max_over_ranks(float(np.mean(ms)), world, dev)
     # offline SDC estimate E~ beside the k = 64 pre-softmax table, same rows
     ki64 = MKC_KS.index(64)
     topt.calibrate_multik(Q, K, row_len, ks, 0, wl.S, theta=theta, status=status, workspace=ws)
@@ -1102,15 +1106,17 @@ def main_mkc(args, dev, rank, local, world):
     sdc_passes = -(-rows_total // min((1 << 30) // (wl.S * 4) // 8 * 8, 65535 * 8))
     line = {
         "metric": "multi-k cumulative calibration: pooled calibration scores per second",
-        "value": pooled / (res["pre"] / 1e3), "unit": "scores/s", "n_gpus": 1, "steps": args.steps,
+        "value": pooled * world / (res["pre"] / 1e3), "unit": "scores/s", "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["pre"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
                    "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS),
                    "heads_per_pass": int(heads_per_pass),
-                   "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call"},
+                   "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call",
+                   "parallelism": f"replicas x{world} (independent calibrations per GPU)"},
         "ms_per_call": res, "pooled_scores": pooled,
-        "post_scores_per_s": pooled / (res["post"] / 1e3),
+        "post_scores_per_s": pooled * world / (res["post"] / 1e3),
         "sdc_offline_calibration": {"ms_per_call": sdc_ms, "table": "k = 64 pre-softmax theta",
                                     "rows": rows_total, "scores_per_s": pooled / (sdc_ms / 1e3)},
         "gpu_launches": args.steps * (launches_pre + launches_post + 2 * sdc_passes + 2),
@@ -1120,6 +1126,8 @@ def main_mkc(args, dev, rank, local, world):
         line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
 
 
 def prefill_e2e(st, args, dev, world):
@@ -1146,11 +1154,7 @@ def prefill_e2e(st, args, dev, world):
     for _ in range(steps):
         step()
     torch.cuda.synchronize(dev)
-    dt_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt_s = float(t.item())
+    dt_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     h2d = sum(h_.numel() * h_.element_size() for h_ in host)
     kept_total = float(st.kept.double().sum().item())
     return {"value": kept_elem_flops(wl, kept_total) * steps * world / dt_s / 1e12, "unit": "TFLOP/s",
@@ -1190,11 +1194,7 @@ def run_e2e(state, args, dev, world):
     for _ in range(steps):
         step()
     torch.cuda.synchronize(dev)
-    dt_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt_s = float(t.item())
+    dt_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     h2d = sum(q_host[l].numel() * 2 + kv_host[l].numel() * 2 for l in range(layers))
     d2h = sum(out_host[l].numel() * 4 for l in range(layers))
     return {"value": wl.B * steps * world / dt_s, "unit": "tokens/s", "steps": steps,
