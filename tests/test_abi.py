@@ -130,3 +130,40 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(topt, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         topt.lib()
+
+
+STRUCTS = {"topt_decode_args": "DecodeArgs", "topt_prefill_args": "PrefillArgs",
+           "topt_calib_args": "CalibArgs", "topt_sdc_calib_args": "SdcCalibArgs",
+           "topt_mkc_args": "MkcArgs", "topt_vmean_args": "VmeanArgs"}
+
+
+def test_header_is_c99_and_binding_layouts_match(tmp_path):
+    """include/topt.h compiles as strict C99, and every argument struct of the
+    ctypes binding has the C struct's size and field offsets."""
+    gcc = "gcc"
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "topt.h"', "int main(void) {"]
+    for cname, pyname in STRUCTS.items():
+        cls = getattr(topt, pyname)
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {}
+    for ln in out:
+        if ln:
+            parts = ln.split()
+            got[(parts[0], parts[1])] = int(parts[2])
+    for cname, pyname in STRUCTS.items():
+        cls = getattr(topt, pyname)
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
