@@ -19,6 +19,8 @@
 // The second half of the file is multi-k cumulative calibration
 // [TopTheta App. D, Algorithm 2]: every threshold table theta(k) of a list of
 // targets k from one pass over the calibration rows.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -965,12 +967,17 @@ cudaError_t mkc_scores(const CalibParams& cp, long total, float* ws, cudaStream_
 }
 
 cudaError_t calibrate_multik_launch(const topt_mkc_args& a, cudaStream_t s) {
-  static bool attr_set = false;
+  // the group kernel's shared-memory limit, raised once per device
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_set[kMaxDevices];
   cudaError_t e;
-  if (!attr_set) {
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev].load()) {
     e = cudaFuncSetAttribute(mkc_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(MkcSmem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev].store(true);
   }
   char* w = static_cast<char*>(a.workspace);
   const size_t lb = align256((size_t)(a.theta_len + 1) * sizeof(int32_t));
