@@ -339,13 +339,16 @@ __device__ void fill_nearest_rows(int Lmax, int k, const Has& has, const Val& va
   }
 }
 
-// One head's row of a threshold table from a least-squares polynomial of
-// degree min(2, n - 1) in x = ln L through the n usable calibrated row ids
-// L > k: y = theta (PRE) or ln theta (POST, theta > 0 only).  Every L > k
-// takes the fitted value (exp of it for POST); L <= k and a head without
-// usable row ids are dense.  The pages mention a fitted function of the
-// sequence length without its form; this is the plainest such fit.  fp64
-// normal equations, solved by one thread (at most 3 x 3).
+// One head's row of a threshold table from a least-squares line (degree
+// min(1, n - 1)) in x = ln L through the n usable calibrated row ids L > k:
+// y = theta (PRE) or ln theta (POST, theta > 0 only).  Every L > k takes the
+// fitted value (exp of it for POST); L <= k and a head without usable row ids
+// are dense.  The pages mention a fitted function of the sequence length
+// without its form; a line in ln L extrapolates past the calibrated lengths
+// far better than a quadratic.  fp64 normal equations (the sums cover a
+// quadratic), solved by one thread.
+constexpr int kFitDegree = 1;  // degree of the fitted polynomial in ln L (at most 2)
+
 template <class Has, class Val>
 __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& val, float* out) {
   constexpr int kW = kFinThreads / kWarp;
@@ -389,7 +392,7 @@ __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& v
       for (int w = 0; w < kW; ++w) S[q] += red[q][w];
     }
     const int n = (int)(S[0] + 0.5);
-    const int deg = n < 3 ? n - 1 : 2;
+    const int deg = n < 2 ? n - 1 : kFitDegree;
     if (deg >= 0) {
       // A c = t with A[r][c] = sum x^(r+c), t[r] = sum y x^r; partial pivoting
       const int sz = deg + 1;

@@ -246,10 +246,10 @@ topt_status topt_calibrate_workspace(const topt_calib_args* args, size_t* bytes)
  *   L <= k            -INFINITY (the row is kept whole)
  *   otherwise         the value of the nearest calibrated L (ties: smaller L);
  *                     -INFINITY if the head has no calibrated row.
- * With TOPT_CALIB_FIT every L > k instead takes a least-squares polynomial
- * of degree min(2, n-1) in ln L through the n calibrated values (PRE), or
- * exp of one through their logarithms (POST, positive values only); a head
- * with no usable value is dense.  The paper mentions fitting thresholds as a
+ * With TOPT_CALIB_FIT every L > k instead takes a least-squares line in
+ * ln L through the n calibrated values (PRE; a constant when n = 1), or exp
+ * of one through their logarithms (POST, positive values only); a head with
+ * no usable value is dense.  The paper mentions fitting thresholds as a
  * function of the sequence length without giving the form. */
 topt_status topt_calibrate(const topt_calib_args* args, topt_stream stream);
 

@@ -46,9 +46,10 @@ reason in the design notes of the repository):
       it is, whatever the row itself keeps.
 * c22 fitted theta(L): the pages mention a function of the sequence length
       fitted to the calibrated thresholds without its form; here a least-
-      squares polynomial of degree min(2, n - 1) in ln L through the n
-      calibrated row ids L > k, fitted to theta (pre) or to ln theta (post,
-      positive values only), and used for every row id L > k.
+      squares line (degree min(1, n - 1)) in ln L through the n calibrated
+      row ids L > k, fitted to theta (pre) or to ln theta (post, positive
+      values only), and used for every row id L > k.  A quadratic in ln L
+      was tried first and extrapolated badly past the calibrated lengths.
 * c21 GQA group policies (§4.6, the two alternatives): UNION gives every head
       of a group the union of the group's kept sets; VOTE keeps a key for a
       head only if the head keeps it and at least t heads of the group do.
@@ -177,8 +178,8 @@ def fit_row_ids(value, Lmax, k, mode):
     calibrated row ids ``value`` (L -> theta), reading c22.
 
     y = theta (PRE) or ln theta (POST, theta > 0 only) is fitted by least
-    squares with a polynomial of degree min(2, n - 1) in x = ln L over the n
-    usable row ids; every L > k takes the fitted value (exp of it for POST),
+    squares with a line (degree min(1, n - 1)) in x = ln L over the n usable
+    row ids; every L > k takes the fitted value (exp of it for POST),
     L <= k stays dense, and a head without usable row ids is dense.
     """
     row = np.full(Lmax, -np.inf)
@@ -189,7 +190,7 @@ def fit_row_ids(value, Lmax, k, mode):
     y = np.array([v for _, v in pts], dtype=np.float64)
     if mode == POST:
         y = np.log(y)
-    deg = min(2, len(pts) - 1)
+    deg = min(1, len(pts) - 1)
     coef = np.polynomial.polynomial.polyfit(x, y, deg)
     Ls = np.arange(k + 1, Lmax + 1, dtype=np.float64)
     fitted = np.polynomial.polynomial.polyval(np.log(Ls), coef)

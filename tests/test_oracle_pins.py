@@ -372,12 +372,12 @@ def test_offline_sdc_one_row_calibration_is_exact_on_that_row():
 
 
 # ---------------------------------------------------------------------------
-# Fitted theta(L) (reading c22): exact recovery of functions of ln L.
+# Fitted theta(L) (reading c22): exact recovery of lines in ln L.
 # ---------------------------------------------------------------------------
 def check_fitted_theta():
     k, Lmax = 3, 200
-    c = (0.7, 0.45, -0.04)
-    f = lambda L: c[0] + c[1] * math.log(L) + c[2] * math.log(L) ** 2
+    c = (0.7, 0.45)
+    f = lambda L: c[0] + c[1] * math.log(L)
     # one calibration row per length, its k-th largest score set to f(L)
     for L in (5, 9, 17, 33, 64, 90):
         row = np.concatenate([f(L) + 1.0 + np.arange(k - 1), [f(L)], f(L) - 1.0 - np.arange(L - k)])
@@ -420,7 +420,7 @@ def check_fitted_theta():
     assert np.all(np.isneginf(ref.finalize_fitted({}, 1, 30, k, 0.0, ref.PRE)))
 
 
-def test_fitted_theta_recovers_functions_of_log_length():
+def test_fitted_theta_recovers_lines_in_log_length():
     check_fitted_theta()
 
 
