@@ -274,7 +274,6 @@ class DecodeState:
             if events is not None:
                 a.events[0] = events[l][0]
                 a.events[1] = events[l][1]
-                a.events[2] = events[l][2]
             rc = L.topt_decode(ctypes.byref(a), stream)
             if rc:
                 raise topt.ToptError("topt_decode", rc)
@@ -283,7 +282,6 @@ class DecodeState:
         for a in self.dargs:
             a.events[0] = None
             a.events[1] = None
-            a.events[2] = None
 
 
 def time_dense(state, L, stream, steps, warmup):
@@ -743,8 +741,8 @@ def main():
     torch.cuda.synchronize(dev)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.eager:
-        # events around the two decode kernels of every layer call of every step
-        ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+        # events around the decode kernel of every layer call of every step
+        ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
               for _ in range(args.steps)]
         for s_ in ev:
             for l_ in s_:
@@ -752,20 +750,17 @@ def main():
                     e.record(stream)
         handles = [[[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in s_] for s_ in ev]
     else:
-        # One step captured as a CUDA graph, twice: `graph` times the whole
-        # decode call of every layer (events before the score kernel and after
-        # the select kernel, which leave the two kernels' overlap intact);
-        # `graph_split` adds an event between them to time the score kernel.
-        def capture(with_split):
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+        # One step captured as a CUDA graph, twice: `graph` is the timed step
+        # (no events inside, so each kernel may start while the previous one
+        # drains); `graph_calls` has events around every decode call and
+        # times the calls alone.
+        def capture(with_events):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
             for l_ in evs:
                 for e in l_:
                     e.record(stream)
             torch.cuda.synchronize(dev)
-            hs = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in evs]
-            if not with_split:
-                for l_ in hs:
-                    l_[1] = None
+            hs = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in evs] if with_events else None
             gr = torch.cuda.CUDAGraph()
             cap = torch.cuda.Stream(dev)
             cap.wait_stream(stream)
@@ -777,8 +772,8 @@ def main():
                 gr.replay()
             torch.cuda.synchronize(dev)
             return gr, evs
-        graph, ev1 = capture(False)
-        graph_split, ev_split = capture(True)
+        graph, _ = capture(False)
+        graph_calls, ev_calls = capture(True)
     barrier()
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -798,29 +793,23 @@ def main():
     clk = clocks.stop(t0, t1)
     ms = max_over_ranks(start.elapsed_time(stop), world, dev)
     if args.eager:
-        score_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
-        kern_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][2]) for s_ in range(args.steps) for l_ in range(layers)]
+        kern_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
     else:
-        # whole calls: the last replay of the timed region; score kernel: a
-        # short run of the split graph right after it
-        kern_ms = [ev1[l_][0].elapsed_time(ev1[l_][2]) for l_ in range(layers)]
-        score_ms = []
+        # the decode calls alone: a short run of the graph with events
+        kern_ms = []
         for _ in range(max(5, args.steps // 20)):
-            graph_split.replay()
+            graph_calls.replay()
             torch.cuda.synchronize(dev)
-            score_ms += [ev_split[l_][0].elapsed_time(ev_split[l_][1]) for l_ in range(layers)]
+            kern_ms += [ev_calls[l_][0].elapsed_time(ev_calls[l_][1]) for l_ in range(layers)]
     ms_per_step = ms / args.steps
     tokens = wl.B * args.steps * world
     value = tokens / (ms / 1e3)
 
     k_bytes, per_layer = algorithmic_bytes(state)
     kern_avg = float(np.mean(kern_ms)) / 1e3
-    score_avg = float(np.mean(score_ms)) / 1e3
     peak, peak_kind = hbm_peak()
     alg_bytes = float(np.mean(per_layer))
-    q_bytes = wl.B * wl.Hq * wl.d * 2
-    achieved = (k_bytes + q_bytes) / score_avg / 1e9
-    call_gbs = alg_bytes / kern_avg / 1e9
+    achieved = alg_bytes / kern_avg / 1e9
     traffic = recorded_traffic(DECODE_TRAFFIC)
     vrows_per_group = float(np.mean([state.vrows[l].double().mean().item() for l in range(layers)]))
 
@@ -841,23 +830,18 @@ def main():
                          f"{k_bytes / 1e6:.0f} MB K cache",
                    "parallelism": f"replicas x{world} (independent sequences per GPU)",
                    "launch": "eager host launches" if args.eager else "one step replayed as a CUDA graph"},
-        "roofline": {"bound": "hbm", "kernel": "decode_scores_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": traffic,
-                     "algorithmic_bytes_per_launch": k_bytes + q_bytes,
-                     "bytes": "whole K cache + q",
-                     "avg_launch_ms": score_avg * 1e3},
-        "decode_call": {"gbs": call_gbs, "frac_of_measured": call_gbs / peak,
-                        "frac_of_8tbs": call_gbs / NOMINAL_HBM_GBS, "avg_ms": kern_avg * 1e3,
-                        "select_avg_ms": (kern_avg - score_avg) * 1e3,
-                        "bytes_per_call": alg_bytes,
-                        "bytes": "whole K cache + union V rows + theta entries + q, mu, out"},
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "bytes": "whole K cache + union V rows + theta entries + q, mu, out",
+                     "avg_launch_ms": kern_avg * 1e3},
         "vrows_per_group": vrows_per_group,
         "kept_over_k": kept_ratio_by_bucket(state),
-        "gpu_launches": args.steps * layers * 2,
+        "gpu_launches": args.steps * layers * 2,   # vmean + decode per layer
         "clocks": clk,
     }
     if e2e is not None:

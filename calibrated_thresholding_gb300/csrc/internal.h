@@ -11,8 +11,7 @@ namespace topt {
 
 // ------------------------------------------------------------------ decode
 size_t decode_workspace_bytes(const topt_decode_args& a);
-int decode_max_batch();
-int decode_max_pairs();
+long decode_max_pairs();
 cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s);
 size_t decode_noalloc_capacity();
 cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s);

@@ -35,6 +35,11 @@ __global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int 
   constexpr int LPR = D / 8;
   constexpr int RL = kThreads / LPR;  // row lanes
   __shared__ float red[RL][D];
+  // Launched so that it may start while the previous kernel of the stream
+  // drains: wait for that kernel's writes, then let the next kernel be
+  // scheduled (it waits for this one in turn).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int pair = blockIdx.x;
   const int b = pair / Hkv;
   const int n0 = n_old[b];
@@ -67,12 +72,20 @@ __global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int 
 template <typename T>
 cudaError_t launch_t(const topt_vmean_args& a, cudaStream_t s) {
   const T* v = static_cast<const T*>(a.v_cache);
-  const unsigned grid = (unsigned)(a.batch * a.n_kv_heads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.batch * a.n_kv_heads));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a.head_dim == 128)
-    vmean_kernel<T, 128><<<grid, kThreads, 0, s>>>(a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu, a.status);
-  else
-    vmean_kernel<T, 64><<<grid, kThreads, 0, s>>>(a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu, a.status);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 128>, a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu,
+                              a.status);
+  return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 64>, a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu,
+                            a.status);
 }
 
 }  // namespace

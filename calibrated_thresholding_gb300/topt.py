@@ -199,8 +199,8 @@ def decode_workspace_bytes(a: DecodeArgs) -> int:
 
 
 def decode_workspace(a: DecodeArgs, device) -> torch.Tensor:
-    """A zero-filled workspace for topt_decode (its counters start at zero)."""
-    return torch.zeros(decode_workspace_bytes(a), device=device, dtype=torch.uint8)
+    """A workspace for topt_decode (it needs no initialisation)."""
+    return torch.empty(decode_workspace_bytes(a), device=device, dtype=torch.uint8)
 
 
 def decode(q, k_cache, v_cache, seq_len, theta, *, mode, sdc=SDC_NONE, vmc=False, mu=None,

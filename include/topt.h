@@ -88,9 +88,9 @@ typedef enum { TOPT_GQA_OWN = 0, TOPT_GQA_UNION = 1, TOPT_GQA_VOTE = 2 } topt_gq
 /* [TopTheta §2.2 (generative decoding), Fig. 1, §3.2, §4.6 (GQA)]          */
 /* ------------------------------------------------------------------------ */
 typedef struct {
-  int32_t batch;        /* B, 1 .. 256 */
+  int32_t batch;        /* B >= 1 */
   int32_t n_q_heads;    /* Hq */
-  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 8, B * Hkv <= 16382 */
+  int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 8, B * Hkv <= 2^26 */
   int32_t head_dim;     /* d: 64 or 128 */
   int32_t cache_len;    /* Nmax >= 1: token capacity of each cache */
   int32_t theta_len;    /* Lmax >= 1: entries per head of `theta` */
@@ -111,17 +111,17 @@ typedef struct {
   int32_t* vrows;       /* [B][Hkv] V rows read (union over the group), or NULL */
   uint32_t* mask;       /* [B][Hq][ceil(Nmax/32)] kept bitmap (bit j%32 of word j/32), or NULL */
   int32_t* status;      /* device-side error word, or NULL */
-  /* Scratch, >= topt_decode_workspace() bytes, 256-byte aligned.  Its first
-   * 128 KiB hold work counters that must be zero before the first call; every
-   * call that runs to completion leaves them zero again, so one zero-filled
-   * workspace serves any number of calls and shapes. */
+  /* Scratch, >= topt_decode_workspace() bytes, 256-byte aligned: the fp32
+   * scores of the call ([B][Hkv][Nmax rounded up to 32][G rounded up to
+   * even]).  Every score is written before it is read, so the contents need
+   * no initialisation and one workspace serves any number of calls. */
   void* workspace;
   size_t workspace_bytes;
   /* Optional profiling hook: cudaEvent_t handles (or NULL) recorded on
-   * `stream` before the score kernel [0], between the score and the select
-   * kernel [1] and after the select kernel [2].  An event between the two
-   * kernels keeps the select kernel from being scheduled early, so leave [1]
-   * NULL unless the split is wanted. */
+   * `stream` right before [0] and right after [1] the decode kernel; [2] is
+   * not used.  The call is one kernel, launched so that it may start while
+   * the previous kernel of the stream drains; an event in between removes
+   * that overlap. */
   void* events[3];
   int32_t gqa_policy;     /* topt_gqa_policy; 0 (OWN) when zero-initialised */
   int32_t gqa_min_heads;  /* TOPT_GQA_VOTE: t >= 1 heads (t = 1 is OWN); else ignored */
@@ -133,7 +133,8 @@ topt_status topt_decode_workspace(const topt_decode_args* args, size_t* bytes);
 /* out[b][h] = Top-theta attention of q[b][h] over keys 0..seq_len[b]-1 of
  * KV head h / (Hq/Hkv).  The whole K row range is read; only V rows kept by
  * at least one head of the group are read.  Masked bits beyond seq_len[b]
- * are written as 0. */
+ * are written as 0.  A sequence with seq_len[b] outside 1..Nmax sets *status
+ * to TOPT_EINVAL and leaves its outputs untouched. */
 topt_status topt_decode(const topt_decode_args* args, topt_stream stream);
 
 /* Same operation as topt_decode, for callers that cannot allocate device
@@ -147,8 +148,11 @@ topt_status topt_decode(const topt_decode_args* args, topt_stream stream);
  *     32 MiB (topt_decode_workspace) return TOPT_EWORKSPACE and launch nothing.
  *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
  *     call.  The first call on a device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture.  Each call clears the array's counters on `stream` first.
+ *     (with that device current) and keeps it for the life of the process;
+ *     make that first call before any stream capture, and do not use this
+ *     entry point across a cudaDeviceReset of that device.  The array keeps
+ *     the previous call's contents; the kernel writes every value it reads,
+ *     so nothing has to be cleared between calls.
  *   - Every call on a device shares the one array: calls that overlap on the
  *     GPU (other streams, other threads) race and corrupt each other's
  *     results.  Serialise them. */

@@ -184,7 +184,7 @@ def test_decode_reuses_workspace():
     for _ in range(3):
         b = topt.decode(q, K, V, seq_len, theta, mode=ref.POST, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(first, b["out"])              # deterministic, counters reset
+    assert torch.equal(first, b["out"])              # deterministic: no state kept between calls
 
 
 # ---------------------------------------------------------------------------

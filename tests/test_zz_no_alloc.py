@@ -5,7 +5,7 @@ set at start-up, or a host framework whose allocator owns all device memory);
 this entry point uses a scratch array the library holds instead of a caller
 workspace.  Its results must match topt_decode's on the same inputs, on two
 calls in a row (the array keeps the previous call's contents, so the second
-call checks that the entry point clears what must start at zero).
+call checks that nothing left over from the first one leaks into it).
 
 The file name puts it last in collection order, so a run that stops at the
 first failure has already run every other test.
