@@ -29,6 +29,7 @@ topt_status check_decode_shape(const topt_decode_args* a) {
   if (a->n_q_heads % a->n_kv_heads != 0) return TOPT_ESHAPE;
   if (a->n_q_heads / a->n_kv_heads > 8) return TOPT_ESHAPE;
   if ((long)a->batch * a->n_kv_heads > decode_max_pairs()) return TOPT_ESHAPE;
+  if (a->cache_len > decode_max_cache()) return TOPT_ESHAPE;
   if (a->gqa_policy < TOPT_GQA_OWN || a->gqa_policy > TOPT_GQA_VOTE) return TOPT_EINVAL;
   if (a->gqa_policy == TOPT_GQA_VOTE && a->gqa_min_heads < 1) return TOPT_EINVAL;
   return check_common_mode(a->mode, a->sdc);

@@ -18,20 +18,19 @@
 //     bf16 MMAs (keys on M, query heads on N), writes a = q K^T / sqrt(d)
 //     [Eq. 1] to an L2-resident scratch row and keeps a running softmax
 //     partial (m, Z) per head;
-//  2. publishes its (m, Z) in shared memory; after a cluster barrier every
-//     CTA merges the C partials in rank order (identical bits everywhere) and
-//     turns theta into a bound on the score (post-softmax:
+//  2. writes its (m, Z) into every CTA's shared memory; after a cluster
+//     barrier every CTA merges the C partials in rank order (identical bits
+//     everywhere) and turns theta into a bound on the score (post-softmax:
 //     s >= theta <=> a >= m + ln theta + ln Z);
 //  3. per warp, re-reads its own units' scores, ballots the per-head masks,
 //     applies the GQA group policy, compacts the group's union into a list
 //     with each kept key's weights exp(a - m), gathers only those V rows and
 //     accumulates sum exp(a - m) v per head; the score lines are dropped from
 //     L2 once read (never written back);
-//  4. reduces its warps' sums; after a second cluster barrier every CTA reads
-//     the C partials of its share of the outputs through distributed shared
-//     memory (summed in rank order), applies SDC [Eq. 4] and VMC [Eq. 5-7]
-//     and writes them; a third barrier keeps every CTA's shared memory alive
-//     until its peers have read it.
+//  4. reduces its warps' sums and writes each slice of them into the shared
+//     memory of the CTA that owns that slice of the outputs; after a second
+//     cluster barrier every CTA sums the C partials of its slice (rank
+//     order), applies SDC [Eq. 4] and VMC [Eq. 5-7] and writes the outputs.
 //
 // Nothing waits on another grid or on a flag: the only waits are cp.async
 // groups and cluster barriers that every CTA of a cluster reaches through the
@@ -53,6 +52,9 @@ constexpr int kUnit = 32;         // keys per unit: one mask word, one ballot
 constexpr int kMaxDevices = 64;
 constexpr int kMinUnitsPerCta = 8;  // a CTA of a cluster gets at least 256 keys
 constexpr int kMaxCluster = 16;
+// A union list entry packs the key (below 2^24) with its per-head keep bits.
+constexpr int kKeyBits = 24;
+constexpr unsigned kKeyMask = (1u << kKeyBits) - 1u;
 
 // Score columns per key in the scratch: G rounded up to even (8-byte stores).
 __host__ __device__ constexpr int score_cols(int G) { return G == 1 ? 1 : (G + 1) / 2 * 2; }
@@ -61,17 +63,22 @@ __host__ __device__ constexpr int score_cols(int G) { return G == 1 ? 1 : (G + 1
 constexpr int kWarpSmem = 12288;
 template <int D>
 __host__ __device__ constexpr int ring_stages() { return kWarpSmem / (kTile * D * 2); }
-// Select state: a ring of kBatches score batches (kBatches - 1 in flight) and
-// the union list (key, G weights).  A batch is batch_units 32-key units.
-constexpr int kBatches = 4;
+// Select state: a ring of kBatches candidate batches (all in flight before the
+// cluster barrier, each refilled once consumed) and the union list (key, G
+// weights).  A batch holds batch_units * 32 candidates.
+constexpr int kBatches = 3;
 template <int G>
 __host__ __device__ constexpr int batch_units() { return score_cols(G) <= 2 ? 8 : (score_cols(G) <= 4 ? 4 : 2); }
 template <int G>
 __host__ __device__ constexpr int batch_floats() { return batch_units<G>() * kUnit * score_cols(G); }
 template <int G>
 __host__ __device__ constexpr int list_cap() {
-  return (kWarpSmem - kBatches * batch_floats<G>() * 4) / (4 + 4 * G) / 32 * 32;
+  return (kWarpSmem - kBatches * (batch_floats<G>() + batch_units<G>() * kUnit) * 4) / (4 + 4 * G) / 32 * 32;
 }
+// A post-softmax candidate needs a >= lse + ln theta - kLogSlack for the largest
+// log-sum-exp that a warp of the cluster had reached over its keys so far; the
+// slack keeps rounding from dropping a key the exact test keeps.
+constexpr float kLogSlack = 1.0f / 1024.0f;
 // Gather layout: VEC d-values (VEC * 2 bytes) per lane, G * VEC accumulators,
 // 16 V rows in flight per warp.
 template <int G>
@@ -94,14 +101,20 @@ struct DecodeParams {
   int32_t* vrows;
   uint32_t* mask;
   int32_t* status;
-  float* scores;         // scratch [pairs][nstride][score_cols(G)]
+  float* scores;         // scratch [pairs][nstride][score_cols(G)]: each warp's candidates, compacted
+  int32_t* cidx;         // scratch [pairs][nstride]: their key indices
 };
 
-size_t scratch_bytes(const topt_decode_args& a) {
+size_t scores_bytes(const topt_decode_args& a) {
   const size_t pairs = (size_t)a.batch * a.n_kv_heads;
   const int G = a.n_q_heads / a.n_kv_heads;
   const size_t nstride = (size_t)(a.cache_len + kUnit - 1) / kUnit * kUnit;
   return align256(pairs * nstride * score_cols(G) * sizeof(float));
+}
+size_t scratch_bytes(const topt_decode_args& a) {
+  const size_t pairs = (size_t)a.batch * a.n_kv_heads;
+  const size_t nstride = (size_t)(a.cache_len + kUnit - 1) / kUnit * kUnit;
+  return scores_bytes(a) + align256(pairs * nstride * sizeof(int32_t));
 }
 
 // ------------------------------------------------------------ PTX helpers --
@@ -149,15 +162,14 @@ __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ int ld_peer_s32(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_peer_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_v2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -169,6 +181,40 @@ __device__ __forceinline__ void ms_add2(float& m, float& z, float x0, float x1) 
   const float mn = fmaxf(m, mt);
   z = z * __expf(m - mn) + __expf(x0 - mn) + __expf(x1 - mn);
   m = mn;
+}
+
+// Order-preserving map of floats to unsigned ints (for an integer max).
+__device__ __forceinline__ unsigned fkey(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float funkey(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ void red_max_peer(uint32_t addr, unsigned v) {
+  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_peer_u32(uint32_t addr) {
+  unsigned v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bit g (g = 0..7) set iff any of bits 4g .. 4g+3 of b is set: from a ballot
+// over lanes 4g + t to one bit per key row g of an MMA tile.
+__device__ __forceinline__ unsigned quad_any(unsigned b) {
+  b |= b >> 1;
+  b |= b >> 2;
+  b &= 0x11111111u;
+  b = (b | (b >> 3)) & 0x03030303u;
+  b = (b | (b >> 6)) & 0x000F000Fu;
+  return (b | (b >> 12)) & 0xFFu;
 }
 
 // VEC consecutive bf16 of a V row as floats (VEC = 8: 16 bytes, 4: 8 bytes).
@@ -190,9 +236,10 @@ __device__ __forceinline__ void ld_vrow(const __nv_bfloat16* p, uint32_t (&w)[VE
 template <int G>
 union WarpSel {
   struct {
-    float sc[kBatches][batch_floats<G>()];  // score batches [key][column]
-    int j[list_cap<G>()];                   // union keys
-    float w[list_cap<G>()][G];              // their weights exp(a - m), 0 for a head that drops the key
+    float sc[kBatches][batch_floats<G>()];          // candidate scores [entry][column]
+    int ci[kBatches][batch_units<G>() * kUnit];     // candidate keys
+    int j[list_cap<G>()];                           // union keys
+    float w[list_cap<G>()][G];                      // their weights exp(a - m), 0 for a head that drops the key
   } s;
   unsigned char raw[kWarpSmem];             // exactly one warp's ring
 };
@@ -205,14 +252,18 @@ struct DecodeSmem {
     float acc[kWarps][G][D];                                      // then per-warp sums; acc[0] the CTA's
   } u;
   float wm[kWarps][G], wz[kWarps][G];  // per-warp softmax partials
-  float cm[G], cz[G];                  // this CTA's partial, read by the cluster
   float M[G], Z[G], T[G], th[G];       // the row's statistics, bounds, thresholds
   float wr[kWarps][G];
   int wk[kWarps][G], wn[kWarps];
-  float R[G];                          // this CTA's sums, read by the leader
-  int KT[G], NU;
-  float Rt[G];                         // the leader's totals
+  float Rt[G];                         // the row's totals
   int Kt[G];
+  unsigned clse[G];                    // leader only: the largest warp log-sum-exp so far (fkey)
+  // written by the cluster's CTAs into each other's shared memory:
+  float2 pstat[kMaxCluster][G];        // (m, Z) per head of every CTA
+  float rnum[G * D];                   // partial sums of this CTA's share of the outputs, by source CTA
+  float rR[kMaxCluster][G];            // R per head of every CTA
+  int rK[kMaxCluster][G];              // kept keys per head of every CTA
+  int rN[kMaxCluster];                 // (rank 0) union rows of every CTA
 };
 
 // ----------------------------------------------------------------------------
@@ -239,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   constexpr int NS = ring_stages<D>();
   constexpr int BU = batch_units<G>();
   constexpr int BF = batch_floats<G>();
+  constexpr int BK = BU * kUnit;                    // candidates per batch
   constexpr int kChunksB = BF * 4 / 16 / kWarp;     // 16-byte copies per lane per score batch
+  constexpr int kChunksI = (BK * 4 / 16 + kWarp - 1) / kWarp;  // ... per index batch
   constexpr int UNR = gather_unroll<G>();
   constexpr int VEC = gather_vec<G>();
   constexpr int LPR = D / VEC;                      // lanes per V row
@@ -263,7 +316,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
     if (crank == 0 && threadIdx.x == 0) set_status(p.status, TOPT_EINVAL);
     return;
   }
-  if (threadIdx.x < G) sm.th[threadIdx.x] = p.theta[(size_t)(kvh * G + threadIdx.x) * p.Lmax + (min(L, p.Lmax) - 1)];
+  if (threadIdx.x < G) {
+    sm.th[threadIdx.x] = p.theta[(size_t)(kvh * G + threadIdx.x) * p.Lmax + (min(L, p.Lmax) - 1)];
+    sm.clse[threadIdx.x] = fkey(-CUDART_INF_F);
+  }
+  // the leader's bound slots are initialised before any CTA of the cluster
+  // touches them (waited for after the first tile)
+  cluster_arrive();
 
   // Units of the row, of this CTA and of this warp.
   const int nunits = (L + kUnit - 1) / kUnit;
@@ -282,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   const int g = lane >> 2;
   const int t = lane & 3;
   const int h0 = 2 * t, h1 = 2 * t + 1;
-  float* srow = p.scores + (size_t)pair * p.nstride * GC;
+  // this warp's candidate region of the scratch: one entry per key it streams
+  float* cscore = p.scores + ((size_t)pair * p.nstride + (size_t)wu0 * kUnit) * GC;
+  int32_t* ckey = p.cidx + (size_t)pair * p.nstride + (size_t)wu0 * kUnit;
+  int ncand = 0;  // candidates of this warp (warp-uniform)
   {
     const __nv_bfloat16* kbase = p.k + (size_t)pair * p.Nmax * D;
     const uint64_t pol_k = l2_evict_first_policy();
@@ -302,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       cp_async_commit();
     };
 #pragma unroll
-    for (int s = 0; s < NS - 1; ++s) {
+    for (int s = 0; s < NS; ++s) {  // every slot in flight
       if (t0 + s < t1) issue(t0 + s, s);
       else cp_async_commit();
     }
@@ -319,13 +381,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       for (int pp = 0; pp < NP; ++pp) qf[pp][0] = qf[pp][1] = qf[pp][2] = qf[pp][3] = 0u;
     }
     const float scale = p.sm_scale;
+    const bool pre = p.mode == TOPT_PRE;
+    const float th0 = h0 < G ? sm.th[h0] : 0.f;
+    const float th1 = h1 < G ? sm.th[h1] : 0.f;
+    // every key is a candidate of a post-softmax head whose threshold is <= 0
+    const bool all0 = !pre && !(th0 > 0.f), all1 = !pre && !(th1 > 0.f);
+    const float lth0 = all0 ? 0.f : __logf(th0) - kLogSlack, lth1 = all1 ? 0.f : __logf(th1) - kLogSlack;
+    // cluster-wide bound: slots of heads h0, h1 in the leader CTA
+    const uint32_t slot0 = peer_addr(&sm.clse[h0 < G ? h0 : 0], 0);
+    const uint32_t slot1 = peer_addr(&sm.clse[h1 < G ? h1 : 0], 0);
+    float bl0 = -CUDART_INF_F, bl1 = -CUDART_INF_F;        // candidate bounds on a (post-softmax)
+    unsigned pend0 = fkey(-CUDART_INF_F), pend1 = pend0;  // the cluster's largest lse, last read
+    bool waited = false;
     float m0 = -CUDART_INF_F, z0 = 0.f, m1 = -CUDART_INF_F, z1 = 0.f;
     int slot = 0;
     for (int tile = t0; tile < t1; ++tile) {
-      // keep NS-1 copies ahead: refill the slot consumed last iteration
-      if (tile + NS - 1 < t1) issue(tile + NS - 1, (slot + NS - 1) % NS);
-      else cp_async_commit();
-      cp_async_wait<NS - 1>();
+      cp_async_wait<NS - 1>();  // this tile has landed
       __syncwarp();
       const unsigned char* tb = &sm.u.ring[warp][slot][0];
       uint4 ka[NP], kb[NP];
@@ -334,7 +405,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
         ka[pp] = *reinterpret_cast<const uint4*>(tb + (size_t)g * D * 2 + (32 * pp + 8 * t) * 2);
         kb[pp] = *reinterpret_cast<const uint4*>(tb + (size_t)(g + 8) * D * 2 + (32 * pp + 8 * t) * 2);
       }
-      __syncwarp();  // the slot may be refilled from here on
+      __syncwarp();  // the tile is in registers: refill its slot before the math
+      if (tile + NS < t1) issue(tile + NS, slot);
+      else cp_async_commit();
       float cs[NP][4];
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) {
@@ -362,48 +435,110 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       const float a01 = j0 < L ? cc[1] * scale : -CUDART_INF_F;
       const float a10 = j1 < L ? cc[2] * scale : -CUDART_INF_F;
       const float a11 = j1 < L ? cc[3] * scale : -CUDART_INF_F;
-      if constexpr (G == 1) {
-        if (t == 0) {
-          if (j0 < L) st_hint_f32(srow + j0, a00, pol_s);
-          if (j1 < L) st_hint_f32(srow + j1, a10, pol_s);
-        }
-      } else if (h0 < G) {
-        if (j0 < L) st_hint_v2(srow + (size_t)j0 * GC + h0, a00, a01, pol_s);
-        if (j1 < L) st_hint_v2(srow + (size_t)j1 * GC + h0, a10, a11, pol_s);
+      ms_add2(m0, z0, a00, a10);  // this lane's partial of heads h0, h1
+      ms_add2(m1, z1, a01, a11);
+      // Candidates: a key some head may keep.  The log-sum-exp of any subset
+      // of the row's keys is at most the row's, so a key below such a bound
+      // [post: s >= theta <=> a >= m + ln Z + ln theta] fails the row's bound
+      // too; pre-softmax compares with theta itself.
+      bool c0 = false, c1 = false;
+      if (h0 < G) {
+        c0 = pre ? a00 >= th0 : a00 >= bl0;
+        c1 = pre ? a10 >= th0 : a10 >= bl0;
       }
-      if (h0 < G) ms_add2(m0, z0, a00, a10);
-      if (h1 < G) ms_add2(m1, z1, a01, a11);
+      if (h1 < G) {
+        c0 = c0 || (pre ? a01 >= th1 : a01 >= bl1);
+        c1 = c1 || (pre ? a11 >= th1 : a11 >= bl1);
+      }
+      const int done = tile - t0 + 1;
+      if (!pre && (done <= 2 || (done & 3) == 0)) {
+        // Refresh the bound from this warp's log-sum-exp so far and the largest
+        // one the cluster had published at the previous refresh; publish ours.
+        if (!waited) {
+          cluster_wait();
+          waited = true;
+        }
+        float wm0 = m0, wz0 = z0, wm1 = m1, wz1 = z1;
+        ms_warp_merge(wm0, wz0, 4);
+        ms_warp_merge(wm1, wz1, 4);
+        const float own0 = wm0 + __logf(wz0), own1 = wm1 + __logf(wz1);
+        const float cl0 = __shfl_sync(0xffffffffu, funkey(pend0), t);
+        const float cl1 = __shfl_sync(0xffffffffu, funkey(pend1), t);
+        bl0 = all0 ? -CUDART_INF_F : fmaxf(own0, cl0) + lth0;
+        bl1 = all1 ? -CUDART_INF_F : fmaxf(own1, cl1) + lth1;
+        if (g == 0) {
+          if (h0 < G) {
+            red_max_peer(slot0, fkey(own0));
+            pend0 = ld_peer_u32(slot0);
+          }
+          if (h1 < G) {
+            red_max_peer(slot1, fkey(own1));
+            pend1 = ld_peer_u32(slot1);
+          }
+        }
+      }
+      const unsigned tmask = quad_any(__ballot_sync(0xffffffffu, c0 && j0 < L)) |
+                             (quad_any(__ballot_sync(0xffffffffu, c1 && j1 < L)) << 8);
+      if (tmask) {  // warp-uniform: store the tile's candidates, compacted in key order
+        const bool k0 = (tmask >> g) & 1u, k1 = (tmask >> (g + 8)) & 1u;
+        const int r0 = ncand + __popc(tmask & ((1u << g) - 1u));
+        const int r1 = ncand + __popc(tmask & ((1u << (g + 8)) - 1u));
+        if constexpr (G == 1) {
+          if (t == 0) {
+            if (k0) st_hint_f32(cscore + r0, a00, pol_s);
+            if (k1) st_hint_f32(cscore + r1, a10, pol_s);
+          }
+        } else if (h0 < G) {
+          if (k0) st_hint_v2(cscore + (size_t)r0 * GC + h0, a00, a01, pol_s);
+          if (k1) st_hint_v2(cscore + (size_t)r1 * GC + h0, a10, a11, pol_s);
+        }
+        if (t == 0) {
+          if (k0) ckey[r0] = j0;
+          if (k1) ckey[r1] = j1;
+        }
+        ncand += __popc(tmask);
+      }
       slot = (slot + 1) % NS;
     }
     cp_async_wait<0>();
-    // this warp's partial per head: lanes with the same t hold the same heads
-    ms_warp_merge(m0, z0, 4);
+    if (!waited) cluster_wait();  // pairs the arrive at the start
+    ms_warp_merge(m0, z0, 4);     // this warp's partial per head: lanes with the same t
     ms_warp_merge(m1, z1, 4);
     if (g == 0) {
       if (h0 < G) { sm.wm[warp][h0] = m0; sm.wz[warp][h0] = z0; }
       if (h1 < G) { sm.wm[warp][h1] = m1; sm.wz[warp][h1] = z1; }
     }
   }
-  // This warp's ring is drained: its first score batches go into the same
+  // This warp's ring is drained: its first candidate batches go into the same
   // bytes now and travel while the cluster exchanges the row statistics.
-  const int nbatch = (wu1 - wu0 + BU - 1) / BU;
+  const int nbatch = (ncand + BK - 1) / BK;
   WarpSel<G>& ws = sm.u.sel[warp];
   const uint64_t pol_b = l2_evict_first_policy();
-  auto fetch = [&](int bi) {  // batch bi of this warp's units into slot bi % kBatches
-    const int bu = wu0 + bi * BU;
-    const int bytes = min(BU, wu1 - bu) * kUnit * GC * 4;
-    const char* src = reinterpret_cast<const char*>(srow + (size_t)bu * kUnit * GC);
+  auto fetch = [&](int bi) {  // candidates [bi * BK, ..) into slot bi % kBatches
+    const int n = min(BK, ncand - bi * BK);
+    const int sbytes = n * GC * 4, ibytes = n * 4;
+    const char* src = reinterpret_cast<const char*>(cscore + (size_t)bi * BK * GC);
     const uint32_t dst = smem_u32(&ws.s.sc[bi % kBatches][0]);
 #pragma unroll
     for (int i = 0; i < kChunksB; ++i) {
       const int off = (i * kWarp + lane) * 16;
-      const bool ok = off < bytes;
-      cp_async16(dst + off, src + (ok ? off : 0), ok ? 16u : 0u, pol_b);
+      const int nb = min(max(sbytes - off, 0), 16);  // the rest of the 16 bytes reads as 0
+      cp_async16(dst + off, src + (nb ? off : 0), (unsigned)nb, pol_b);
+    }
+    const char* isrc = reinterpret_cast<const char*>(ckey + (size_t)bi * BK);
+    const uint32_t idst = smem_u32(&ws.s.ci[bi % kBatches][0]);
+#pragma unroll
+    for (int i = 0; i < kChunksI; ++i) {
+      const int off = (i * kWarp + lane) * 16;
+      if (off < BK * 4) {
+        const int nb = min(max(ibytes - off, 0), 16);
+        cp_async16(idst + off, isrc + (nb ? off : 0), (unsigned)nb, pol_b);
+      }
     }
   };
-  __syncwarp();  // every lane's score stores come before any lane's copy of them
+  __syncwarp();  // every lane's candidate stores come before any lane's copy of them
 #pragma unroll
-  for (int bi = 0; bi < kBatches - 1; ++bi) {
+  for (int bi = 0; bi < kBatches; ++bi) {
     if (bi < nbatch) fetch(bi);
     cp_async_commit();
   }
@@ -414,26 +549,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
     float mm = -CUDART_INF_F, zz = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) ms_merge(mm, zz, sm.wm[w][h], sm.wz[w][h]);
-    sm.cm[h] = mm;
-    sm.cz[h] = zz;
+    for (uint32_t r = 0; r < csize; ++r) st_peer_v2(peer_addr(&sm.pstat[crank][h], r), mm, zz);
   }
-  cluster_sync();  // #1: every CTA's partial is published
+  cluster_sync();  // #1: every CTA's partial is in every CTA's shared memory
 
   // ---------------------------------------------------- row statistics
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
-    float pm[kMaxCluster], pz[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {  // every load in flight before the first use
-      if (r < (int)csize) {
-        pm[r] = ld_peer_f32(peer_addr(&sm.cm[h], r));
-        pz[r] = ld_peer_f32(peer_addr(&sm.cz[h], r));
-      }
-    }
     float mm = -CUDART_INF_F, zz = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)  // rank order: the same bits in every CTA
-      if (r < (int)csize) ms_merge(mm, zz, pm[r], pz[r]);
+    for (uint32_t r = 0; r < csize; ++r)  // rank order: the same bits in every CTA
+      ms_merge(mm, zz, sm.pstat[r][h].x, sm.pstat[r][h].y);
     sm.M[h] = mm;
     sm.Z[h] = zz;
     sm.T[h] = score_bound(p.mode, sm.th[h], mm, zz);
@@ -462,59 +587,81 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
   const __nv_bfloat16* vbase = p.v + (size_t)pair * p.Nmax * D + dl * VEC;
   int* jl = ws.s.j;
   float (*wl)[G] = ws.s.w;
-  auto gather = [&]() {  // accumulate the listed V rows, then empty the list
-    __syncwarp();
-    for (int r0 = 0; r0 < cnt; r0 += RPI * UNR) {
-      uint32_t vv[UNR][VEC / 2];
+  // Accumulates union list entry r of warp w: its V row times each head's
+  // weight; with a mask, one lane of the row sets the row's kept bits.
+  auto gather_rows = [&](int w, int r0, int n) {  // entries [r0, r0 + RPI * UNR) below n
+    const int* jw = sm.u.sel[w].s.j;
+    const float (*ww)[G] = sm.u.sel[w].s.w;
+    uint32_t vv[UNR][VEC / 2];
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int r = r0 + u * RPI + rsub;
-        if (r < cnt) ld_vrow<VEC>(vbase + (size_t)jl[r] * D, vv[u]);
-      }
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * RPI + rsub;
+      if (r < n) ld_vrow<VEC>(vbase + (size_t)(jw[r] & kKeyMask) * D, vv[u]);
+    }
 #pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const int r = r0 + u * RPI + rsub;
-        if (r < cnt) {
-          float vf[VEC];
+    for (int u = 0; u < UNR; ++u) {
+      const int r = r0 + u * RPI + rsub;
+      if (r < n) {
+        float vf[VEC];
 #pragma unroll
-          for (int e = 0; e < VEC / 2; ++e) {
-            vf[2 * e] = bf16lo(vv[u][e]);
-            vf[2 * e + 1] = bf16hi(vv[u][e]);
-          }
+        for (int e = 0; e < VEC / 2; ++e) {
+          vf[2 * e] = bf16lo(vv[u][e]);
+          vf[2 * e + 1] = bf16hi(vv[u][e]);
+        }
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float wh = wl[r][h];
+        for (int h = 0; h < G; ++h) {
+          const float wh = ww[r][h];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
-          }
+          for (int e = 0; e < VEC; ++e) acc[h][e] = fmaf(wh, vf[e], acc[h][e]);
+        }
+        if (mrow && dl == 0) {
+          const unsigned jj = (unsigned)jw[r];
+          const unsigned key = jj & kKeyMask;
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if ((jj >> (kKeyBits + h)) & 1u) atomicOr(&mrow[(size_t)h * p.mask_words + (key >> 5)], 1u << (key & 31));
         }
       }
     }
+  };
+  auto gather = [&]() {  // this warp's own list, when it is full
+    __syncwarp();
+    for (int r0 = 0; r0 < cnt; r0 += RPI * UNR) gather_rows(warp, r0, cnt);
     nsel += cnt;
     cnt = 0;
     __syncwarp();
   };
-  for (int bi = 0; bi < nbatch; ++bi) {
-    if (bi + kBatches - 1 < nbatch) fetch(bi + kBatches - 1);  // into the slot consumed last
-    cp_async_commit();
-    cp_async_wait<kBatches - 1>();
+  if (mrow) {  // this warp's mask words: zero, then the kept bits of its candidates
+    for (int x = lane; x < (wu1 - wu0) * G; x += kWarp)
+      mrow[(size_t)(x / (wu1 - wu0)) * p.mask_words + wu0 + x % (wu1 - wu0)] = 0u;
     __syncwarp();
-    const int bu = wu0 + bi * BU;
-    const int nr = min(BU, wu1 - bu);
+  }
+  for (int bi = 0; bi < nbatch; ++bi) {
+    cp_async_wait<kBatches - 1>();  // batches 0..bi have landed
+    __syncwarp();
+    const int n = min(BK, ncand - bi * BK);
     // the batch is in shared memory: drop its scratch lines from L2
-    for (int x = lane; x < nr * GC; x += kWarp) discard_line(srow + (size_t)bu * kUnit * GC + (size_t)x * 32);
-    if (cnt + nr * kUnit > list_cap<G>()) gather();
+    {
+      const char* sb0 = reinterpret_cast<const char*>(cscore + (size_t)bi * BK * GC);
+      const char* ib0 = reinterpret_cast<const char*>(ckey + (size_t)bi * BK);
+      const int lines = (n * GC * 4) / 128;  // whole lines only (a partial one ends the candidates)
+      const int ilines = (n * 4) / 128;
+      for (int x = lane; x < lines + ilines; x += kWarp)
+        discard_line(x < lines ? sb0 + (size_t)x * 128 : ib0 + (size_t)(x - lines) * 128);
+    }
+    if (cnt + n > list_cap<G>()) gather();
     const float* sb = ws.s.sc[bi % kBatches];
-    // The batch's decisions first (independent units), then the list.
+    const int* kb_j = ws.s.ci[bi % kBatches];
+    // The batch's decisions first (independent rounds of 32), then the list.
     unsigned kb[BU], un[BU];
 #pragma unroll
     for (int i = 0; i < BU; ++i) {
-      const int j = (bu + i) * kUnit + lane;
+      const int e = i * kUnit + lane;
       unsigned bits = 0u;
-      if (i < nr && j < L) {
+      if (e < n) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          if (sb[(i * kUnit + lane) * GC + h] >= Th[h]) bits |= 1u << h;
+          if (sb[e * GC + h] >= Th[h]) bits |= 1u << h;
       }
       if constexpr (POL == TOPT_GQA_UNION) {
         if (bits) bits = (1u << G) - 1u;
@@ -524,28 +671,18 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       kb[i] = bits;
       un[i] = __ballot_sync(0xffffffffu, bits != 0u);
     }
-    if (mrow) {  // per-head mask words
-#pragma unroll
-      for (int i = 0; i < BU; ++i) {
-        if (i < nr) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const unsigned bal = __ballot_sync(0xffffffffu, (kb[i] >> h) & 1u);
-            if (lane == 0) mrow[(size_t)h * p.mask_words + bu + i] = bal;
-          }
-        }
-      }
-    }
 #pragma unroll
     for (int i = 0; i < BU; ++i) {
       const unsigned bits = kb[i];
       if (bits) {
+        const int e = i * kUnit + lane;
+        const int j = kb_j[e];
         const int pos = cnt + __popc(un[i] & ((1u << lane) - 1u));
-        jl[pos] = (bu + i) * kUnit + lane;
+        jl[pos] = j | (int)(bits << kKeyBits);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const bool keep = (bits >> h) & 1u;
-          const float w = keep ? __expf(sb[(i * kUnit + lane) * GC + h] - Mh[h]) : 0.f;
+          const float w = keep ? __expf(sb[e * GC + h] - Mh[h]) : 0.f;
           kt[h] += keep ? 1 : 0;
           Rl[h] += w;
           wl[pos][h] = w;
@@ -553,7 +690,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       }
       cnt += __popc(un[i]);
     }
-    __syncwarp();  // the slot may be refilled from here on
+    __syncwarp();  // the slot is consumed: refill it with a later batch
+    if (bi + kBatches < nbatch) fetch(bi + kBatches);
+    cp_async_commit();
   }
   cp_async_wait<0>();
   gather();
@@ -585,12 +724,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
     sm.wn[warp] = nsel;
   }
   __syncthreads();
+  // This CTA's partial sums go to the CTA that combines them: output idx
+  // belongs to CTA idx / slice, which keeps one slice per source CTA.
+  const int slice = G * D / (int)csize;
   for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
     const int h = idx / D, dd = idx - h * D;
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) s += sm.u.acc[w][h][dd];
-    sm.u.acc[0][h][dd] = s;  // read and written by this thread only
+    const int c = idx / slice;
+    st_peer_f32(peer_addr(&sm.rnum[(int)crank * slice + (idx - c * slice)], (uint32_t)c), s);
   }
   if (threadIdx.x < G) {
     float r = 0.f;
@@ -600,60 +743,44 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       r += sm.wr[w][threadIdx.x];
       k += sm.wk[w][threadIdx.x];
     }
-    sm.R[threadIdx.x] = r;
-    sm.KT[threadIdx.x] = k;
+    for (uint32_t c = 0; c < csize; ++c) {
+      st_peer_f32(peer_addr(&sm.rR[crank][threadIdx.x], c), r);
+      st_peer_s32(peer_addr(&sm.rK[crank][threadIdx.x], c), k);
+    }
   }
   if (threadIdx.x == 0) {
     int n = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) n += sm.wn[w];
-    sm.NU = n;
+    st_peer_s32(peer_addr(&sm.rN[crank], 0), n);
   }
-  cluster_sync();  // #2: the partials are visible to the leader
+  cluster_sync();  // #2: every partial is in its combining CTA's shared memory
 
-  // ------------------------- combine, SDC and VMC (shared out over the cluster)
+  // ----------------------------- combine, SDC and VMC (shared out over the cluster)
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
-    float pr[kMaxCluster];
-    int pk[kMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      if (c < (int)csize) {
-        pr[c] = ld_peer_f32(peer_addr(&sm.R[h], c));
-        pk[c] = ld_peer_s32(peer_addr(&sm.KT[h], c));
-      }
-    }
     float r = 0.f;
     int k = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      if (c < (int)csize) {
-        r += pr[c];
-        k += pk[c];
-      }
+    for (uint32_t c = 0; c < csize; ++c) {  // rank order
+      r += sm.rR[c][h];
+      k += sm.rK[c][h];
     }
     sm.Rt[h] = r;
     sm.Kt[h] = k;
   }
   if (crank == 0 && threadIdx.x == kWarp && p.vrows) {
     int n = 0;
-    for (uint32_t c = 0; c < csize; ++c) n += ld_peer_s32(peer_addr(&sm.NU, c));
+    for (uint32_t c = 0; c < csize; ++c) n += sm.rN[c];
     p.vrows[pair] = n;
   }
   __syncthreads();
   {
-    const int o0 = G * D * (int)crank / (int)csize;  // this CTA's share of the G x D outputs
-    const int o1 = G * D * ((int)crank + 1) / (int)csize;
-    for (int idx = o0 + threadIdx.x; idx < o1; idx += kThreads) {
+    const int o0 = slice * (int)crank;  // this CTA's share of the G x D outputs
+    for (int k = threadIdx.x; k < slice; k += kThreads) {
+      const int idx = o0 + k;
       const int h = idx / D, dd = idx - h * D;
-      float pn[kMaxCluster];
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)
-        if (c < (int)csize) pn[c] = ld_peer_f32(peer_addr(&sm.u.acc[0][h][dd], c));
       float num = 0.f;
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c)  // rank order
-        if (c < (int)csize) num += pn[c];
+      for (uint32_t c = 0; c < csize; ++c) num += sm.rnum[c * slice + k];  // rank order
       const float e_off = (p.mode == TOPT_PRE && p.sdc == TOPT_SDC_OFFLINE)
                               ? p.e_tilde[(size_t)(kvh * G + h) * p.Lmax + (min(L, p.Lmax) - 1)]
                               : 0.f;
@@ -667,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
       if (dd == 0 && p.kept) p.kept[row] = sm.Kt[h];
     }
   }
-  cluster_sync();  // #3: shared memory stays alive until every peer has read it
+  // The CTA leaves: nothing reads its shared memory after the second barrier.
 }
 
 // ----------------------------------------------------------------------------
@@ -788,6 +915,7 @@ __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocBytes];
 
 size_t decode_noalloc_capacity() { return kNoAllocBytes; }
 long decode_max_pairs() { return 1L << 26; }
+int decode_max_cache() { return (int)kKeyMask; }
 
 cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s) {
   static std::mutex mu;
@@ -845,6 +973,7 @@ cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s) {
   p.nstride = (a.cache_len + kUnit - 1) / kUnit * kUnit;
   if (a.workspace_bytes < scratch_bytes(a)) return cudaErrorInvalidValue;
   p.scores = static_cast<float*>(a.workspace);
+  p.cidx = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + scores_bytes(a));
   const int G = a.n_q_heads / a.n_kv_heads;
   if (a.head_dim == 128) return launch_d<128>(p, G, a, s);
   if (a.head_dim == 64) return launch_d<64>(p, G, a, s);

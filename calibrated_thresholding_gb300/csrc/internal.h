@@ -12,6 +12,7 @@ namespace topt {
 // ------------------------------------------------------------------ decode
 size_t decode_workspace_bytes(const topt_decode_args& a);
 long decode_max_pairs();
+int decode_max_cache();
 cudaError_t decode_launch(const topt_decode_args& a, cudaStream_t s);
 size_t decode_noalloc_capacity();
 cudaError_t decode_noalloc_launch(const topt_decode_args& a, cudaStream_t s);

@@ -92,7 +92,7 @@ typedef struct {
   int32_t n_q_heads;    /* Hq */
   int32_t n_kv_heads;   /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 8, B * Hkv <= 2^26 */
   int32_t head_dim;     /* d: 64 or 128 */
-  int32_t cache_len;    /* Nmax >= 1: token capacity of each cache */
+  int32_t cache_len;    /* Nmax: token capacity of each cache, 1 .. 2^24 - 1 */
   int32_t theta_len;    /* Lmax >= 1: entries per head of `theta` */
   int32_t mode;         /* topt_mode */
   int32_t sdc;          /* topt_sdc */
