@@ -10,14 +10,18 @@ token and topt_decode runs (score pass + select/gather pass).
 
 Printed: one JSON line.  value = tokens/s over all ranks (inputs resident);
 e2e = the same metric through the public Python API with the step's inputs
-copied from pinned host memory and outputs copied back; roofline = the score
-kernel's algorithmic bytes / its CUDA-event duration; cpu_baseline = the
-float64 oracle on a bounded sample, on the host cores.
+copied from pinned host memory and outputs copied back; roofline = the decode
+kernel's algorithmic bytes (whole K cache + union V rows + theta + q, mu,
+out) / its average launch duration over calls launched back to back;
+cpu_baseline = the float64 oracle on a bounded sample, on the host cores.
 
-The line also carries ``prefill``: the LLaMA-3-8B-shaped causal prefill
-(batch 1, 32 query / 8 KV heads, d = 128, 4096 tokens, k = 64) in both
-threshold modes, as dense-equivalent TFLOP/s of the executed tiles against
-the bf16 tensor peak.  ``--workload cfg3`` prints that prefill as the line.
+The line also carries ``decode_workloads`` (the LLaMA-3-70B-shaped decode with
+the k~/k drift over row-length buckets under the nearest-row and the fitted
+theta(L), and the LLaMA-2-7B-shaped long-context decode with its dense
+timing) and ``prefill``: the LLaMA-3-8B-shaped causal prefill (batch 1, 32
+query / 8 KV heads, d = 128, 4096 tokens, k = 64) in both threshold modes, as
+dense-equivalent TFLOP/s of the executed tiles against the bf16 tensor peak.
+``--workload cfg3`` prints that prefill as the line.
 
 ``--impl reference`` times the float64 oracle instead (the method has no
 other implementation); it needs no GPU.
@@ -53,9 +57,8 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture
-# (profiles/decode_kernels_llama3_8b_decode.md, profiles/prefill_tc_kernel_llama3_8b_prefill.md),
-# with the hash of the kernel sources the counters were taken on; reported as
-# null once the sources differ.
+# of each kernel, with the hash of the kernel sources the counters were taken
+# on; reported as null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
                   "source_sha256": "7efae2f933856af9497fd1857b9a01a4a2a80b1c674009de679c4805b0963c7b",
@@ -74,6 +77,8 @@ def parse():
     p.add_argument("--workload", choices=["cfg2", "cfg3", "cfg4", "cfg5", "mkc"], default="cfg2",
                    help="mkc: multi-k cumulative calibration on the cfg3 calibration shape")
     p.add_argument("--no-prefill", action="store_true", help="leave out the prefill object")
+    p.add_argument("--no-other-decode", action="store_true",
+                   help="leave out the 70B-shaped and long-context decode objects")
     p.add_argument("--dense", action="store_true",
                    help="also time the decode step with theta = -inf (on for cfg5)")
     p.add_argument("--prefill-steps", type=int, default=30)
@@ -198,7 +203,7 @@ class DecodeState:
         B, Hq, Hkv, d, n = wl.B, wl.Hq, wl.Hkv, wl.d, wl.n
         self.ch = synth.outlier_channels(synth.seed_of(wl.name, "channels"), Hkv, d)
         self.K, self.V, self.q, self.theta, self.mu, self.out = [], [], [], [], [], []
-        self.kept, self.vrows = [], []
+        self.kept, self.vrows, self.cals = [], [], []
         self.seq_len = torch.full((B,), n, device=dev, dtype=torch.int32)
         self.n_old = torch.full((B,), n - 1, device=dev, dtype=torch.int32)
         zero = torch.zeros((B,), device=dev, dtype=torch.int32)
@@ -263,7 +268,17 @@ class DecodeState:
                 Q = synth.prefill_queries(gen, K, wl.Hq)
                 cal.add(Q, K, row_len, reset=(s0 == 0))
                 del K, Q
+        self.cals.append(cal)
         return cal.finalize().clone()
+
+    def fitted_theta(self, layer):
+        """The same calibration finalised as the fitted function of ln L."""
+        cal = self.cals[layer]
+        cal.fit = True
+        try:
+            return cal.finalize().clone()
+        finally:
+            cal.fit = False
 
     def run_step(self, L, stream, events=None):
         for l in range(self.layers):
@@ -282,6 +297,95 @@ class DecodeState:
         for a in self.dargs:
             a.events[0] = None
             a.events[1] = None
+
+
+def graph_of(dev, fn):
+    """``fn(stream_handle)`` captured as one CUDA graph on a side stream, replayed
+    three times before it is returned."""
+    cur = torch.cuda.current_stream(dev)
+    gr = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(cur)
+    with torch.cuda.graph(gr, stream=cap):
+        fn(ctypes.c_void_p(cap.cuda_stream))
+    cur.wait_stream(cap)
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize(dev)
+    return gr
+
+
+def time_decode_calls(state, L, stream, dev, reps):
+    """Duration of one decode call (ms), measured two ways with CUDA events on
+    ``stream``.  Back to back: at least 32 decode calls (every layer's, in
+    order) in one graph with no event between them, so each call may start
+    while the previous one drains as it does inside a step; events around the
+    replay, total / calls.  Isolated: events right before and after every call
+    (the call then also pays its launch)."""
+    layers = state.layers
+    per = max(1, 32 // layers)
+
+    def calls(sh):
+        for _ in range(per):
+            for l in range(layers):
+                rc = L.topt_decode(ctypes.byref(state.dargs[l]), sh)
+                if rc:
+                    raise topt.ToptError("topt_decode", rc)
+
+    g = graph_of(dev, calls)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b2b = []
+    for _ in range(reps):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        b2b.append(e0.elapsed_time(e1) / (per * layers))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
+    for l_ in evs:                 # a torch event exists once recorded
+        for e in l_:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    hs = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in evs]
+
+    def calls_ev(sh):
+        for l in range(layers):
+            a = state.dargs[l]
+            a.events[0], a.events[1] = hs[l][0], hs[l][1]
+            rc = L.topt_decode(ctypes.byref(a), sh)
+            if rc:
+                raise topt.ToptError("topt_decode", rc)
+        state.clear_events()
+
+    g2 = graph_of(dev, calls_ev)
+    iso = []
+    for _ in range(reps):
+        g2.replay()
+        torch.cuda.synchronize(dev)
+        iso += [evs[l][0].elapsed_time(evs[l][1]) for l in range(layers)]
+    return float(np.median(b2b)), float(np.mean(iso))
+
+
+def decode_roofline(state, b2b_ms, iso_ms):
+    """The decode kernel against the measured copy bandwidth: algorithmic bytes
+    of one call (whole K cache + union V rows + theta entries + q, mu, out)
+    over its back-to-back duration; the isolated call beside it."""
+    peak, peak_kind = hbm_peak()
+    _, per_layer = algorithmic_bytes(state)
+    alg = float(np.mean(per_layer))
+    achieved = alg / (b2b_ms / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+            "traffic": recorded_traffic(DECODE_TRAFFIC) if state.wl is workloads.CFG2 else None,
+            "algorithmic_bytes_per_launch": alg,
+            "bytes": "whole K cache + union V rows + theta entries + q, mu, out",
+            "avg_launch_ms": b2b_ms,
+            "timing": "calls launched back to back in one CUDA graph, CUDA events around the replay",
+            "isolated_call_ms": iso_ms,
+            "isolated_frac": alg / (iso_ms / 1e3) / 1e9 / peak}
 
 
 def time_dense(state, L, stream, steps, warmup):
@@ -312,12 +416,14 @@ def time_dense(state, L, stream, steps, warmup):
             "theta": "-inf (every valid key kept)", "launch": "eager host launches"}
 
 
-def drift_sweep(state):
+def drift_sweep(state, theta=None):
     """k~/k per row-length bucket with the first layer's caches at ~16 lengths
-    spread over the buckets (theta calibrated on shorter rows is extended by the
-    last calibrated row), through topt.decode with fresh queries per length."""
+    spread over the buckets, through topt.decode with fresh queries per length.
+    ``theta`` defaults to the layer's table (rows longer than the calibrated
+    ones take the last calibrated row's threshold)."""
     wl = state.wl
-    K, V, theta = state.K[0], state.V[0], state.theta[0]
+    K, V = state.K[0], state.V[0]
+    theta = state.theta[0] if theta is None else theta
     per_bucket = {}
     lengths = list(workloads.DRIFT_LENGTHS)
     for c in range(0, len(lengths), wl.B):
@@ -616,6 +722,15 @@ def prefill_cpu_baseline(wl, seconds):
                       f"float64 numpy, {cores} threads; scaled to {rows_per_call} rows per call"}
 
 
+def prefill_config(wl, mode_name, world):
+    """The ``config`` of a prefill line (both arms print the same one)."""
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+            "S": wl.S, "k": wl.k, "mode": mode_name,
+            "flops": "kept-element: 2 d per causal element (QK^T) + 2 d per kept element (P.V)",
+            "l2": f"{L2_FLUSH_BYTES >> 20} MiB written between timed calls",
+            "parallelism": f"replicas x{world} (independent prefills per GPU)"}
+
+
 def run_reference_prefill(args, wl):
     cores = host_cores()
     sample = host_prefill_sample(wl)
@@ -631,15 +746,16 @@ def run_reference_prefill(args, wl):
     t_row = sum(r[0] for r in runs) / args.steps
     rows_per_call = wl.B * wl.Hq * wl.S
     kept_total = float(np.mean([r[1] for r in runs])) * rows_per_call
-    ms = t_row * rows_per_call * 1e3
+    ms = t_row * rows_per_call * 1e3               # the whole call's rows at the sampled rate
     value = kept_elem_flops(wl, kept_total) / (ms / 1e3) / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                       "S": wl.S, "k": wl.k, "mode": "post-softmax+VMC",
-                       "flops": "kept-element: 2 d per causal element (QK^T) + 2 d per kept element (P.V)"},
+            "ms_per_step": t_row * per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": prefill_config(wl, PREFILL_MODES[0][0], args.gpus),
+            "extrapolated": True, "sample_rows_per_step": per_step, "rows_per_step": rows_per_call,
+            "note": "ms_per_step is the measured time of the sampled rows of a step; value "
+                    "scales their rate to the call's rows",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} prefill rows per step of {rows_per_call}, "
                                        "float64 numpy oracle"},
@@ -681,13 +797,16 @@ def run_reference(args):
     total = sum(one_step(i) for i in range(args.steps))
     rows_per_step = wl.B * wl.Hq * layers_total
     t_row = total / (args.steps * per_step_rows)
-    value = wl.B / (t_row * rows_per_step)
+    value = wl.B / (t_row * rows_per_step)      # the whole step's rows at the sampled rate
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": t_row * rows_per_step * 1e3, "higher_is_better": True,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                       "n": wl.n, "layers": layers_total},
+            "config": decode_config(wl, layers_total, args.gpus),
+            "extrapolated": True,
+            "sample_rows_per_step": per_step_rows, "rows_per_step": rows_per_step,
+            "note": "ms_per_step is the measured time of the sampled rows of a step; value "
+                    "scales their rate to the step's rows",
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step_rows} (batch, head) rows per step of "
                                        f"{rows_per_step}, float64 numpy oracle"},
@@ -699,6 +818,64 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # main (GPU) arm
 # ---------------------------------------------------------------------------
+def decode_config(wl, layers, world, eager=False):
+    """The ``config`` of a decode line (both arms print the same one)."""
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+            "n": wl.n, "layers": layers, "k": wl.k,
+            "k_layers_0_1": wl.k_first_layers or wl.k,
+            "mode": "post-softmax+VMC" if wl.mode == 1 else "pre-softmax",
+            "l2": "inputs larger than L2: each layer call streams a distinct "
+                  f"{wl.B * wl.Hkv * wl.n * wl.d * 2 / 1e6:.0f} MB K cache",
+            "parallelism": f"replicas x{world} (independent sequences per GPU)",
+            "launch": "eager host launches" if eager else "one step replayed as a CUDA graph"}
+
+
+def decode_step_graph(state, L, dev):
+    """One decode step (vmean update + decode per layer) as a CUDA graph."""
+    return graph_of(dev, lambda sh: state.run_step(L, sh))
+
+
+def other_decode_report(wl, L, dev, stream, steps, warmup):
+    """A decode workload besides the main line: tokens/s of its step (graph
+    replays, CUDA events), the decode kernel's roofline, V rows per group, and
+    k~/k -- per row-length bucket for the 70B-shaped workload (nearest-row and
+    fitted theta(L)), with dense (theta = -inf) timing for the long-context one."""
+    state = DecodeState(wl, wl.layers, 0, dev)
+    g = decode_step_graph(state, L, dev)
+    for _ in range(warmup):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = e0.elapsed_time(e1) / steps
+    b2b, iso = time_decode_calls(state, L, stream, dev, max(5, steps // 2))
+    out = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d, "n": wl.n,
+           "k": wl.k, "layers": wl.layers,
+           "mode": "post-softmax+VMC" if wl.mode == 1 else "pre-softmax",
+           "tokens_per_s": wl.B / (step_ms / 1e3), "ms_per_step": step_ms,
+           "roofline": decode_roofline(state, b2b, iso),
+           "vrows_per_group": float(np.mean([state.vrows[l].double().mean().item()
+                                             for l in range(state.layers)])),
+           "kept_over_k": kept_ratio_by_bucket(state),
+           "gpu_launches_per_step": 2 * wl.layers}
+    if wl.cal_len:
+        out["kept_over_k_by_bucket"] = {
+            "nearest_row": drift_sweep(state),
+            "fitted_ln_L": drift_sweep(state, state.fitted_theta(0)),
+            "theta": f"calibrated on rows 1..{wl.cal_len} of {wl.n_cal} sequences"}
+    if wl is workloads.CFG5:
+        dense = time_dense(state, L, stream, max(10, steps), warmup)
+        dense["topt_over_dense_speedup"] = dense["ms_per_step"] / step_ms
+        out["dense"] = dense
+    del state
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -740,77 +917,29 @@ def main():
         state.run_step(L, sh)
     torch.cuda.synchronize(dev)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if args.eager:
-        # events around the decode kernel of every layer call of every step
-        ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
-              for _ in range(args.steps)]
-        for s_ in ev:
-            for l_ in s_:
-                for e in l_:
-                    e.record(stream)
-        handles = [[[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in s_] for s_ in ev]
-    else:
-        # One step captured as a CUDA graph, twice: `graph` is the timed step
-        # (no events inside, so each kernel may start while the previous one
-        # drains); `graph_calls` has events around every decode call and
-        # times the calls alone.
-        def capture(with_events):
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layers)]
-            for l_ in evs:
-                for e in l_:
-                    e.record(stream)
-            torch.cuda.synchronize(dev)
-            hs = [[ctypes.c_void_p(e.cuda_event) for e in l_] for l_ in evs] if with_events else None
-            gr = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream(dev)
-            cap.wait_stream(stream)
-            with torch.cuda.graph(gr, stream=cap):
-                state.run_step(L, ctypes.c_void_p(cap.cuda_stream), hs)
-            state.clear_events()
-            stream.wait_stream(cap)
-            for _ in range(3):
-                gr.replay()
-            torch.cuda.synchronize(dev)
-            return gr, evs
-        graph, _ = capture(False)
-        graph_calls, ev_calls = capture(True)
+    # the timed step: one CUDA graph (no event inside, so each kernel may start
+    # while the previous one drains), or eager host launches
+    graph = None if args.eager else decode_step_graph(state, L, dev)
     barrier()
     clocks = ClockSampler(local)
     time.sleep(0.3)
     barrier()
     t0 = time.time()
     start.record(stream)
-    if args.eager:
-        for s_ in range(args.steps):
-            state.run_step(L, sh, handles[s_])
-    else:
-        for _ in range(args.steps):
+    for _ in range(args.steps):
+        if graph is None:
+            state.run_step(L, sh)
+        else:
             graph.replay()
     stop.record(stream)
     barrier()
     t1 = time.time()
-    state.clear_events()
     clk = clocks.stop(t0, t1)
     ms = max_over_ranks(start.elapsed_time(stop), world, dev)
-    if args.eager:
-        kern_ms = [ev[s_][l_][0].elapsed_time(ev[s_][l_][1]) for s_ in range(args.steps) for l_ in range(layers)]
-    else:
-        # the decode calls alone: a short run of the graph with events
-        kern_ms = []
-        for _ in range(max(5, args.steps // 20)):
-            graph_calls.replay()
-            torch.cuda.synchronize(dev)
-            kern_ms += [ev_calls[l_][0].elapsed_time(ev_calls[l_][1]) for l_ in range(layers)]
     ms_per_step = ms / args.steps
     tokens = wl.B * args.steps * world
     value = tokens / (ms / 1e3)
-
-    k_bytes, per_layer = algorithmic_bytes(state)
-    kern_avg = float(np.mean(kern_ms)) / 1e3
-    peak, peak_kind = hbm_peak()
-    alg_bytes = float(np.mean(per_layer))
-    achieved = alg_bytes / kern_avg / 1e9
-    traffic = recorded_traffic(DECODE_TRAFFIC)
+    b2b_ms, iso_ms = time_decode_calls(state, L, stream, dev, max(5, args.steps // 4))
     vrows_per_group = float(np.mean([state.vrows[l].double().mean().item() for l in range(layers)]))
 
     e2e = None
@@ -822,23 +951,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                   "n": wl.n, "layers": layers, "k": wl.k,
-                   "k_layers_0_1": wl.k_first_layers or wl.k,
-                   "mode": "post-softmax+VMC" if wl.mode == 1 else "pre-softmax",
-                   "l2": "inputs larger than L2: each layer call streams a distinct "
-                         f"{k_bytes / 1e6:.0f} MB K cache",
-                   "parallelism": f"replicas x{world} (independent sequences per GPU)",
-                   "launch": "eager host launches" if args.eager else "one step replayed as a CUDA graph"},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_launch": alg_bytes,
-                     "bytes": "whole K cache + union V rows + theta entries + q, mu, out",
-                     "avg_launch_ms": kern_avg * 1e3},
+        "config": decode_config(wl, layers, world, args.eager),
+        "roofline": decode_roofline(state, b2b_ms, iso_ms),
         "vrows_per_group": vrows_per_group,
         "kept_over_k": kept_ratio_by_bucket(state),
         "gpu_launches": args.steps * layers * 2,   # vmean + decode per layer
@@ -847,15 +961,19 @@ def main():
     if e2e is not None:
         line["e2e"] = e2e
     if args.workload == "cfg4":
-        line["kept_over_k_by_bucket"] = drift_sweep(state)
+        line["kept_over_k_by_bucket"] = {"nearest_row": drift_sweep(state),
+                                         "fitted_ln_L": drift_sweep(state, state.fitted_theta(0))}
     if args.dense or args.workload == "cfg5":
         # after every thresholded figure above: it overwrites kept and vrows
         line["dense"] = time_dense(state, L, stream, max(10, args.steps // 4), args.warmup)
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    del state
+    torch.cuda.empty_cache()
+    if args.workload == "cfg2" and not args.no_other_decode:
+        line["decode_workloads"] = [other_decode_report(w, L, dev, stream, 10, 3)
+                                    for w in (workloads.CFG4, workloads.CFG5)]
     if not args.no_prefill:
-        del state
-        torch.cuda.empty_cache()
         line["prefill"] = prefill_report(L, workloads.CFG3, dev, stream, args.prefill_steps, 3)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -897,11 +1015,7 @@ def main_prefill(args, dev, rank, local, world):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": call * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                   "S": wl.S, "k": wl.k, "mode": name,
-                   "flops": "kept-element: 2 d per causal element (QK^T) + 2 d per kept element (P.V)",
-                   "l2": f"{L2_FLUSH_BYTES >> 20} MiB written between timed calls",
-                   "parallelism": f"replicas x{world} (independent prefills per GPU)"},
+        "config": prefill_config(wl, name, world),
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
@@ -993,6 +1107,14 @@ def mkc_cpu_baseline(wl, seconds):
                       f"{cores} threads"}
 
 
+def mkc_config(wl, world):
+    """The ``config`` of a multi-k calibration line (both arms print the same one)."""
+    return {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
+            "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS),
+            "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call",
+            "parallelism": f"replicas x{world} (independent calibrations per GPU)"}
+
+
 def run_reference_mkc(args, wl):
     cores = host_cores()
     sample = host_mkc_sample(wl)
@@ -1006,10 +1128,14 @@ def run_reference_mkc(args, wl):
     line = {"impl": "reference",
             "metric": "multi-k cumulative calibration: pooled calibration scores per second",
             "value": value, "unit": "scores/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": pooled / value * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": sum(r[0] for r in runs) / args.steps * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
-                       "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS)},
+            "config": mkc_config(wl, args.gpus),
+            "extrapolated": True, "sample_scores_per_step": sum(r[1] for r in runs) // args.steps,
+            "scores_per_call": pooled,
+            "note": "ms_per_step is the measured time of the sampled groups of a step; value is "
+                    "their pooled-score rate",
             "cpu_baseline": {"value": value, "unit": "scores/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} (head, row length) groups per step, "
                                        "float64 numpy oracle, pre-softmax"},
@@ -1094,11 +1220,8 @@ def main_mkc(args, dev, rank, local, world):
         "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["pre"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name + " calibration (MKC)", "N": wl.n_cal, "Hq": wl.Hq,
-                   "Hkv": wl.Hkv, "d": wl.d, "S": wl.S, "ks": list(MKC_KS),
-                   "heads_per_pass": int(heads_per_pass),
-                   "l2": "scores workspace of 4 GiB, larger than L2, rewritten every call",
-                   "parallelism": f"replicas x{world} (independent calibrations per GPU)"},
+        "config": mkc_config(wl, world),
+        "heads_per_pass": int(heads_per_pass),
         "ms_per_call": res, "pooled_scores": pooled,
         "post_scores_per_s": pooled * world / (res["post"] / 1e3),
         "sdc_offline_calibration": {"ms_per_call": sdc_ms, "table": "k = 64 pre-softmax theta",
