@@ -21,6 +21,8 @@
 // targets k from one pass over the calibration rows.
 #include <atomic>
 
+#include <cfloat>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -342,8 +344,10 @@ __device__ void fill_nearest_rows(int Lmax, int k, const Has& has, const Val& va
 // One head's row of a threshold table from a least-squares line (degree
 // min(1, n - 1)) in x = ln L through the n usable calibrated row ids L > k:
 // y = theta (PRE) or ln theta (POST, theta > 0 only).  Every L > k takes the
-// fitted value (exp of it for POST); L <= k and a head without usable row ids
-// are dense.  The pages mention a fitted function of the sequence length
+// fitted value (exp of it for POST, kept between the smallest normal float and
+// the head's largest calibrated value, so that an extrapolated row neither
+// drops every key nor reads as "keep all"); L <= k and a head without usable
+// row ids are dense.  The pages mention a fitted function of the sequence length
 // without its form; a line in ln L extrapolates past the calibrated lengths
 // far better than a quadratic.  fp64 normal equations (the sums cover a
 // quadratic), solved by one thread.
@@ -357,7 +361,10 @@ __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& v
   __shared__ double A[3][4];   // normal equations | right-hand side
   __shared__ double coef[3];
   __shared__ int s_deg;
+  __shared__ float s_cap;
+  __shared__ float red_cap[kW];
   double m[8];  // sums of x^0..x^4, then of y x^0..y x^2
+  float cap = 0.f;  // largest usable calibrated value (POST)
 #pragma unroll
   for (int q = 0; q < 8; ++q) m[q] = 0.0;
   for (int i = threadIdx.x; i < Lmax; i += kFinThreads) {
@@ -366,6 +373,7 @@ __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& v
     double y = (double)val(i);
     if (mode == TOPT_POST) {
       if (!(y > 0.0)) continue;
+      cap = fmaxf(cap, val(i));
       y = log(y);
     }
     const double x = log((double)L);
@@ -385,12 +393,18 @@ __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& v
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     if (lane == 0) red[q][warp] = v;
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cap = fmaxf(cap, __shfl_xor_sync(0xffffffffu, cap, off));
+  if (lane == 0) red_cap[warp] = cap;
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int q = 0; q < 8; ++q) {
       S[q] = 0.0;
       for (int w = 0; w < kW; ++w) S[q] += red[q][w];
     }
+    float c = 0.f;
+    for (int w = 0; w < kW; ++w) c = fmaxf(c, red_cap[w]);
+    s_cap = c;
     const int n = (int)(S[0] + 0.5);
     const int deg = n < 2 ? n - 1 : kFitDegree;
     if (deg >= 0) {
@@ -434,7 +448,7 @@ __device__ void fit_rows(int Lmax, int k, int mode, const Has& has, const Val& v
     }
     const double x = log((double)L);
     const double y = coef[0] + x * (coef[1] + x * coef[2]);
-    out[i] = (float)(mode == TOPT_POST ? exp(y) : y);
+    out[i] = mode == TOPT_POST ? fmaxf(fminf((float)exp(y), s_cap), FLT_MIN) : (float)y;
   }
 }
 

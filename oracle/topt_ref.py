@@ -50,6 +50,9 @@ reason in the design notes of the repository):
       row ids L > k, fitted to theta (pre) or to ln theta (post, positive
       values only), and used for every row id L > k.  A quadratic in ln L
       was tried first and extrapolated badly past the calibrated lengths.
+      The post-softmax value is kept between the smallest normal float32 and
+      the largest calibrated value (a probability threshold of 1 or more
+      would drop every key of a row, one of 0 would keep them all).
 * c21 GQA group policies (§4.6, the two alternatives): UNION gives every head
       of a group the union of the group's kept sets; VOTE keeps a key for a
       head only if the head keeps it and at least t heads of the group do.
@@ -66,6 +69,7 @@ SDC_NONE, SDC_EXACT, SDC_EXPTH, SDC_OFFLINE = 0, 1, 2, 3
 GQA_OWN, GQA_UNION, GQA_VOTE = 0, 1, 2
 GAMMA = 0.05          # [TopTheta §3.2.1, exp-threshold estimator]
 BAND_REL = 1e-3       # decisions within this relative distance of theta are not compared
+FLT32_MIN_NORMAL = 2.0 ** -126
 
 
 # ---------------------------------------------------------------------------
@@ -179,8 +183,11 @@ def fit_row_ids(value, Lmax, k, mode):
 
     y = theta (PRE) or ln theta (POST, theta > 0 only) is fitted by least
     squares with a line (degree min(1, n - 1)) in x = ln L over the n usable
-    row ids; every L > k takes the fitted value (exp of it for POST),
-    L <= k stays dense, and a head without usable row ids is dense.
+    row ids; every L > k takes the fitted value (exp of it for POST, kept
+    between the smallest normal float32 and the largest calibrated value, so an
+    extrapolated post-softmax threshold never reaches 1, which would drop every
+    key, nor 0, which would keep them all), L <= k stays dense, and a head
+    without usable row ids is dense.
     """
     row = np.full(Lmax, -np.inf)
     pts = [(L, v) for L, v in sorted(value.items()) if L > k and (mode == PRE or v > 0)]
@@ -194,7 +201,10 @@ def fit_row_ids(value, Lmax, k, mode):
     coef = np.polynomial.polynomial.polyfit(x, y, deg)
     Ls = np.arange(k + 1, Lmax + 1, dtype=np.float64)
     fitted = np.polynomial.polynomial.polyval(np.log(Ls), coef)
-    row[k:] = np.exp(fitted) if mode == POST else fitted
+    if mode == POST:
+        row[k:] = np.clip(np.exp(fitted), FLT32_MIN_NORMAL, max(v for _, v in pts))
+    else:
+        row[k:] = fitted
     return row
 
 
@@ -461,6 +471,33 @@ def attend_row(a, Vrows, theta, mode, sdc=SDC_NONE, vmc=False, mu=None,
         out = out + beta * np.asarray(mu, dtype=np.float64)    # Eq. 7
     return dict(out=out, keep=keep, kept=kt, band=band, m=m, Z=Z, R=R, E=E,
                 beta=beta)
+
+
+def prefill_decisions(Q, K, theta_row, mode):
+    """The keep and band decisions of every causal row of one head at once.
+
+    Row i of a causal prefill sees keys 0..i (reading c6), so L = i + 1 and its
+    threshold is theta_for_row(theta_row, L) (readings c3, c5).  The element
+    x_ij is a_ij (PRE) or softmax(a_i)_j (POST) and is kept iff x_ij >= theta
+    (reading c1); band marks |x - theta| <= 1e-3 |theta| for finite theta.
+    These are attend_row's decisions, computed for all rows as whole matrices.
+    Q, K [S][d]; returns keep [S][S], band [S][S] (False above the diagonal).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    S, d = Q.shape
+    causal = np.tril(np.ones((S, S), dtype=bool))
+    a = np.where(causal, (Q @ K[:S].T) / math.sqrt(d), -np.inf)
+    theta = np.array([theta_for_row(theta_row, i + 1) for i in range(S)])[:, None]
+    if mode == PRE:
+        x = a
+    else:
+        e = np.exp(a - a.max(axis=1, keepdims=True))
+        x = e / e.sum(axis=1, keepdims=True)
+    keep = (x >= theta) & causal
+    with np.errstate(invalid="ignore"):     # -inf - (-inf) above the diagonal of dense rows
+        band = np.isfinite(theta) & (np.abs(x - theta) <= BAND_REL * np.abs(theta)) & causal
+    return keep, band
 
 
 def vmean_ref(Vrows):

@@ -405,11 +405,20 @@ def check_fitted_theta():
         ref.collect_thresholds(Qs[i:i + 1], Ks[i:i + 1], [L], k, ref.PRE, sets)
     th = ref.finalize_fitted(sets, 1, 120, k, 0.0, ref.PRE)
     np.testing.assert_allclose(th[0, k:], want[k:120], rtol=0, atol=1e-12)
-    # post-softmax: a power law in L is a line in ln L after the log
+    # post-softmax: a power law in L is a line in ln L after the log; rows
+    # shorter than the shortest calibrated one would extrapolate above every
+    # calibrated value and stay at the largest one instead
     sets = {(0, L): [0.3 * L ** -1.2] for L in (6, 20, 70)}
     th = ref.finalize_fitted(sets, 1, Lmax, k, 0.0, ref.POST)
-    Lr = np.arange(k + 1, Lmax + 1)
-    np.testing.assert_allclose(th[0, k:], 0.3 * Lr ** -1.2, rtol=1e-12, atol=0)
+    Lr = np.arange(6, Lmax + 1)
+    np.testing.assert_allclose(th[0, 5:], 0.3 * Lr ** -1.2, rtol=1e-12, atol=0)
+    assert np.all(th[0, k:5] == 0.3 * 6 ** -1.2)
+    # an extrapolated probability threshold never reaches 1 (the row would keep
+    # nothing) nor falls to 0 (it would keep everything)
+    th = ref.finalize_fitted({(0, 10): [0.9], (0, 40): [0.5]}, 1, 60, k, 0.0, ref.POST)
+    assert th[0, 3] == 0.9 and 0.5 < th[0, 19] < 0.9      # L = 4 extrapolates to 1.33
+    th = ref.finalize_fitted({(0, 10): [1e-30], (0, 20): [1e-36]}, 1, 400, k, 0.0, ref.POST)
+    assert th[0, 399] == 2.0 ** -126 and abs(th[0, 9] - 1e-30) < 1e-12 * 1e-30
     # two calibrated lengths: the line through both points in ln L
     th = ref.finalize_fitted({(0, 10): [1.0], (0, 40): [2.0]}, 1, 80, k, 0.0, ref.PRE)
     assert abs(th[0, 9] - 1.0) < 1e-13 and abs(th[0, 39] - 2.0) < 1e-13
@@ -712,3 +721,33 @@ def test_pins_catch_planted_mistakes(monkeypatch, golden_dir):
              lambda pieces, k: max([lo for lo, hi, t, c in pieces if t >= k * c], default=-np.inf),
              check_mkc_bruteforce)
     assert ref.row_scores is orig_scores and ref.calibration_sample is orig_sample
+
+
+# ---------------------------------------------------------------------------
+# The whole-matrix prefill decisions equal attend_row's, row by row.
+# ---------------------------------------------------------------------------
+def test_prefill_decisions_match_rows():
+    rng = np.random.default_rng(5)
+    S, d = 40, 8
+    Q = rng.standard_normal((S, d))
+    K = rng.standard_normal((S, d))
+    V = rng.standard_normal((S, d))
+    for mode in (ref.PRE, ref.POST):
+        theta = np.full(S, -np.inf)
+        for L in range(4, S + 1):
+            a = ref.row_scores(Q[L - 1], K, L)
+            x = a if mode == ref.PRE else ref.row_softmax(a)
+            xs = np.sort(x)
+            theta[L - 1] = 0.5 * (xs[-3] + xs[-4])         # between the 3rd and 4th largest
+        xs = np.sort(ref.row_scores(Q[20], K, 21) if mode == ref.PRE
+                     else ref.row_softmax(ref.row_scores(Q[20], K, 21)))
+        theta[20] = xs[-3] * (1 + 5e-4 * np.sign(xs[-3]))  # a row with an element inside the band
+        keep, band = ref.prefill_decisions(Q, K, theta, mode)
+        assert not np.triu(keep, 1).any() and not np.triu(band, 1).any()
+        for i in range(S):
+            a = ref.row_scores(Q[i], K, i + 1)
+            r = ref.attend_row(a, V[:i + 1], ref.theta_for_row(theta, i + 1), mode)
+            assert np.array_equal(keep[i, :i + 1], r["keep"]), (mode, i)
+            assert np.array_equal(band[i, :i + 1], r["band"]), (mode, i)
+        assert band.any()                                  # the band case is exercised
+        assert keep[10].sum() == 3 and keep[2].sum() == 3  # 3rd largest keeps 3; a dense row keeps all
