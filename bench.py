@@ -61,8 +61,8 @@ NOMINAL_HBM_GBS = 8000.0
 # on; reported as null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
-                  "source_sha256": "7efae2f933856af9497fd1857b9a01a4a2a80b1c674009de679c4805b0963c7b",
-                  "bytes_per_launch": 268609536 + 13168384}   # decode_scores_kernel, one layer call
+                  "source_sha256": "299e27949f1c896f2a58b0e5f2eb4b2abc6cf33ad978fd72fc9c33b28407c8b0",
+                  "bytes_per_launch": 285350656 + 3795456}   # decode_kernel, one layer call (k = 128)
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
                    "source_sha256": "f0bd74c0af7559c1a0d66f264efb8004ccea2b5a967d0127d663594ba6fa74e6",
                    "bytes_per_launch": 59525120 + 22531584}   # prefill_tc_kernel, post-softmax + VMC
