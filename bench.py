@@ -82,6 +82,8 @@ def parse():
     p.add_argument("--dense", action="store_true",
                    help="also time the decode step with theta = -inf (on for cfg5)")
     p.add_argument("--prefill-steps", type=int, default=30)
+    p.add_argument("--prefill-mode", choices=["post", "pre"], default="post",
+                   help="--workload cfg3: post-softmax + VMC, or pre-softmax + exact SDC + VMC")
     p.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -468,6 +470,11 @@ def kept_ratio_by_bucket(state):
 # the prefill workload
 # ---------------------------------------------------------------------------
 PREFILL_MODES = (("post-softmax+VMC", 1, 0), ("pre-softmax+exact SDC+VMC", 0, 1))
+
+
+def prefill_mode(args):
+    """The (name, mode, sdc) of the cfg3 line's threshold mode."""
+    return PREFILL_MODES[0] if args.prefill_mode == "post" else PREFILL_MODES[1]
 L2_FLUSH_BYTES = 256 << 20     # written between timed prefill calls (L2 is 129 MB)
 
 
@@ -703,13 +710,14 @@ def prefill_rows_sample(wl, n, heads=4, seed=0):
     return [(0, int(rng.integers(heads)), int(i)) for i in rng.integers(0, wl.S, n)]
 
 
-def prefill_cpu_baseline(wl, seconds):
+def prefill_cpu_baseline(wl, seconds, pmode=PREFILL_MODES[0]):
+    name, mode, sdc = pmode
     cores = host_cores()
     sample = host_prefill_sample(wl)
     done, spent, kept_sum = 0, 0.0, 0.0
     while spent < seconds:
         rows = prefill_rows_sample(wl, 8 * cores, seed=done)
-        dt, kept = oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores)
+        dt, kept = oracle_prefill_row_seconds(sample[mode], mode, sdc, rows, cores)
         spent += dt * len(rows)
         kept_sum += kept * len(rows)
         done += len(rows)
@@ -718,7 +726,7 @@ def prefill_cpu_baseline(wl, seconds):
     kept_total = kept_sum / done * rows_per_call
     return {"value": kept_elem_flops(wl, kept_total) / (t_row * rows_per_call) / 1e12, "unit": "TFLOP/s",
             "cores": cores, "kind": "oracle",
-            "sample": f"{done} prefill rows (uniform row index, post-softmax+VMC, k={wl.k}), "
+            "sample": f"{done} prefill rows (uniform row index, {name}, k={wl.k}), "
                       f"float64 numpy, {cores} threads; scaled to {rows_per_call} rows per call"}
 
 
@@ -736,9 +744,11 @@ def run_reference_prefill(args, wl):
     sample = host_prefill_sample(wl)
     per_step = 4 * cores
 
+    _, mode, sdc = prefill_mode(args)
+
     def one_step(i):
         rows = prefill_rows_sample(wl, per_step, seed=i)
-        return oracle_prefill_row_seconds(sample[1], 1, 0, rows, cores)
+        return oracle_prefill_row_seconds(sample[mode], mode, sdc, rows, cores)
 
     for i in range(args.warmup):
         one_step(i)
@@ -752,7 +762,7 @@ def run_reference_prefill(args, wl):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_row * per_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": prefill_config(wl, PREFILL_MODES[0][0], args.gpus),
+            "config": prefill_config(wl, prefill_mode(args)[0], args.gpus),
             "extrapolated": True, "sample_rows_per_step": per_step, "rows_per_step": rows_per_call,
             "note": "ms_per_step is the measured time of the sampled rows of a step; value "
                     "scales their rate to the call's rows",
@@ -986,11 +996,11 @@ def main_prefill(args, dev, rank, local, world):
     wl = workloads.CFG3
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = prefill_cpu_baseline(wl, args.cpu_seconds)
+        cpu = prefill_cpu_baseline(wl, args.cpu_seconds, prefill_mode(args))
     from calibrated_thresholding_gb300 import build
     build.build()
     L = topt.lib()
-    name, mode, sdc = PREFILL_MODES[0]
+    name, mode, sdc = prefill_mode(args)
     st = PrefillState(wl, dev, mode, sdc)
     stream = torch.cuda.current_stream(dev)
     if world > 1:

@@ -6,27 +6,38 @@
 // calibrated threshold theta[h][i] ([TopTheta §3, Fig. 1]), SDC [Eq. 4] and
 // VMC [Eq. 5-7] normalise the output as in the CUDA-core variant.
 //
-// One CTA = 128 query rows of one (batch, head); twenty warps:
-//   warps 0-15 four threads per query row (the row is its TMEM lane; warps
-//              w, w+4, w+8, w+12 share a lane quadrant and take 32 of the
-//              tile's 128 columns each): pass 1 row maximum and sum, pass 2
-//              threshold and P, epilogue
-//   warp 16    TMA producer: the Q block once, K tiles for both passes
-//              (128-byte swizzled boxes of 64 elements)
-//   warp 17    TMEM allocation; lane 0 issues the QK^T tcgen05.mma
-//   warp 18    lane 0 issues the P.V tcgen05.mma (two issuing threads, so the
-//              barrier bookkeeping of one overlaps the MMAs of the other)
-//   warp 19    TMA producer of the V tiles of pass 2 (it waits on P.V to free
-//              a stage, so it runs apart from the K producer)
-// Scores S = Q K^T (128 rows x 128 keys, fp32) rotate through three TMEM
-// buffers so the tensor core computes the next tiles while the row threads
-// read one.  The output accumulator O (128 x d, fp32) stays in TMEM for the
-// whole of pass 2.  Pass 2 writes P = exp(a - m) of kept elements (0
-// elsewhere) as fp16 pairs into the score buffer it was read from, and
-// O += P V takes P straight from TMEM; it is issued only when some row of the
-// tile kept an element, and the executed and causal tile counts are reported.
-// 128-key tiles keep both MMAs at N >= 128, the width at which one tcgen05.mma
-// runs at the tensor core's full rate.
+// One CTA = the same 128-row block of NQ query heads (NQ = 2 when the GQA
+// group size is even: two heads of one KV head, so every K and V tile loaded
+// serves both; else 1).  Each head's block is a "group": four warps, one
+// thread per query row (the row is its TMEM lane), two score buffers S (64
+// keys each) and an output accumulator O in TMEM, and its own MMA-issuing
+// thread.  While a group's rows turn one S into P, the tensor core computes
+// its next S and the other group's P.V and QK^T.
+//
+// Eleven warps:
+//   warps 0-3   rows of group 0; warps 4-7 rows of group 1
+//   warp 8      TMA producer: the Q blocks, then K and V tiles through one
+//               ring of shared-memory slots, in the order they are consumed
+//   warp 9      TMEM allocation; lane 0 issues the MMAs of group 0
+//   warp 10     lane 0 issues the MMAs of group 1
+//
+// A row thread holds its 64 scores of a tile in registers (one 64-column TMEM
+// load), so its row maximum and sums need no exchange.  It writes
+// P = 2^(a log2(e) / sqrt(d) - m2ref) of kept elements (0 elsewhere) as fp16
+// pairs over the first 32 columns of S, and O += P V takes P straight from
+// TMEM; it is issued only when some row of the group kept an element.
+// 64-key tiles make QK^T an N = 64 MMA (two thirds of the N = 128 rate, by
+// measurement) but give each group two S buffers within the 512 TMEM columns,
+// so the next QK^T never waits for the rows.
+//
+// Pre-softmax (keep a >= theta) needs no row statistic before the decision, so
+// one pass does S, P and P.V together.  m2ref is a running reference per row
+// that is raised only when the row maximum passes it by more than 15 (log2
+// units, so P < 2^15 stays finite in fp16); then O, R and the row sum are rescaled by
+// 2^(old - new) -- in a causal row that happens a few times at most.
+// Post-softmax (keep s >= theta, i.e. a >= m + ln theta + ln Z) needs the row
+// maximum and sum first: pass 1 computes them, pass 2 recomputes S and applies
+// the bound with m2ref = the row maximum.
 //
 // P is fp16: rounding it to bf16 costs up to ~2e-3 relative output error on
 // peaked rows, fp16 ~3e-4.  One MMA takes A and B in the same 16-bit type, so
@@ -35,6 +46,8 @@
 // bf16 value above 2^-17 max|V| converts exactly; O is multiplied by 2^e.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <cfloat>
 #include <mutex>
 
 #include "common.cuh"
@@ -46,23 +59,17 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128;          // query rows per CTA = TMEM lanes
-constexpr int BN = 128;          // keys per tile
-constexpr int KST = 3;           // K ring stages (= score buffers: a finished QK^T frees both)
-constexpr int VST = 2;           // V ring stages
-constexpr int SBUF = 3;          // score buffers in TMEM
-constexpr int kRowWarps = 16;    // four warps per TMEM lane quadrant
-constexpr int kParts = kRowWarps / 4;  // parts of a score row (one per warp of a quadrant)
-constexpr int CP = BN / kParts;        // score columns of one part
-constexpr int kProducerWarp = kRowWarps;   // TMA: Q and K
-constexpr int kMmaWarp = kRowWarps + 1;    // issues QK^T; allocates TMEM
-constexpr int kPvWarp = kRowWarps + 2;     // issues P.V
-constexpr int kVProducerWarp = kRowWarps + 3;  // TMA: V (waits on P.V, so apart from K)
-constexpr int kTcThreads = 32 * (kRowWarps + 4);
-constexpr uint32_t kTmemCols = 512;  // score buffers at columns 0, 128, 256; O at 384
-constexpr uint32_t kOCol = 384;
+constexpr int BM = 128;          // query rows per head block = TMEM lanes
+constexpr int BN = 64;           // keys per tile
+constexpr int kGroups = 2;       // head blocks per CTA (at most)
+constexpr int kRowThreads = 128 * kGroups;
+constexpr int kProducerWarp = 8;
+constexpr int kIssueWarp = 9;    // + group; warp 9 also allocates TMEM
+constexpr int kTcThreads = 32 * 11;
+constexpr uint32_t kTmemCols = 512;  // S buffer b of group g at 128 g + 64 b; O of group g at 256 + 128 g
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazy = 15.f;        // headroom of the running reference (log2 units; P < 2^15 fits fp16)
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).  Operand
 // tiles are stored as the 128-byte-swizzle layout TMA writes: rows of 128
@@ -72,34 +79,36 @@ struct TcLayout {
   static constexpr int NP = D / 64;          // 64-element panels along d
   static constexpr uint32_t QP = BM * 128;   // one Q panel
   static constexpr uint32_t KP = BN * 128;   // one K or V panel
+  static constexpr uint32_t QT = NP * QP;    // one Q block
+  static constexpr uint32_t TILE = NP * KP;  // one K or V tile = one ring slot
+  static constexpr int NS = 8;               // ring slots
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K = Q + NP * QP;
-  static constexpr uint32_t V = K + KST * NP * KP;
-  static constexpr uint32_t BAR = V + VST * NP * KP;
-  // barriers: Q full; K full; V full/empty; S full (the QK^T of a score
-  // buffer finished, which also frees the K stage of the same index); S read
-  // by the rows; P.V done (frees a score buffer holding P); P full; O ready;
-  // drains of the two MMA threads
-  static constexpr int B_Q = 0, B_KF = 1, B_VF = B_KF + KST, B_VE = B_VF + VST,
-                       B_SF = B_VE + VST, B_SR = B_SF + SBUF, B_PD = B_SR + SBUF,
-                       B_PF = B_PD + SBUF, B_O = B_PF + SBUF, B_DRAIN = B_O + 1,
-                       NBAR = B_DRAIN + 2;
-  // misc words: abort flag, TMEM address, O written; any-kept flags [SBUF][kRowWarps] bytes
+  static constexpr uint32_t RING = Q + kGroups * QT;
+  static constexpr uint32_t BAR = RING + NS * TILE;
+  // barriers: Q full [group]; slot full / empty (empty counts one arrival per
+  // group); per group and S buffer ([2 g + b]): S full (its QK^T finished),
+  // S read (pass-1 rows loaded S), P full (the rows wrote P), P.V done (or
+  // skipped); per group: O final, MMA drain
+  static constexpr int B_Q = 0, B_FULL = B_Q + kGroups, B_EMPTY = B_FULL + NS,
+                       B_SF = B_EMPTY + NS, B_SR = B_SF + 2 * kGroups, B_PF = B_SR + 2 * kGroups,
+                       B_PD = B_PF + 2 * kGroups, B_O = B_PD + 2 * kGroups, B_DRAIN = B_O + kGroups,
+                       NBAR = B_DRAIN + kGroups;
+  // misc words: abort flag, TMEM address, O written [group]; any-kept flags
+  // [group][S buffer][4 warps]
   static constexpr uint32_t MISC = BAR + NBAR * 8;
-  static constexpr uint32_t ANY = (MISC + 16 + 7) & ~7u;
-  // row statistics of the parts of each row: [kParts][BM] float2, twice
-  static constexpr uint32_t XCH1 = ANY + SBUF * kRowWarps;
-  static constexpr uint32_t XCH2 = XCH1 + kParts * BM * 8;
-  static constexpr uint32_t BYTES = XCH2 + kParts * BM * 8;
+  static constexpr uint32_t ANY = MISC + 16;
+  static constexpr uint32_t BYTES = ANY + kGroups * 2 * 4;
   static constexpr uint32_t ALLOC = BYTES + 1024;  // room to align the base
-  static_assert(KST * NP * KP >= BM * (D + 4) * 4, "output staging fits in the K stages");
-  static_assert(kParts * BM * 8 >= BM * 4, "row betas fit in the first exchange area");
-  static_assert(VST * NP * KP >= (1 + 32 * kRowWarps / (D / 4)) * D * 4, "scan sums fit in the V stages");
-  static_assert(kRowWarps % 8 == 0, "8-byte words of any-kept flags per P buffer");
-  static_assert(KST == SBUF, "a K stage is freed by the QK^T of the score buffer of the same index");
+  // epilogue: both output blocks staged in the ring (16-byte chunks swizzled
+  // by row), the row betas and the VMC scan sums in the idle Q blocks
+  static constexpr uint32_t STAGE = RING;
+  static constexpr uint32_t BETAS = Q;
+  static constexpr uint32_t SCAN = Q + kGroups * BM * 4;
+  static_assert(kGroups * BM * D * 4 <= NS * TILE, "output staging fits in the ring");
+  static_assert(SCAN + (1 + kRowThreads / (D / 4)) * D * 4 <= RING, "scan sums fit in the Q blocks");
   static_assert(ALLOC <= 227 * 1024, "shared memory");
-  static_assert(ANY % 8 == 0 && XCH1 % 8 == 0 && XCH2 % 8 == 0, "8-byte words and float2");
-  static_assert(V % 1024 == 0 && K % 1024 == 0 && Q % 1024 == 0, "128-byte-swizzle tiles");
+  static_assert(MISC % 8 == 0 && ANY % 4 == 0, "alignment");
+  static_assert(RING % 1024 == 0 && TILE % 1024 == 0 && QT % 1024 == 0, "128-byte-swizzle tiles");
 };
 
 struct TcParams {
@@ -125,9 +134,9 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Barrier of the row threads only.
+// Barrier of the row threads of both groups.
 __device__ __forceinline__ void rows_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kRowWarps) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -135,42 +144,94 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int D>
+// Largest of the BN scores of a tile (three-input max, four chains).
+__device__ __forceinline__ float row_max(const uint32_t (&v)[BN]) {
+  float mx[4] = {__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                 __uint_as_float(v[3])};
+#pragma unroll
+  for (int c = 4; c < BN; c += 8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      mx[q] = fmax3(mx[q], __uint_as_float(v[c + 2 * q]), __uint_as_float(v[c + 2 * q + 1]));
+  }
+  return fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+}
+
+// Weights of 32 scores v[c0 .. c0 + 31]: P = 2^(a c2 - m2ref) where a >= braw
+// (0 elsewhere) packed as fp16 pairs into w[c0 / 2 ..], with the sums of P,
+// of the kept indicator and of 2^(a c2 - m2ref) over every element.
+// Hidden keys hold -inf: weight 0, never kept (braw is finite or -FLT_MAX).
+__device__ __forceinline__ void chunk_weights(const uint32_t (&v)[BN], int c0, float2 cc, float2 mm,
+                                              float braw, uint32_t (&w)[BN / 2], float2& tR,
+                                              float2& tK, float2& tZ) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float a0 = __uint_as_float(v[c0 + c]), a1 = __uint_as_float(v[c0 + c + 1]);
+    const float2 y = ffma2(make_float2(a0, a1), cc, mm);
+    const float2 e = make_float2(ex2(y.x), ex2(y.y));
+    tZ = fadd2(tZ, e);
+    const float2 k = make_float2(setge(a0, braw), setge(a1, braw));
+    const float2 pw = fmul2(e, k);
+    tR = fadd2(tR, pw);
+    tK = fadd2(tK, k);
+    w[(c0 + c) >> 1] = pack_half2(pw.x, pw.y);
+  }
+}
+
+// Key tiles are taken from the diagonal backwards (tile nt-1 first): in a
+// causal row the largest scores tend to be near the diagonal, so the running
+// reference of the pre-softmax pass is seldom raised after its first tile.
+// Load sequence of one CTA (the order the MMAs consume tiles), with
+// T_u = tile nt-1-u:
+//   post-softmax: K(T_0) .. K(T_{nt-1}) (pass 1), then K(T_0) V(T_0) K(T_1) V(T_1) ... (pass 2)
+//   pre-softmax:  K(T_0) V(T_0) K(T_1) V(T_1) ...
+// Load n goes to ring slot n % NS, its (n / NS)-th use.  QK^T number j of a
+// group (pass-1 tiles first, then pass-2 tiles) uses S buffer j % 2; the
+// per-buffer barriers complete once per use of their buffer, so a use's
+// parity is (its index among that buffer's uses) & 1.
+template <int D, int NQ>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
   using L = TcLayout<D>;
+  constexpr int NS = L::NS;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   unsigned char* gb = smem_raw + (sb - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::MISC);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gb + L::MISC + 4);
-  volatile int* o_written = reinterpret_cast<volatile int*>(gb + L::MISC + 8);
-  volatile uint8_t* anyf = reinterpret_cast<volatile uint8_t*>(gb + L::ANY);  // [SBUF][kRowWarps]
+  volatile int* o_written = reinterpret_cast<volatile int*>(gb + L::MISC + 8);  // [group]
+  volatile uint8_t* anyf = reinterpret_cast<volatile uint8_t*>(gb + L::ANY);    // [group][4]
   auto bar = [sb](int i) -> uint32_t { return sb + L::BAR + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // heaviest row blocks (most causal key tiles) first
-  const int per = p.Hq * p.B;
+  const int hgroups = p.Hq / NQ;
+  const int per = p.B * hgroups;
   const int qb = p.nqb - 1 - (int)(blockIdx.x / per);
   const int rem = (int)(blockIdx.x % per);
-  const int h = rem % p.Hq, b = rem / p.Hq;
-  const int kvh = h / (p.Hq / p.Hkv);
+  const int h0 = (rem % hgroups) * NQ, b = rem / hgroups;
+  const int kvh = h0 / (p.Hq / p.Hkv);
   const int row0 = qb * BM;
   const int nt = (min(row0 + BM, p.S) - 1) / BN + 1;  // causal key tiles
-  const int bh_q = b * p.Hq + h, bh_kv = b * p.Hkv + kvh;
+  const int bh_kv = b * p.Hkv + kvh;
+  const bool pre = p.mode == TOPT_PRE;
+  const int P1 = pre ? 0 : nt;  // pass-1 tiles
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
-      const bool per_warp = (i >= L::B_SR && i < L::B_SR + SBUF) || (i >= L::B_PF && i < L::B_PF + SBUF);
-      mbar_init(bar(i), per_warp ? kRowWarps : (i == L::B_O ? 2 : 1));
+      uint32_t count = 1;
+      if (i >= L::B_EMPTY && i < L::B_EMPTY + NS) count = NQ;
+      if ((i >= L::B_SR && i < L::B_SR + 2 * kGroups) || (i >= L::B_PF && i < L::B_PF + 2 * kGroups))
+        count = 4;
+      mbar_init(bar(i), count);
     }
     *abort_flag = 0;
-    *o_written = 0;
+    o_written[0] = o_written[1] = 0;
     mbar_init_fence();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kIssueWarp) {
     tmem_alloc(smem_u32(gb + L::MISC + 4), kTmemCols);
     tmem_relinquish();
   }
@@ -185,138 +246,116 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kProducerWarp) {
-    // --------------------------------------------------- producer: Q and K
+    // ------------------------------------------------ producer: Q, K, V
     if (lane == 0) {
-      int kcount[KST] = {};
-      int ks = 0, kph = 0;
-      mbar_expect_tx(bar(L::B_Q), L::NP * L::QP);
-      for (int pn = 0; pn < L::NP; ++pn)
-        tma_load_3d(sb + L::Q + pn * L::QP, &tmQ, bar(L::B_Q), 64 * pn, row0, bh_q);
-      for (int tt = 0; tt < 2 * nt; ++tt) {
-        const int kt = tt < nt ? tt : tt - nt;
-        if (p.withhold_k && tt == 0) {  // the QK^T thread's first wait must run out
-          if (++ks == KST) { ks = 0; kph ^= 1; }
-          continue;
-        }
-        if (!mbar_wait(bar(L::B_SF + ks), kph ^ 1, abort_flag)) break;
-        mbar_expect_tx(bar(L::B_KF + ks), L::NP * L::KP);
+      for (int g = 0; g < NQ; ++g) {
+        mbar_expect_tx(bar(L::B_Q + g), L::QT);
         for (int pn = 0; pn < L::NP; ++pn)
-          tma_load_3d(sb + L::K + (ks * L::NP + pn) * L::KP, &tmK, bar(L::B_KF + ks), 64 * pn,
-                      kt * BN, bh_kv);
-        ++kcount[ks];
-        if (++ks == KST) { ks = 0; kph ^= 1; }
+          tma_load_3d(sb + L::Q + g * L::QT + pn * L::QP, &tmQ, bar(L::B_Q + g), 64 * pn, row0,
+                      b * p.Hq + h0 + g);
+      }
+      const int nseq = P1 + 2 * nt;
+      bool v_ready = false;
+      int issued = 0;
+      for (int n = 0; n < nseq; ++n) {
+        const int s = n % NS;
+        if (n >= NS && !mbar_wait(bar(L::B_EMPTY + s), ((n / NS) - 1) & 1, abort_flag)) break;
+        const bool isv = n >= P1 && ((n - P1) & 1);
+        const int tile = nt - 1 - (n < P1 ? n : (n - P1) >> 1);
+        if (isv && !v_ready) {
+          pdl_wait();  // the fp16 copy of V is written by the previous grid
+          v_ready = true;
+        }
+        issued = n + 1;
+        if (p.withhold_k && n == 0) continue;  // the first wait on slot 0 must run out
+        mbar_expect_tx(bar(L::B_FULL + s), L::TILE);
+        for (int pn = 0; pn < L::NP; ++pn)
+          tma_load_3d(sb + L::RING + s * L::TILE + pn * L::KP, isv ? &tmV : &tmK, bar(L::B_FULL + s),
+                      64 * pn, tile * BN, bh_kv);
       }
       // every copy this thread issued lands before the CTA releases its memory
-      bool drained = mbar_wait_drain(bar(L::B_Q), 0);
-      for (int s = 0; s < KST; ++s)
-        if (kcount[s]) drained &= mbar_wait_drain(bar(L::B_KF + s), (kcount[s] - 1) & 1);
-      if (!drained) set_status(p.status, TOPT_ETIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == kVProducerWarp) {
-    // ----------------------------------------------------- producer: V
-    if (lane == 0) {
-      int vcount[VST] = {};
-      int vs = 0, vph = 0;
-      pdl_wait();  // the fp16 copy of V is written by the previous grid
-      for (int u = 0; u < nt; ++u) {
-        if (!mbar_wait(bar(L::B_VE + vs), vph ^ 1, abort_flag)) break;
-        mbar_expect_tx(bar(L::B_VF + vs), L::NP * L::KP);
-        for (int pn = 0; pn < L::NP; ++pn)
-          tma_load_3d(sb + L::V + (vs * L::NP + pn) * L::KP, &tmV, bar(L::B_VF + vs), 64 * pn,
-                      u * BN, bh_kv);
-        ++vcount[vs];
-        if (++vs == VST) { vs = 0; vph ^= 1; }
-      }
       bool drained = true;
-      for (int s = 0; s < VST; ++s)
-        if (vcount[s]) drained &= mbar_wait_drain(bar(L::B_VF + s), (vcount[s] - 1) & 1);
+      for (int g = 0; g < NQ; ++g) drained &= mbar_wait_drain(bar(L::B_Q + g), 0);
+      for (int n = max(0, issued - NS); n < issued; ++n)
+        if (!(p.withhold_k && n == 0)) drained &= mbar_wait_drain(bar(L::B_FULL + n % NS), (n / NS) & 1);
       if (!drained) set_status(p.status, TOPT_ETIMEOUT);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ QK^T MMA
-    if (lane == 0) {
+  } else if (warp >= kIssueWarp) {
+    // ------------------------------------------- MMAs of one group (head)
+    const int g = warp - kIssueWarp;
+    if (lane == 0 && g < NQ) {
       constexpr uint32_t idS = idesc_f16(BN, 1, 1, 0);  // bf16 Q, bf16 K (K-major)
+      constexpr uint32_t idO = idesc_f16(D, 0, 0, 1);   // fp16 P (TMEM), fp16 V (N-major)
       // descriptor words: every shared operand has 8-row groups 1024 bytes apart
       constexpr uint32_t hi = sdesc_hi(1024);
-      const uint32_t q_lo = sdesc_lo(sb + L::Q, 16);
-      const uint32_t k_lo = sdesc_lo(sb + L::K, 16);
-      uint32_t pd_par = 0;  // per score buffer: parity of its next P.V-done phase
-      bool ok = mbar_wait(bar(L::B_Q), 0, abort_flag);
-      int sbuf = 0, use = 0;  // score buffer (= K stage) of tile tt and its use count
-      for (int tt = 0; ok && tt < 2 * nt; ++tt) {
-        if (!(ok = mbar_wait(bar(L::B_KF + sbuf), use & 1, abort_flag))) break;
-        if (tt >= SBUF) {
-          if (tt - SBUF >= nt) {
-            // the buffer held P of a pass-2 tile: P.V done (the rows read S
-            // before they wrote P)
-            ok = mbar_wait(bar(L::B_PD + sbuf), (pd_par >> sbuf) & 1, abort_flag);
-            pd_par ^= 1u << sbuf;
-          } else {
-            ok = mbar_wait(bar(L::B_SR + sbuf), (use & 1) ^ 1, abort_flag);
-          }
-          if (!ok) break;
+      const uint32_t q_lo = sdesc_lo(sb + L::Q + g * L::QT, 16);
+      const uint32_t k_lo = sdesc_lo(sb + L::RING, 16);
+      const uint32_t v_lo = sdesc_lo(sb + L::RING, L::KP);
+      const uint32_t sO = tmem + 256u + 128u * g;
+      bool ok = mbar_wait(bar(L::B_Q + g), 0, abort_flag);
+      const int nq = P1 + nt;  // QK^T of this group
+      // QK^T number j into S buffer j % 2, once the buffer's previous user
+      // (j - 2) is released: read by the pass-1 rows, or its P.V done
+      auto qk = [&](int j) -> bool {
+        const int bb = j & 1;
+        const int n = j < P1 ? j : P1 + 2 * (j - P1);  // load holding K of QK^T j
+        const int s = n % NS;
+        if (!mbar_wait(bar(L::B_FULL + s), (n / NS) & 1, abort_flag)) return false;
+        const int prev = j - 2;
+        if (prev >= 0) {
+          const bool r1 = prev < P1;
+          const int idx = r1 ? prev >> 1 : (prev - P1) >> 1;
+          if (!mbar_wait(bar((r1 ? L::B_SR : L::B_PD) + 2 * g + bb), idx & 1, abort_flag)) return false;
         }
         tc_fence_after();
-        const uint32_t ka = k_lo + sbuf * (L::NP * L::KP >> 4);
+        const uint32_t ka = k_lo + s * (L::TILE >> 4);
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s)
-          tc_mma_f16_w(tmem + (uint32_t)sbuf * BN, q_lo + (s >> 2) * (L::QP >> 4) + 2 * (s & 3),
-                       ka + (s >> 2) * (L::KP >> 4) + 2 * (s & 3), hi, idS, (uint32_t)s);
-        tc_commit(bar(L::B_SF + sbuf));
-        if (++sbuf == SBUF) { sbuf = 0; ++use; }
-      }
-      tc_commit(bar(L::B_DRAIN));
-      const bool drained = mbar_wait_drain(bar(L::B_DRAIN), 0);
-      if (!ok || !drained) set_status(p.status, TOPT_ETIMEOUT);
-    }
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // ------------------------------------------------------------- P.V MMA
-    if (lane == 0) {
-      constexpr uint32_t idO = idesc_f16(D, 0, 0, 1);  // fp16 P (TMEM), fp16 V (N-major)
-      constexpr uint32_t hi = sdesc_hi(1024);
-      const uint32_t v_lo = sdesc_lo(sb + L::V, L::KP);
-      volatile unsigned long long* any8 = reinterpret_cast<volatile unsigned long long*>(anyf);
-      uint32_t started = 0, pf_par = 0;
+        for (int k = 0; k < D / 16; ++k)
+          tc_mma_f16_w(tmem + 128u * g + 64u * bb, q_lo + (k >> 2) * (L::QP >> 4) + 2 * (k & 3),
+                       ka + (k >> 2) * (L::KP >> 4) + 2 * (k & 3), hi, idS, (uint32_t)k);
+        tc_commit(bar(L::B_SF + 2 * g + bb));
+        tc_commit(bar(L::B_EMPTY + s));
+        return true;
+      };
+      uint32_t started = 0;
       unsigned long long executed = 0;
-      int vs = 0, vph = 0;  // V stage and phase
-      bool ok = true;
+      // pass 1: two QK^T ahead of the rows
+      for (int j = 0; ok && j < P1; ++j) ok = qk(j);
+      // pass 2 / single pass: the first two QK^T, then per tile P.V and the
+      // QK^T two tiles on
+      for (int j = P1; ok && j < min(nq, P1 + 2); ++j) ok = qk(j);
       for (int u = 0; ok && u < nt; ++u) {
-        const int sbuf = (nt + u) % SBUF;
-        if (!(ok = mbar_wait(bar(L::B_PF + sbuf), (pf_par >> sbuf) & 1, abort_flag))) break;
-        pf_par ^= 1u << sbuf;
-        bool any = false;
-#pragma unroll
-        for (int q = 0; q < kRowWarps / 8; ++q) any |= any8[sbuf * (kRowWarps / 8) + q] != 0ull;
-        if (!(ok = mbar_wait(bar(L::B_VF + vs), vph, abort_flag))) break;
+        const int bb = (P1 + u) & 1;
+        const int sv = (P1 + 2 * u + 1) % NS, nv = P1 + 2 * u + 1;  // load holding V of tile u
+        if (!(ok = mbar_wait(bar(L::B_PF + 2 * g + bb), (u >> 1) & 1, abort_flag))) break;
+        const bool any = *reinterpret_cast<volatile uint32_t*>(anyf + 8 * g + 4 * bb) != 0u;
+        // the slot is released only after its bytes arrived, also when unused
+        if (!(ok = mbar_wait(bar(L::B_FULL + sv), (nv / NS) & 1, abort_flag))) break;
         if (any) {
           tc_fence_after();
-          // P of key j = CP q + c sits in column CP q + c / 2 of the score buffer
-          const uint32_t pa = tmem + (uint32_t)sbuf * BN;
-          const uint32_t va = v_lo + vs * (L::NP * L::KP >> 4);
+          // P of keys 2c, 2c + 1 sits in column c of S
+          const uint32_t pa = tmem + 128u * g + 64u * bb;
+          const uint32_t va = v_lo + sv * (L::TILE >> 4);
 #pragma unroll
-          for (int s = 0; s < BN / 16; ++s)
-            tc_mma_f16_ts(tmem + kOCol, pa + CP * (16 * s / CP) + (16 * s % CP) / 2, va + 128 * s, hi,
-                          idO, started | (uint32_t)s);
+          for (int k = 0; k < BN / 16; ++k)
+            tc_mma_f16_ts(sO, pa + 8 * k, va + 128 * k, hi, idO, started | (uint32_t)k);
           started = 1;
           ++executed;
-          tc_commit(bar(L::B_PD + sbuf));
-          tc_commit(bar(L::B_VE + vs));
+          tc_commit(bar(L::B_PD + 2 * g + bb));
+          tc_commit(bar(L::B_EMPTY + sv));
         } else {
-          mbar_arrive(bar(L::B_PD + sbuf));
-          mbar_arrive(bar(L::B_VE + vs));
+          mbar_arrive(bar(L::B_PD + 2 * g + bb));
+          mbar_arrive(bar(L::B_EMPTY + sv));
         }
-        if (++vs == VST) { vs = 0; vph ^= 1; }
+        if (P1 + u + 2 < nq) ok = qk(P1 + u + 2);
       }
-      if (ok) {
-        *o_written = (int)started;
-        tc_commit(bar(L::B_O));
-        mbar_arrive(bar(L::B_O));
+      tc_commit(bar(L::B_DRAIN + g));
+      const bool drained = mbar_wait_drain(bar(L::B_DRAIN + g), 0);
+      if (ok && drained) {
+        o_written[g] = (int)started;
+        mbar_arrive(bar(L::B_O + g));  // releases o_written and the finished O
       }
-      tc_commit(bar(L::B_DRAIN + 1));
-      const bool drained = mbar_wait_drain(bar(L::B_DRAIN + 1), 0);
       if (!ok || !drained) set_status(p.status, TOPT_ETIMEOUT);
       if (p.tiles) {
         atomicAdd(p.tiles + 0, executed);
@@ -326,230 +365,207 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- query rows
-    // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows) and columns
-    // CP (w / 4) .. + CP - 1 of each score tile: each row is split in kParts.
-    const int quad = warp & 3, part = warp >> 2;
+    // Thread = row r of group g's head block: TMEM lane r of S and O.
+    const int g = warp >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
     const int i = row0 + r;
-    const bool row_ok = i < p.S;
-    const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(CP * part);
+    const bool active = g < NQ;
+    const bool row_ok = active && i < p.S;
+    const int h = h0 + g, bh_q = b * p.Hq + h;
+    const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+    const uint32_t sS = tmem + lanes + 128u * g, sO = tmem + lanes + 256u + 128u * g;
     const float c2 = p.sm_scale * kLog2e;
-    bool ok = true;
-
-    // pass 1: m2 = max_j a_j log2(e), z = sum_j 2^(a_j log2(e) - m2) over this part
-    float m2 = -CUDART_INF_F, z = 0.f;
-    for (int t = 0; t < nt; ++t) {
-      const int sbuf = t % SBUF;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[CP];
-      tmem_ld<CP>(trow + (uint32_t)sbuf * BN, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
-      const int lim = i - t * BN - CP * part;  // columns c <= lim of this part are visible
-      if (!__all_sync(0xffffffffu, lim >= CP - 1)) {
+    const int Lrow = i + 1;
+    const float th = row_ok ? p.theta[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)] : 0.f;
+    bool ok = active;
+    uint32_t v[BN];
+    // hidden keys of key tile t (beyond the row, or the whole row when
+    // i >= S) -> -inf
+    auto hide = [&](int t) {
+      const int lim = row_ok ? i - t * BN : -1;  // columns c <= lim are visible
+      if (!__all_sync(0xffffffffu, lim >= BN - 1)) {
 #pragma unroll
-        for (int c = 0; c < CP; ++c)
+        for (int c = 0; c < BN; ++c)
           if (c > lim) v[c] = __float_as_uint(-CUDART_INF_F);
       }
-      // maximum by three-input max (two new scores per instruction), four chains
-      float mx[4] = {__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
-                     __uint_as_float(v[3])};
-#pragma unroll
-      for (int c = 4; c < CP; c += 8) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          mx[q] = fmax3(mx[q], __uint_as_float(v[c + 2 * q]), __uint_as_float(v[c + 2 * q + 1]));
-      }
-      const float mn = fmaxf(m2, fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c2);
-      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden part so far
-      // 2^(a log2(e) - mref) by packed fma, summed by packed add (two chains)
-      float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    };
+
+    // pass 1 (post-softmax): m2 = max_j a_j c2, z = sum_j 2^(a_j c2 - m2)
+    float m2 = -CUDART_INF_F, z = 0.f;
+    for (int t = 0; ok && t < P1; ++t) {
+      const int bb = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + 2 * g + bb), (t >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      tmem_ld<BN>(sS + 64u * bb, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_SR + 2 * g + bb));  // S may be overwritten now
+      hide(nt - 1 - t);
+      const float mn = fmaxf(m2, row_max(v) * c2);
+      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden row so far
+      // 2^(a c2 - mref) by packed fma, summed by packed add (four chains)
+      float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
       const float2 cc = make_float2(c2, c2), mm = make_float2(-mref, -mref);
 #pragma unroll
-      for (int c = 0; c < CP; c += 2) {
+      for (int c = 0; c < BN; c += 2) {
         const float2 y = ffma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), cc, mm);
-        sm[(c >> 1) & 1] = fadd2(sm[(c >> 1) & 1], make_float2(ex2(y.x), ex2(y.y)));
+        sm[(c >> 1) & 3] = fadd2(sm[(c >> 1) & 3], make_float2(ex2(y.x), ex2(y.y)));
       }
-      const float2 st2 = fadd2(sm[0], sm[1]);
+      const float2 st2 = fadd2(fadd2(sm[0], sm[1]), fadd2(sm[2], sm[3]));
       z = z * ex2(m2 - mref) + (st2.x + st2.y);
       m2 = mn;
     }
-    // merge the parts of the row in a fixed order, so every thread of the row
-    // gets bit-identical m2 and z (every row thread reaches this barrier, also
-    // after an abort)
-    {
-      float2* xch = reinterpret_cast<float2*>(gb + L::XCH1);
-      xch[part * BM + r] = make_float2(m2, z);
-      rows_sync();
-      float2 o[kParts];
-#pragma unroll
-      for (int q = 0; q < kParts; ++q) o[q] = xch[q * BM + r];
-      float M = o[0].x;
-#pragma unroll
-      for (int q = 1; q < kParts; ++q) M = fmaxf(M, o[q].x);
-      float Z = 0.f;
-#pragma unroll
-      for (int q = 0; q < kParts; ++q) Z += o[q].y * ex2(o[q].x - M);
-      m2 = M;
-      z = Z;
-    }
-    const float m = m2 * kLn2;
-    const int Lrow = i + 1;
-    const float th = row_ok ? p.theta[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)] : 0.f;
-    const float bound = score_bound(p.mode, th, m, z);
-    const float braw = bound / p.sm_scale;  // keep iff raw score >= braw
+    // keep iff the raw score a * sqrt(d) >= braw; a hidden key (-inf) never
+    // passes the finite bound
+    const float braw = fmaxf((pre ? th : score_bound(p.mode, th, m2 * kLn2, z)) / p.sm_scale, -FLT_MAX);
 
-    // pass 2: keep on visible keys; P = exp(a - m) where kept, 0 elsewhere,
-    // written as fp16 pairs over the first half of this thread's columns.  R
-    // sums the fp32 weights (P.V multiplies them rounded to fp16: relative
-    // difference below 2^-11 per weight).
-    float R0 = 0.f, R1 = 0.f;
-    int cnt = 0;
+    // pass 2 (post) or the single pass (pre): P where kept.  R sums the fp32
+    // weights (P.V multiplies them rounded to fp16: relative difference below
+    // 2^-11 per weight).  Pre: m2ref follows the row maximum, Z sums every
+    // weight (used by exact SDC; one packed add per two keys, cheaper than a
+    // second code path), m2max is the row maximum.
+    float m2ref = pre ? -CUDART_INF_F : m2, m2max = -CUDART_INF_F;
+    float R = 0.f, KEPT = 0.f, Z = 0.f;
     uint32_t* mrow = (p.mask && row_ok) ? p.mask + ((size_t)bh_q * p.S + i) * p.mask_words : nullptr;
     for (int u = 0; ok && u < nt; ++u) {
-      const int t = nt + u, sbuf = t % SBUF;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + sbuf), (t / SBUF) & 1, abort_flag));
+      const int j = P1 + u, bb = j & 1;
+      const uint32_t sSb = sS + 64u * bb;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + 2 * g + bb), (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[CP];
-      tmem_ld<CP>(trow + (uint32_t)sbuf * BN, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_SR + sbuf));
-      const int lim = row_ok ? i - u * BN - CP * part : -1;
-      if (!__all_sync(0xffffffffu, lim >= CP - 1)) {
-        // hidden keys compare false against any bound (NaN)
-#pragma unroll
-        for (int c = 0; c < CP; ++c)
-          if (c > lim) v[c] = 0x7fc00000u;
-      }
-      // exponentials only in 8-key chunks where some row of the warp keeps a
-      // key (the chunk maximum against the bound decides)
-      uint32_t w[CP / 2];
-      int tcnt = 0;
-      bool wany = false;
-#pragma unroll
-      const float2 cc = make_float2(c2, c2), mm = make_float2(-m2, -m2);
-      float2 Rp = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < CP / 8; ++j) {
-        const float* vj = reinterpret_cast<const float*>(v) + 8 * j;
-        const float cm = fmax3(fmax3(vj[0], vj[1], vj[2]), fmax3(vj[3], vj[4], vj[5]),
-                               fmaxf(vj[6], vj[7]));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[4 * j + e] = 0u;
-        if (__any_sync(0xffffffffu, cm >= braw)) {
-          wany = true;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a0 = vj[2 * e], a1 = vj[2 * e + 1];
-            const bool q0 = a0 >= braw, q1 = a1 >= braw;
-            const float2 y = ffma2(make_float2(a0, a1), cc, mm);
-            const float e0 = ex2(q0 ? y.x : -CUDART_INF_F);
-            const float e1 = ex2(q1 ? y.y : -CUDART_INF_F);
-            Rp = fadd2(Rp, make_float2(e0, e1));
-            tcnt += (int)q0 + (int)q1;
-            w[4 * j + e] = pack_half2(e0, e1);
-          }
+      tmem_ld<BN>(sSb, v);
+      const int tile = nt - 1 - u;
+      hide(tile);
+      float factor = 1.f;
+      bool rescale_o = false;
+      if (pre) {
+        const float t2 = row_max(v) * c2;
+        m2max = fmaxf(m2max, t2);
+        if (t2 > m2ref + kLazy) {  // -inf + kLazy = -inf: the first visible tile
+          rescale_o = m2ref != -CUDART_INF_F;
+          factor = rescale_o ? ex2(m2ref - t2) : 0.f;
+          m2ref = t2;
+          R *= factor;
+          Z *= factor;
         }
       }
-      R0 += Rp.x;
-      R1 += Rp.y;
-      tmem_st<CP / 2>(trow + (uint32_t)sbuf * BN, w);
-      tc_fence_before();
-      if (lane == 0) anyf[sbuf * kRowWarps + warp] = wany ? 1 : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_PF + sbuf));
-      cnt += tcnt;
-      if (mrow) {
+      const float mref = m2ref == -CUDART_INF_F ? 0.f : m2ref;
+      const float2 cc = make_float2(c2, c2), mm = make_float2(-mref, -mref);
+      // all P words first, then one store: the scores of a chunk are dead
+      // once its words and mask bits exist
+      float2 tR = make_float2(0.f, 0.f), tK = make_float2(0.f, 0.f), tZ = make_float2(0.f, 0.f);
+      uint32_t w[BN / 2];
 #pragma unroll
-        for (int q = 0; q < CP / 32; ++q) {
+      for (int q = 0; q < BN / 32; ++q) {
+        chunk_weights(v, 32 * q, cc, mm, braw, w, tR, tK, tZ);
+        if (mrow) {
           uint32_t k = 0u;
 #pragma unroll
           for (int c = 0; c < 32; ++c) k |= (uint32_t)(__uint_as_float(v[32 * q + c]) >= braw) << c;
-          const int wd = (BN / 32) * u + (CP / 32) * part + q;
+          const int wd = (BN / 32) * tile + q;
           if (wd < p.mask_words) mrow[wd] = k;
         }
       }
-    }
-    float R = R0 + R1;
-    if (mrow)
-      for (int wd = (BN / 32) * nt + (CP / 32) * part; wd < p.mask_words; wd += BN / 32)
-        for (int q = 0; q < CP / 32 && wd + q < p.mask_words; ++q) mrow[wd + q] = 0u;
-    // merge R and the kept count of the parts, in a fixed order (every row
-    // thread reaches this barrier, also after an abort)
-    {
-      float2* xch = reinterpret_cast<float2*>(gb + L::XCH2);
-      xch[part * BM + r] = make_float2(R, __int_as_float(cnt));
-      rows_sync();
-      R = 0.f;
-      cnt = 0;
+      tmem_st<BN / 2>(sSb, w);  // waits for the store
+      const float tk = tK.x + tK.y;
+      R += tR.x + tR.y;
+      KEPT += tk;
+      Z += tZ.x + tZ.y;
+      if (pre && __any_sync(0xffffffffu, rescale_o)) {
+        // O += P V of the previous tile has finished; the next P.V of this
+        // group starts only after this warp signals P full
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(L::B_PD + 2 * g + (bb ^ 1)), ((u - 1) >> 1) & 1, abort_flag));
+        if (ok) {
+          // the whole O row in one load and one store (the score registers
+          // are free by now)
+          tc_fence_after();
+          uint32_t o[D];
+          tmem_ld<D>(sO, o);
 #pragma unroll
-      for (int q = 0; q < kParts; ++q) {
-        const float2 o = xch[q * BM + r];
-        R += o.x;
-        cnt += __float_as_int(o.y);
+          for (int k = 0; k < D; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * factor);
+          tmem_st_full<D>(sO, o);
+        }
       }
+      tc_fence_before();
+      const bool wany = __any_sync(0xffffffffu, tk > 0.f);
+      if (lane == 0) anyf[8 * g + 4 * bb + quad] = wany ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_PF + 2 * g + bb));
     }
+    if (mrow)
+      for (int wd = (BN / 32) * nt; wd < p.mask_words; ++wd) mrow[wd] = 0u;
+    const int cnt = (int)KEPT;
 
-    // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7].  The
-    // rows stage O * scale in shared memory (the K stages are idle by now),
-    // then all row threads stream the block out with coalesced 16-byte
-    // stores, adding beta mu (prefix means computed here) on the way.
-    constexpr int SD = D + 4;  // staging row stride in floats (conflict-free float4 writes)
-    float* stage = reinterpret_cast<float*>(gb + L::K);
-    float* betas = reinterpret_cast<float*>(gb + L::XCH1);  // free after the pass-1 merge
+    // epilogue: out = O * scale 2^e + beta mu   [TopTheta Eq. 4-7].  Both
+    // groups stage O * scale in shared memory (the ring is idle by now: every
+    // load of this CTA was consumed), then all row threads stream the blocks
+    // out with coalesced 16-byte stores, adding beta mu (prefix means of V,
+    // the same for both heads) on the way.
+    float* stage = reinterpret_cast<float*>(gb + L::STAGE);  // [group][BM][D], chunks swizzled by row
+    float* betas = reinterpret_cast<float*>(gb + L::BETAS);  // [group][BM]
+    auto chunk_at = [](int row, int c4) { return row * D + 4 * (c4 ^ (row & 7)); };
     pdl_wait();  // vexp and the block sums come from the preparation grids
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_O), 0, abort_flag));
+    // the staging area is the ring and the Q blocks: every MMA of both groups
+    // has finished reading them before any row writes there
+#pragma unroll
+    for (int gg = 0; gg < NQ; ++gg)
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_O + gg), 0, abort_flag));
     if (ok) {
       tc_fence_after();
-      const bool have_o = *o_written != 0;
+      const bool have_o = o_written[g] != 0;
       float sc = 0.f, beta = 0.f;
       if (row_ok) {
-        const float e_off = (p.mode == TOPT_PRE && p.sdc == TOPT_SDC_OFFLINE)
-                                ? p.e_tilde[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)]
-                                : 0.f;
-        out_scale_beta(p.mode, p.sdc, p.gamma, th, m, z, R, Lrow, cnt, e_off, sc, beta);
+        // pre-softmax sums are relative to 2^m2ref; the offline E~ is
+        // relative to the row maximum
+        const float mref = pre ? m2ref : m2;
+        float e_off = 0.f;
+        if (pre && p.sdc == TOPT_SDC_OFFLINE)
+          e_off = p.e_tilde[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)] * ex2(m2max - m2ref);
+        out_scale_beta(p.mode, p.sdc, p.gamma, th, mref * kLn2, pre ? Z : z, R, Lrow, cnt, e_off, sc,
+                       beta);
       }
       const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
-      constexpr int OC = D / kParts;  // output columns of this thread
-      const int c0 = OC * part;
-      uint32_t o[OC];
-      tmem_ld<OC>(tmem + ((uint32_t)(quad * 32) << 16) + kOCol + (uint32_t)c0, o);
+      float* st = stage + g * BM * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(sO + c, o);
 #pragma unroll
-      for (int c = 0; c < OC; c += 4) {
-        float4 val;
-        val.x = have_o ? __uint_as_float(o[c + 0]) * f : 0.f;
-        val.y = have_o ? __uint_as_float(o[c + 1]) * f : 0.f;
-        val.z = have_o ? __uint_as_float(o[c + 2]) * f : 0.f;
-        val.w = have_o ? __uint_as_float(o[c + 3]) * f : 0.f;
-        *reinterpret_cast<float4*>(stage + r * SD + c0 + c) = val;
+        for (int k = 0; k < 32; k += 4) {
+          float4 val;
+          val.x = have_o ? __uint_as_float(o[k + 0]) * f : 0.f;
+          val.y = have_o ? __uint_as_float(o[k + 1]) * f : 0.f;
+          val.z = have_o ? __uint_as_float(o[k + 2]) * f : 0.f;
+          val.w = have_o ? __uint_as_float(o[k + 3]) * f : 0.f;
+          *reinterpret_cast<float4*>(st + chunk_at(r, (c + k) / 4)) = val;
+        }
       }
-      if (part == 0) betas[r] = beta;
-      if (row_ok && part == 0 && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
+      betas[g * BM + r] = beta;
+      if (row_ok && p.kept) p.kept[(size_t)bh_q * p.S + i] = cnt;
     }
     rows_sync();  // every row thread reaches it, also after an abort
     const int rows_here = min(BM, p.S - row0);
-    float* out_blk = p.out + ((size_t)bh_q * p.S + row0) * D;
+    constexpr int QD = D / 4;  // 16-byte column chunks of a row
     if (!p.vmc) {
       if (!*abort_flag)
-        for (int idx = threadIdx.x; idx < rows_here * (D / 4); idx += 32 * kRowWarps) {
-          const int rr = idx / (D / 4), c = 4 * (idx % (D / 4));
-          *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) =
-              *reinterpret_cast<const float4*>(stage + rr * SD + c);
+        for (int idx = threadIdx.x; idx < NQ * rows_here * QD; idx += kRowThreads) {
+          const int gg = idx / (rows_here * QD), rr = (idx / QD) % rows_here, c4 = idx % QD;
+          float* out_blk = p.out + ((size_t)(b * p.Hq + h0 + gg) * p.S + row0) * D;
+          *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + 4 * c4) =
+              *reinterpret_cast<const float4*>(stage + gg * BM * D + chunk_at(rr, c4));
         }
     } else {
       // mu_i = (sum of V rows 0..i) / (i + 1): the column sums of the blocks
       // before this one plus a scan over this block's rows, by segments of
       // RPS rows (thread: 4 columns x RPS rows), in fp32 from the bf16 V.
-      constexpr int QD = D / 4, NSEG = 32 * kRowWarps / QD, RPS = BM / NSEG;
+      constexpr int NSEG = kRowThreads / QD, RPS = BM / NSEG;
       const int c4 = threadIdx.x % QD, seg = threadIdx.x / QD, c = 4 * c4;
-      float* pre = reinterpret_cast<float*>(gb + L::V);  // [D]: sum of V rows 0 .. row0-1
-      float* segsum = pre + D;                           // [NSEG][D]: totals of the segments
-      if (threadIdx.x < D) pre[threadIdx.x] = p.bsum[((size_t)bh_kv * p.nqb + qb) * D + threadIdx.x];
+      float* pre_sum = reinterpret_cast<float*>(gb + L::SCAN);  // [D]: sum of V rows 0 .. row0-1
+      float* segsum = pre_sum + D;                               // [NSEG][D]: totals of the segments
+      if (threadIdx.x < D) pre_sum[threadIdx.x] = p.bsum[((size_t)bh_kv * p.nqb + qb) * D + threadIdx.x];
       float4 run[RPS];
       float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
       const uint32_t* vblk = p.v + ((size_t)bh_kv * p.S + row0) * (D / 2);
@@ -568,7 +584,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       *reinterpret_cast<float4*>(segsum + seg * D + c) = tot;
       rows_sync();
       if (!*abort_flag) {
-        float4 base = *reinterpret_cast<const float4*>(pre + c);
+        float4 base = *reinterpret_cast<const float4*>(pre_sum + c);
         for (int q = 0; q < seg; ++q) {
           const float4 t4 = *reinterpret_cast<const float4*>(segsum + q * D + c);
           base.x += t4.x;
@@ -581,13 +597,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int rr = seg * RPS + k;
           if (rr < rows_here) {
             const float inv = 1.f / (float)(row0 + rr + 1);
-            const float bt = betas[rr];
-            float4 val = *reinterpret_cast<const float4*>(stage + rr * SD + c);
-            val.x = fmaf(bt, (base.x + run[k].x) * inv, val.x);
-            val.y = fmaf(bt, (base.y + run[k].y) * inv, val.y);
-            val.z = fmaf(bt, (base.z + run[k].z) * inv, val.z);
-            val.w = fmaf(bt, (base.w + run[k].w) * inv, val.w);
-            *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) = val;
+            const float4 mu = make_float4((base.x + run[k].x) * inv, (base.y + run[k].y) * inv,
+                                          (base.z + run[k].z) * inv, (base.w + run[k].w) * inv);
+#pragma unroll
+            for (int gg = 0; gg < NQ; ++gg) {
+              const float bt = betas[gg * BM + rr];
+              float4 val = *reinterpret_cast<const float4*>(stage + gg * BM * D + chunk_at(rr, c4));
+              val.x = fmaf(bt, mu.x, val.x);
+              val.y = fmaf(bt, mu.y, val.y);
+              val.z = fmaf(bt, mu.z, val.z);
+              val.w = fmaf(bt, mu.w, val.w);
+              float* out_blk = p.out + ((size_t)(b * p.Hq + h0 + gg) * p.S + row0) * D;
+              *reinterpret_cast<float4*>(out_blk + (size_t)rr * D + c) = val;
+            }
           }
         }
       }
@@ -596,7 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kIssueWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -727,6 +749,33 @@ bool tensor_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int D,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int D, int NQ>
+cudaError_t launch_tc(const topt_prefill_args& a, const TcParams& p, void* v16, cudaStream_t s) {
+  const int BHkv = a.batch * a.n_kv_heads;
+  CUtensorMap tq, tk, tv;
+  if (!tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
+      !tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, D, a.seq, BHkv, BN) ||
+      !tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v16, D, a.seq, BHkv, BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, NQ>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcLayout<D>::ALLOC);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  // programmatic launch: loads of Q and K overlap the preparation grids (a
+  // profiling event in between serialises them, which only moves time
+  // between them)
+  cfg.gridDim = dim3((unsigned)((size_t)p.nqb * a.n_q_heads / NQ * a.batch));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcLayout<D>::ALLOC;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, NQ>, tq, tk, tv, p);
+}
+
 template <int D>
 cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint32_t* vmax,
                   int32_t* vexp, cudaStream_t s) {
@@ -752,24 +801,10 @@ cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint
                               (const uint32_t*)vmax, static_cast<uint4*>(v16), vexp,
                               const_cast<float*>(p.bsum), p.nqb)) != cudaSuccess)
     return e;
-
-  CUtensorMap tq, tk, tv;
-  if (!tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
-      !tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, D, a.seq, BHkv, BN) ||
-      !tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v16, D, a.seq, BHkv, BN))
-    return cudaErrorInvalidValue;
-  const int smem = (int)TcLayout<D>::ALLOC;
-  if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem)) != cudaSuccess)
-    return e;
-  const unsigned grid = (unsigned)((size_t)p.nqb * a.n_q_heads * a.batch);
   if ((e = record_event(a.events[0], s)) != cudaSuccess) return e;
-  // programmatic launch: pass 1 overlaps the preparation grids (a profiling
-  // event in between serialises them, which only moves time between them)
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  if ((e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, tq, tk, tv, p)) != cudaSuccess) return e;
+  // two heads per CTA when they share a KV head
+  e = (a.n_q_heads / a.n_kv_heads) % 2 == 0 ? launch_tc<D, 2>(a, p, v16, s) : launch_tc<D, 1>(a, p, v16, s);
+  if (e != cudaSuccess) return e;
   return record_event(a.events[1], s);
 }
 
