@@ -64,8 +64,9 @@ DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
                   "source_sha256": "299e27949f1c896f2a58b0e5f2eb4b2abc6cf33ad978fd72fc9c33b28407c8b0",
                   "bytes_per_launch": 285350656 + 3795456}   # decode_kernel, one layer call (k = 128)
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "f0bd74c0af7559c1a0d66f264efb8004ccea2b5a967d0127d663594ba6fa74e6",
-                   "bytes_per_launch": 59525120 + 22531584}   # prefill_tc_kernel, post-softmax + VMC
+                   "source_sha256": "87ce9ab1f1e43f0fede6b1da3a71bf681c0f9e19312a24677a5c7da2ecb73f22",
+                   # prefill_tc_kernel per threshold mode (None: not captured for these sources)
+                   "bytes_per_launch": {0: 59839232 + 17040896, 1: 59756544 + 17250304}}
 
 
 def parse():
@@ -121,8 +122,12 @@ def source_sha(names):
     return h.hexdigest()
 
 
-def recorded_traffic(rec):
-    return rec["bytes_per_launch"] if source_sha(rec["sources"]) == rec["source_sha256"] else None
+def recorded_traffic(rec, key=None):
+    """DRAM bytes per launch from an ncu capture, while the kernel's sources
+    still hash to the captured ones (else None)."""
+    if source_sha(rec["sources"]) != rec["source_sha256"]:
+        return None
+    return rec["bytes_per_launch"] if key is None else rec["bytes_per_launch"].get(key)
 
 
 def hbm_peak():
@@ -580,7 +585,7 @@ def prefill_report(L, wl, dev, stream, steps, warmup):
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                          if kind == "measured" else "fallback 1.9 PFLOP/s",
-                         "traffic": recorded_traffic(PREFILL_TRAFFIC) if mode == 1 else None,
+                         "traffic": recorded_traffic(PREFILL_TRAFFIC, mode),
                          "avg_launch_ms": kern * 1e3,
                          "flops_per_launch": useful,
                          "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
@@ -1030,7 +1035,7 @@ def main_prefill(args, dev, rank, local, world):
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                      if kind == "measured" else "fallback 1.9 PFLOP/s",
-                     "traffic": recorded_traffic(PREFILL_TRAFFIC), "avg_launch_ms": kern * 1e3,
+                     "traffic": recorded_traffic(PREFILL_TRAFFIC, mode), "avg_launch_ms": kern * 1e3,
                      "flops_per_launch": useful,
                      "flops": "dense-equivalent: QK^T on every causal tile + P.V on executed tiles",
                      "issued_tflops": issued / kern / 1e12},
