@@ -23,6 +23,8 @@
 
 #include <cfloat>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -521,11 +523,38 @@ __global__ void __launch_bounds__(kFinThreads) calib_e_finalize_kernel(const Cal
   }
 }
 
+// Scores of rows [it0, it0 + nrows) into ws: the tensor-core kernel for bf16
+// rows it suits (calib_tc.cu), the CUDA-core kernel above otherwise.
+template <typename T, int D>
+cudaError_t calib_scores(const CalibParams& p, long it0, int nrows, float* ws, cudaStream_t s) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    CalibScoreArgs a;
+    a.q = p.q;
+    a.keys = p.keys;
+    a.row_len = p.row_len;
+    a.N = p.N;
+    a.Hq = p.Hq;
+    a.Hkv = p.Hkv;
+    a.R = p.R;
+    a.Nk = p.Nk;
+    a.D = D;
+    a.h0 = p.h0;
+    a.Hp = p.Hp;
+    a.scale = p.sm_scale;
+    a.it0 = it0;
+    a.nrows = nrows;
+    a.ws = ws;
+    a.status = p.status;
+    if (calib_scores_tc_ok(a)) return calib_scores_tc(a, s);
+  }
+  dim3 g((p.Nk + kScoreKeys - 1) / kScoreKeys, (nrows + kScoreRows - 1) / kScoreRows);
+  calib_scores_kernel<T, D><<<g, kScoreKeys, 0, s>>>(p, it0, nrows, ws);
+  return cudaGetLastError();
+}
+
 template <typename T, int D, bool kSdc = false>
 cudaError_t calib_pass(const CalibParams& p, long it0, int nrows, float* ws, cudaStream_t s) {
-  dim3 g1((p.Nk + kScoreKeys - 1) / kScoreKeys, (nrows + kScoreRows - 1) / kScoreRows);
-  calib_scores_kernel<T, D><<<g1, kScoreKeys, 0, s>>>(p, it0, nrows, ws);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = calib_scores<T, D>(p, it0, nrows, ws, s);
   if (e != cudaSuccess) return e;
   if (kSdc) calib_e_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
   else calib_select_kernel<<<nrows, kSelThreads, 0, s>>>(p, it0, ws);
@@ -975,9 +1004,7 @@ template <typename T, int D>
 cudaError_t mkc_scores(const CalibParams& cp, long total, float* ws, cudaStream_t s) {
   for (long it0 = 0; it0 < total; it0 += kMaxPassRows) {
     const int nrows = (int)((total - it0) < kMaxPassRows ? (total - it0) : kMaxPassRows);
-    dim3 g((cp.Nk + kScoreKeys - 1) / kScoreKeys, (nrows + kScoreRows - 1) / kScoreRows);
-    calib_scores_kernel<T, D><<<g, kScoreKeys, 0, s>>>(cp, it0, nrows, ws + it0 * (long)cp.Nk);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = calib_scores<T, D>(cp, it0, nrows, ws + it0 * (long)cp.Nk, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

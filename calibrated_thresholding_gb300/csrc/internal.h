@@ -44,6 +44,24 @@ size_t calibrate_multik_fixed_bytes(const topt_mkc_args& a);
 size_t calibrate_multik_head_bytes(const topt_mkc_args& a);
 int calibrate_multik_max_samples();
 cudaError_t calibrate_multik_launch(const topt_mkc_args& a, cudaStream_t s);
+// Calibration scores of bf16 rows on the tensor cores (calib_tc.cu): rows
+// [it0, it0 + nrows) of the flattened (seq, head h0 .. h0+Hp-1, row) index of
+// q [N][Hq][R][D] against keys [N][Hkv][Nk][D]; row it, key j < row_len[i]
+// goes to ws[(it - it0) * Nk + j] (times `scale`).  _ok: the shape and
+// pointers suit the kernel (16-byte aligned q and keys, d = 64 or 128).
+struct CalibScoreArgs {
+  const void* q;
+  const void* keys;
+  const int32_t* row_len;
+  int N, Hq, Hkv, R, Nk, D, h0, Hp;
+  float scale;
+  long it0;
+  int nrows;
+  float* ws;
+  int32_t* status;
+};
+bool calib_scores_tc_ok(const CalibScoreArgs& a);
+cudaError_t calib_scores_tc(const CalibScoreArgs& a, cudaStream_t s);
 cudaError_t select_kth_launch(const float* x, int32_t rows, int32_t stride,
                               const int32_t* row_len, int32_t k, float* out,
                               int32_t* status, cudaStream_t s);
