@@ -108,8 +108,18 @@ __device__ uint32_t cta_select_key(const Visit& visit, unsigned kk, SelectSmem& 
 
 // Exact k-th largest (1-based, 1 <= k <= L) of row[0..L-1].
 __device__ float cta_select_kth(const float* __restrict__ row, int L, int k, SelectSmem& sm) {
+  // four independent loads in flight per thread before any is used
   const auto visit = [&](auto&& f) {
-    for (int j = threadIdx.x; j < L; j += blockDim.x) f(f2key(row[j]));
+    const int nt = blockDim.x;
+    int j = threadIdx.x;
+    for (; j + 3 * nt < L; j += 4 * nt) {
+      const float x0 = row[j], x1 = row[j + nt], x2 = row[j + 2 * nt], x3 = row[j + 3 * nt];
+      f(f2key(x0));
+      f(f2key(x1));
+      f(f2key(x2));
+      f(f2key(x3));
+    }
+    for (; j < L; j += nt) f(f2key(row[j]));
   };
   return key2f(cta_select_key(visit, (unsigned)k, sm));
 }
@@ -751,17 +761,30 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
     const int i = p.order[base + idx];
     return p.ws + (((long)n * p.Hp + hl) * p.R + i) * p.Nk;
   };
+  // f(key) for the keys of row s that this lane owns (j = lane mod 32): eight
+  // independent loads in flight before any of them is used (the workspace is
+  // read from L2 again and again; one load at a time left the warps waiting)
+  const auto row_keys = [&](int s, auto&& f) {
+    const float* row = rowp(s);
+    int j = lane;
+    for (; j + 7 * kWarp < L; j += 8 * kWarp) {
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = row[j + u * kWarp];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) f(f2key(x[u]));
+    }
+    for (; j < L; j += kWarp) f(f2key(row[j]));
+  };
   // 1. maximum and minimum of every row; padding (key 0) sorts last
   for (int s = warp; s < cap; s += nw) {
     uint32_t hi_k = 0u, lo_k = 0u;
     if (s < Nr) {
-      const float* row = rowp(s);
       lo_k = 0xffffffffu;
-      for (int j = lane; j < L; j += kWarp) {
-        const uint32_t key = f2key(row[j]);
+      row_keys(s, [&](uint32_t key) {
         hi_k = max(hi_k, key);
         lo_k = min(lo_k, key);
-      }
+      });
       hi_k = __reduce_max_sync(0xffffffffu, hi_k);
       lo_k = __reduce_min_sync(0xffffffffu, lo_k);
     }
@@ -800,21 +823,16 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
   }
   __syncthreads();
   for (int s = warp; s < Nr; s += nw) {
-    const float* row = rowp(s);
-    for (int j = lane; j < L; j += kWarp) {
-      const uint32_t key = f2key(row[j]);
+    row_keys(s, [&](uint32_t key) {
       atomicAdd(&sh.px[count_ge(sh.mx, Nr, key)], 1u);
       atomicAdd(&sh.pn[count_ge(sh.mn, Nr, key)], 1u);
-    }
+    });
   }
   __syncthreads();
   cta_scan2(sh.px, sh.pn, Nr + 1);
   // 4. every target k
   const auto visit = [&](auto&& f) {
-    for (int s = warp; s < Nr; s += nw) {
-      const float* row = rowp(s);
-      for (int j = lane; j < L; j += kWarp) f(f2key(row[j]));
-    }
+    for (int s = warp; s < Nr; s += nw) row_keys(s, f);
   };
   for (int ki = 0; ki < p.n_k; ++ki) {
     const int k = p.ks[ki];
