@@ -592,6 +592,8 @@ cudaError_t calib_pass(const CalibParams& p, long it0, int nrows, float* ws, cud
 // ---------------------------------------------------------------------------
 constexpr int kMkcMaxSamples = 4096;  // calibration rows of one head and length per call
 constexpr int kMkcThreads = kSelThreads;
+constexpr int kMkcMaxK = 8;            // targets selected together (one warp each)
+static_assert(kMkcThreads / kWarp >= kMkcMaxK, "a warp per target");
 constexpr int kIdxThreads = 1024;
 
 struct MkcSmem {
@@ -738,6 +740,8 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
   MkcSmem& sh = *reinterpret_cast<MkcSmem*>(mkc_raw);
   __shared__ SelectSmem sm;
   __shared__ uint32_t s_best[kMkcThreads / kWarp];
+  __shared__ unsigned s_hist[kMkcMaxK][256];  // per target: histogram of the current digit
+  __shared__ uint32_t s_act[kMkcMaxK], s_kk[kMkcMaxK], s_pre[kMkcMaxK], s_u[kMkcMaxK];
   const int L = blockIdx.x + 1;
   const int hl = blockIdx.y;
   const int c = p.len_cnt[L];
@@ -830,46 +834,110 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
   }
   __syncthreads();
   cta_scan2(sh.px, sh.pn, Nr + 1);
-  // 4. every target k
+  // 4. every target k: the highest valid event e (its stretch [e, u)) gives
+  // T; theta(k) = min(u, the T-th largest pooled value).  The selections of
+  // up to kMkcMaxK targets run together: four digit sweeps over the pooled
+  // values, each filling one 256-bin histogram per target.
   const auto visit = [&](auto&& f) {
     for (int s = warp; s < Nr; s += nw) row_keys(s, f);
   };
-  for (int ki = 0; ki < p.n_k; ++ki) {
-    const int k = p.ks[ki];
-    if (k < 1 || k >= L) continue;  // uniform over the CTA
-    uint32_t best = 0u;
-    for (int t = tid; t < 2 * Nr; t += kMkcThreads) {
-      const bool from_max = t < Nr;
-      const uint32_t e = from_max ? sh.mx[t] : sh.mn[t - Nr];
-      const int bx = count_gt(sh.mx, Nr, e);
-      const int a = count_gt(sh.mn, Nr, e);
-      if (bx - a <= 0) continue;
-      const uint32_t P = from_max ? sh.px[bx] : sh.pn[a];
-      const long T = (long)k * bx + (long)(L - k) * a;
-      if ((long)P >= T) best = max(best, e);
-    }
-    best = __reduce_max_sync(0xffffffffu, best);
-    __syncthreads();
-    if (lane == 0) s_best[warp] = best;
-    __syncthreads();
-    best = 0u;
+  for (int k0 = 0; k0 < p.n_k; k0 += kMkcMaxK) {
+    const int nk = min(kMkcMaxK, p.n_k - k0);
+    for (int jj = 0; jj < nk; ++jj) {
+      const int ki = k0 + jj;
+      const int k = p.ks[ki];
+      if (tid == 0) s_act[jj] = 0u;
+      if (k < 1 || k >= L) continue;  // uniform over the CTA
+      uint32_t best = 0u;
+      for (int t = tid; t < 2 * Nr; t += kMkcThreads) {
+        const bool from_max = t < Nr;
+        const uint32_t e = from_max ? sh.mx[t] : sh.mn[t - Nr];
+        const int bx = count_gt(sh.mx, Nr, e);
+        const int a = count_gt(sh.mn, Nr, e);
+        if (bx - a <= 0) continue;
+        const uint32_t P = from_max ? sh.px[bx] : sh.pn[a];
+        const long T = (long)k * bx + (long)(L - k) * a;
+        if ((long)P >= T) best = max(best, e);
+      }
+      best = __reduce_max_sync(0xffffffffu, best);
+      __syncthreads();
+      if (lane == 0) s_best[warp] = best;
+      __syncthreads();
+      best = 0u;
 #pragma unroll
-    for (int w = 0; w < nw; ++w) best = max(best, s_best[w]);
-    const size_t cell = ((size_t)ki * p.Hq + p.h0 + hl) * p.Lmax + (L - 1);
-    if (best == 0u) {  // no stretch reaches k
-      if (tid == 0) p.gval[cell] = -CUDART_INF_F;
-      continue;
+      for (int w = 0; w < nw; ++w) best = max(best, s_best[w]);
+      if (tid == 0) {
+        if (best == 0u) {  // no stretch reaches k
+          p.gval[((size_t)ki * p.Hq + p.h0 + hl) * p.Lmax + (L - 1)] = -CUDART_INF_F;
+        } else {
+          const int bx = count_gt(sh.mx, Nr, best);
+          const int a = count_gt(sh.mn, Nr, best);
+          uint32_t u = sh.mx[bx - 1];  // bx >= 1: a valid stretch has a maximum above it
+          if (a > 0) u = min(u, sh.mn[a - 1]);
+          s_act[jj] = 1u;
+          s_kk[jj] = (unsigned)((long)k * bx + (long)(L - k) * a);
+          s_u[jj] = u;
+          s_pre[jj] = 0u;
+        }
+      }
     }
-    const int bx = count_gt(sh.mx, Nr, best);
-    const int a = count_gt(sh.mn, Nr, best);
-    uint32_t u = sh.mx[bx - 1];  // bx >= 1: a valid stretch has a maximum above it
-    if (a > 0) u = min(u, sh.mn[a - 1]);
-    const unsigned T = (unsigned)((long)k * bx + (long)(L - k) * a);
-    const uint32_t y = cta_select_key(visit, T, sm);
-    if (tid == 0) {
-      const float v = key2f(min(y, u));
-      p.gval[cell] = p.mode == TOPT_POST ? expf(v) : v;
+    __syncthreads();
+    uint32_t pmask = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < nk * 256; i += kMkcThreads) s_hist[i >> 8][i & 255] = 0u;
+      __syncthreads();
+      uint32_t pre[kMkcMaxK];
+      bool act[kMkcMaxK];
+#pragma unroll
+      for (int jj = 0; jj < kMkcMaxK; ++jj) {
+        act[jj] = jj < nk && s_act[jj] != 0u;
+        pre[jj] = act[jj] ? s_pre[jj] : 0u;
+      }
+      visit([&](uint32_t key) {
+#pragma unroll
+        for (int jj = 0; jj < kMkcMaxK; ++jj)
+          if (act[jj] && (key & pmask) == pre[jj]) atomicAdd(&s_hist[jj][(key >> shift) & 255u], 1u);
+      });
+      __syncthreads();
+      if (warp < nk && s_act[warp] != 0u) {
+        // warp jj: the digit of the kk-th largest; lane l owns bins
+        // 255-8l down to 248-8l (descending order of value)
+        const unsigned kk = s_kk[warp];
+        unsigned cnt[8];
+        unsigned tot = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cnt[e] = s_hist[warp][255 - 8 * lane - e];
+          tot += cnt[e];
+        }
+        unsigned incl = tot;
+#pragma unroll
+        for (int off = 1; off < kWarp; off <<= 1) {
+          const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const unsigned excl = incl - tot;
+        if (excl < kk && kk <= incl) {
+          unsigned c = excl;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (c + cnt[e] >= kk) {
+              s_pre[warp] |= (255u - 8u * lane - e) << shift;
+              s_kk[warp] = kk - c;
+              break;
+            }
+            c += cnt[e];
+          }
+        }
+      }
+      __syncthreads();
+      pmask |= 0xffu << shift;
     }
+    if (tid < nk && s_act[tid] != 0u) {
+      const float v = key2f(min(s_pre[tid], s_u[tid]));
+      p.gval[((size_t)(k0 + tid) * p.Hq + p.h0 + hl) * p.Lmax + (L - 1)] = p.mode == TOPT_POST ? expf(v) : v;
+    }
+    __syncthreads();
   }
 }
 
