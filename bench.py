@@ -1285,26 +1285,51 @@ def prefill_e2e(st, args, dev, world):
 
 
 def run_e2e(state, args, dev, world):
-    """Same step through topt.decode with host inputs copied in and outputs copied out."""
+    """The same step through the public API with host inputs and outputs: the
+    per-layer calls are prepared once (topt.decode_args / topt.vmean_args, as a
+    serving loop would), and every step copies all layers' q and appended K/V
+    rows in from pinned host memory (one copy) and all outputs back (one copy)."""
     wl = state.wl
     layers = state.layers
-    q_host = [state.q[l].cpu().pin_memory() for l in range(layers)]
-    kv_host = [torch.stack([state.K[l][:, :, wl.n - 1], state.V[l][:, :, wl.n - 1]]).cpu().pin_memory()
-               for l in range(layers)]
-    out_host = [torch.empty_like(state.out[l], device="cpu").pin_memory() for l in range(layers)]
-    kv_dev = torch.empty_like(kv_host[0], device=dev)
+    B, Hq, Hkv, d = wl.B, wl.Hq, wl.Hkv, wl.d
+    # host inputs of a step: per layer q [B][Hq][d] and the new K, V rows [2][B][Hkv][d]
+    per_in = B * Hq * d + 2 * B * Hkv * d
+    in_host = torch.empty(layers * per_in, dtype=torch.bfloat16).pin_memory()
+    for l in range(layers):
+        o = l * per_in
+        in_host[o:o + B * Hq * d].copy_(state.q[l].reshape(-1).cpu())
+        kv = torch.stack([state.K[l][:, :, wl.n - 1], state.V[l][:, :, wl.n - 1]]).reshape(-1)
+        in_host[o + B * Hq * d:o + per_in].copy_(kv.cpu())
+    in_dev = torch.empty_like(in_host, device=dev)
+    out_dev = torch.empty((layers, B, Hq, d), device=dev, dtype=torch.float32)
+    out_host = torch.empty_like(out_dev, device="cpu").pin_memory()
+    L = topt.lib()
+    sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    views, dargs, vargs = [], [], []
+    for l in range(layers):
+        o = l * per_in
+        q_in = in_dev[o:o + B * Hq * d].view(B, Hq, d)
+        kv_in = in_dev[o + B * Hq * d:o + per_in].view(2, B, Hkv, d)
+        views.append((state.K[l][:, :, wl.n - 1], state.V[l][:, :, wl.n - 1], kv_in))
+        a = topt.decode_args(q_in, state.K[l], state.V[l], state.seq_len, state.theta[l],
+                             mode=wl.mode, sdc=wl.sdc, vmc=wl.vmc, mu=state.mu[l], out=out_dev[l],
+                             kept=state.kept[l], vrows=state.vrows[l])
+        a.workspace = ctypes.c_void_p(state.ws.data_ptr())
+        a.workspace_bytes = state.ws.numel()
+        dargs.append(a)
+        vargs.append(topt.vmean_args(state.V[l], state.n_old, 1, state.mu[l]))
 
     def step():
+        in_dev.copy_(in_host, non_blocking=True)
         for l in range(layers):
-            state.q[l].copy_(q_host[l], non_blocking=True)
-            kv_dev.copy_(kv_host[l], non_blocking=True)
-            state.K[l][:, :, wl.n - 1].copy_(kv_dev[0])
-            state.V[l][:, :, wl.n - 1].copy_(kv_dev[1])
-            topt.vmean_update(state.V[l], state.n_old, 1, state.mu[l])
-            topt.decode(state.q[l], state.K[l], state.V[l], state.seq_len, state.theta[l],
-                        mode=wl.mode, sdc=wl.sdc, vmc=wl.vmc, mu=state.mu[l], out=state.out[l],
-                        kept=state.kept[l], vrows=state.vrows[l], workspace=state.ws)
-            out_host[l].copy_(state.out[l], non_blocking=True)
+            k_row, v_row, kv_in = views[l]
+            k_row.copy_(kv_in[0])
+            v_row.copy_(kv_in[1])
+            rc = L.topt_vmean_update(ctypes.byref(vargs[l]), sh)
+            rc = rc or L.topt_decode(ctypes.byref(dargs[l]), sh)
+            if rc:
+                raise topt.ToptError("e2e step", rc)
+        out_host.copy_(out_dev, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -1317,10 +1342,10 @@ def run_e2e(state, args, dev, world):
         step()
     torch.cuda.synchronize(dev)
     dt_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-    h2d = sum(q_host[l].numel() * 2 + kv_host[l].numel() * 2 for l in range(layers))
-    d2h = sum(out_host[l].numel() * 4 for l in range(layers))
     return {"value": wl.B * steps * world / dt_s, "unit": "tokens/s", "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": in_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 4,
+            "calls": "topt_vmean_update + topt_decode per layer, prepared once (topt.vmean_args, "
+                     "topt.decode_args)"}
 
 
 if __name__ == "__main__":

@@ -459,8 +459,9 @@ def select_kth(x, row_len, k, out=None, status=None, stream=None):
     return out
 
 
-def vmean_update(v_cache, n_old, n_new, mu, status=None, stream=None):
-    """mu <- running mean after appending rows n_old..n_old+n_new-1 (topt_vmean_update)."""
+def vmean_args(v_cache, n_old, n_new, mu, status=None) -> VmeanArgs:
+    """The topt_vmean_update arguments for these tensors (validated once; the
+    struct can be passed to ``lib().topt_vmean_update`` for every step)."""
     B, Hkv, Nmax, d = v_cache.shape
     a = VmeanArgs()
     a.batch, a.n_kv_heads, a.head_dim, a.cache_len = B, Hkv, d, Nmax
@@ -469,5 +470,11 @@ def vmean_update(v_cache, n_old, n_new, mu, status=None, stream=None):
     a.n_old = _ptr(_dev(n_old, "n_old", torch.int32))
     a.mu = _ptr(_dev(mu, "mu", torch.float32))
     a.status = _ptr(_dev(status, "status", torch.int32))
+    return a
+
+
+def vmean_update(v_cache, n_old, n_new, mu, status=None, stream=None):
+    """mu <- running mean after appending rows n_old..n_old+n_new-1 (topt_vmean_update)."""
+    a = vmean_args(v_cache, n_old, n_new, mu, status)
     _check("topt_vmean_update", lib().topt_vmean_update(ctypes.byref(a), _stream(stream)))
     return mu
