@@ -23,8 +23,6 @@
 // 4 d flops), not by the tensor core.
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -226,43 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) set_status(p.status, TOPT_ETIMEOUT);
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// [Z][Y][D] bf16 tensor, boxes of 64 elements x 128 rows x 1, 128-byte
-// swizzle, rows beyond Y read as zero.
-bool map_3d(CUtensorMap* m, const void* base, int D, long Y, long Z) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Y, (cuuint64_t)Z};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Y * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t run_d(const CalibScoreArgs& a, cudaStream_t s) {
   CUtensorMap tq, tk;
-  if (!map_3d(&tq, a.q, D, a.R, (long)a.N * a.Hq) || !map_3d(&tk, a.keys, D, a.Nk, (long)a.N * a.Hkv))
+  if (!tensor_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.R, (long)a.N * a.Hq, BM) ||
+      !tensor_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.keys, D, a.Nk, (long)a.N * a.Hkv, BN))
     return cudaErrorInvalidValue;
   ScoreTcParams p;
   p.N = a.N;

@@ -22,15 +22,21 @@ size_t prefill_workspace_bytes(const topt_prefill_args& a);
 void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys);
 // withhold_k: test hook of topt_prefill_test_timeout (tensor-core path only)
 cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s, int withhold_k = 0);
-// tensor-core path (bf16): 128-row x 128-key tiles; v16 is the fp16 copy of V
+// tensor-core path (bf16): 128-row blocks; v16 is the fp16 copy of V
 // (prefill_tc_v16_bytes), vmax/vexp one word per (batch, kv head), bsum the
 // column sums of 128-row blocks of V (prefill_tc_bsum_bytes; VMC only).
+// prefill_tc.cu runs the preparation and the pre-softmax kernel (64-key
+// tiles); post-softmax thresholds launch the kernel of prefill_tc_post.cu
+// (128-key tiles) on the prepared buffers.
 size_t prefill_tc_v16_bytes(const topt_prefill_args& a);
 size_t prefill_tc_bsum_bytes(const topt_prefill_args& a);
 int prefill_tc_rows();
-int prefill_tc_keys();
+int prefill_tc_keys(int mode);
 cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
                            float* bsum, cudaStream_t s, int withhold_k);
+int prefill_tc_post_keys();
+cudaError_t prefill_tc_post_launch(const topt_prefill_args& a, void* v16, const int32_t* vexp,
+                                   const float* bsum, cudaStream_t s, int withhold_k);
 
 // --------------------------------------------------------------- calibrate
 size_t calibrate_workspace_bytes(const topt_calib_args& a, size_t rows_per_pass);

@@ -264,7 +264,7 @@ size_t prefill_workspace_bytes(const topt_prefill_args& a) { return prefill_layo
 void prefill_tile_shape(const topt_prefill_args& a, int32_t* rows, int32_t* keys) {
   const bool tc = a.dtype == TOPT_BF16;
   *rows = tc ? prefill_tc_rows() : kRows;
-  *keys = tc ? prefill_tc_keys() : kKeys;
+  *keys = tc ? prefill_tc_keys(a.mode) : kKeys;
 }
 
 cudaError_t prefill_launch(const topt_prefill_args& a, cudaStream_t s, int withhold_k) {

@@ -30,14 +30,13 @@
 // measurement) but give each group two S buffers within the 512 TMEM columns,
 // so the next QK^T never waits for the rows.
 //
-// Pre-softmax (keep a >= theta) needs no row statistic before the decision, so
-// one pass does S, P and P.V together.  m2ref is a running reference per row
-// that is raised only when the row maximum passes it by more than 15 (log2
-// units, so P < 2^15 stays finite in fp16); then O, R and the row sum are rescaled by
-// 2^(old - new) -- in a causal row that happens a few times at most.
-// Post-softmax (keep s >= theta, i.e. a >= m + ln theta + ln Z) needs the row
-// maximum and sum first: pass 1 computes them, pass 2 recomputes S and applies
-// the bound with m2ref = the row maximum.
+// This kernel serves pre-softmax thresholds (keep a >= theta), which need no
+// row statistic before the decision, so one pass does S, P and P.V together.
+// m2ref is a running reference per row that is raised only when the row
+// maximum passes it by more than 15 (log2 units, so P < 2^15 stays finite in
+// fp16); then O, R and the row sum are rescaled by 2^(old - new).  Post-softmax
+// thresholds need the row maximum and sum first: prefill_tc_post.cu runs them
+// in two passes on the buffers prepared here.
 //
 // P is fp16: rounding it to bf16 costs up to ~2e-3 relative output error on
 // peaked rows, fp16 ~3e-4.  One MMA takes A and B in the same 16-bit type, so
@@ -87,10 +86,10 @@ struct TcLayout {
   static constexpr uint32_t BAR = RING + NS * TILE;
   // barriers: Q full [group]; slot full / empty (empty counts one arrival per
   // group); per group and S buffer ([2 g + b]): S full (its QK^T finished),
-  // S read (pass-1 rows loaded S), P full (the rows wrote P), P.V done (or
-  // skipped); per group: O final, MMA drain
+  // P full (the rows wrote P), P.V done (or skipped); per group: O final, MMA
+  // drain
   static constexpr int B_Q = 0, B_FULL = B_Q + kGroups, B_EMPTY = B_FULL + NS,
-                       B_SF = B_EMPTY + NS, B_SR = B_SF + 2 * kGroups, B_PF = B_SR + 2 * kGroups,
+                       B_SF = B_EMPTY + NS, B_PF = B_SF + 2 * kGroups,
                        B_PD = B_PF + 2 * kGroups, B_O = B_PD + 2 * kGroups, B_DRAIN = B_O + kGroups,
                        NBAR = B_DRAIN + kGroups;
   // misc words: abort flag, TMEM address, O written [group]; any-kept flags
@@ -182,13 +181,10 @@ __device__ __forceinline__ void chunk_weights(const uint32_t (&v)[BN], int c0, f
 // causal row the largest scores tend to be near the diagonal, so the running
 // reference of the pre-softmax pass is seldom raised after its first tile.
 // Load sequence of one CTA (the order the MMAs consume tiles), with
-// T_u = tile nt-1-u:
-//   post-softmax: K(T_0) .. K(T_{nt-1}) (pass 1), then K(T_0) V(T_0) K(T_1) V(T_1) ... (pass 2)
-//   pre-softmax:  K(T_0) V(T_0) K(T_1) V(T_1) ...
-// Load n goes to ring slot n % NS, its (n / NS)-th use.  QK^T number j of a
-// group (pass-1 tiles first, then pass-2 tiles) uses S buffer j % 2; the
-// per-buffer barriers complete once per use of their buffer, so a use's
-// parity is (its index among that buffer's uses) & 1.
+// T_u = tile nt-1-u: K(T_0) V(T_0) K(T_1) V(T_1) ...  Load n goes to ring
+// slot n % NS, its (n / NS)-th use.  Tile u of a group uses S buffer u % 2;
+// the per-buffer barriers complete once per use of their buffer, so a use's
+// parity is (u / 2) & 1.
 template <int D, int NQ>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -216,15 +212,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row0 = qb * BM;
   const int nt = (min(row0 + BM, p.S) - 1) / BN + 1;  // causal key tiles
   const int bh_kv = b * p.Hkv + kvh;
-  const bool pre = p.mode == TOPT_PRE;
-  const int P1 = pre ? 0 : nt;  // pass-1 tiles
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i) {
       uint32_t count = 1;
       if (i >= L::B_EMPTY && i < L::B_EMPTY + NS) count = NQ;
-      if ((i >= L::B_SR && i < L::B_SR + 2 * kGroups) || (i >= L::B_PF && i < L::B_PF + 2 * kGroups))
-        count = 4;
+      if (i >= L::B_PF && i < L::B_PF + 2 * kGroups) count = 4;
       mbar_init(bar(i), count);
     }
     *abort_flag = 0;
@@ -254,14 +247,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_3d(sb + L::Q + g * L::QT + pn * L::QP, &tmQ, bar(L::B_Q + g), 64 * pn, row0,
                       b * p.Hq + h0 + g);
       }
-      const int nseq = P1 + 2 * nt;
+      const int nseq = 2 * nt;
       bool v_ready = false;
       int issued = 0;
       for (int n = 0; n < nseq; ++n) {
         const int s = n % NS;
         if (n >= NS && !mbar_wait(bar(L::B_EMPTY + s), ((n / NS) - 1) & 1, abort_flag)) break;
-        const bool isv = n >= P1 && ((n - P1) & 1);
-        const int tile = nt - 1 - (n < P1 ? n : (n - P1) >> 1);
+        const bool isv = n & 1;
+        const int tile = nt - 1 - (n >> 1);
         if (isv && !v_ready) {
           pdl_wait();  // the fp16 copy of V is written by the previous grid
           v_ready = true;
@@ -294,20 +287,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t v_lo = sdesc_lo(sb + L::RING, L::KP);
       const uint32_t sO = tmem + 256u + 128u * g;
       bool ok = mbar_wait(bar(L::B_Q + g), 0, abort_flag);
-      const int nq = P1 + nt;  // QK^T of this group
-      // QK^T number j into S buffer j % 2, once the buffer's previous user
-      // (j - 2) is released: read by the pass-1 rows, or its P.V done
+      // QK^T of tile j into S buffer j % 2, once the buffer's previous tile
+      // (j - 2) is done: its P.V finished (or was skipped)
       auto qk = [&](int j) -> bool {
         const int bb = j & 1;
-        const int n = j < P1 ? j : P1 + 2 * (j - P1);  // load holding K of QK^T j
+        const int n = 2 * j;  // load holding K of tile j
         const int s = n % NS;
         if (!mbar_wait(bar(L::B_FULL + s), (n / NS) & 1, abort_flag)) return false;
-        const int prev = j - 2;
-        if (prev >= 0) {
-          const bool r1 = prev < P1;
-          const int idx = r1 ? prev >> 1 : (prev - P1) >> 1;
-          if (!mbar_wait(bar((r1 ? L::B_SR : L::B_PD) + 2 * g + bb), idx & 1, abort_flag)) return false;
-        }
+        if (j >= 2 && !mbar_wait(bar(L::B_PD + 2 * g + bb), ((j - 2) >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t ka = k_lo + s * (L::TILE >> 4);
 #pragma unroll
@@ -320,14 +307,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       uint32_t started = 0;
       unsigned long long executed = 0;
-      // pass 1: two QK^T ahead of the rows
-      for (int j = 0; ok && j < P1; ++j) ok = qk(j);
-      // pass 2 / single pass: the first two QK^T, then per tile P.V and the
-      // QK^T two tiles on
-      for (int j = P1; ok && j < min(nq, P1 + 2); ++j) ok = qk(j);
+      // the first two QK^T, then per tile P.V and the QK^T two tiles on
+      for (int j = 0; ok && j < min(nt, 2); ++j) ok = qk(j);
       for (int u = 0; ok && u < nt; ++u) {
-        const int bb = (P1 + u) & 1;
-        const int sv = (P1 + 2 * u + 1) % NS, nv = P1 + 2 * u + 1;  // load holding V of tile u
+        const int bb = u & 1;
+        const int nv = 2 * u + 1, sv = nv % NS;  // load holding V of tile u
         if (!(ok = mbar_wait(bar(L::B_PF + 2 * g + bb), (u >> 1) & 1, abort_flag))) break;
         const bool any = *reinterpret_cast<volatile uint32_t*>(anyf + 8 * g + 4 * bb) != 0u;
         // the slot is released only after its bytes arrived, also when unused
@@ -348,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(bar(L::B_PD + 2 * g + bb));
           mbar_arrive(bar(L::B_EMPTY + sv));
         }
-        if (P1 + u + 2 < nq) ok = qk(P1 + u + 2);
+        if (u + 2 < nt) ok = qk(u + 2);
       }
       tc_commit(bar(L::B_DRAIN + g));
       const bool drained = mbar_wait_drain(bar(L::B_DRAIN + g), 0);
@@ -390,49 +374,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
 
-    // pass 1 (post-softmax): m2 = max_j a_j c2, z = sum_j 2^(a_j c2 - m2)
-    float m2 = -CUDART_INF_F, z = 0.f;
-    for (int t = 0; ok && t < P1; ++t) {
-      const int bb = t & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + 2 * g + bb), (t >> 1) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      tmem_ld<BN>(sS + 64u * bb, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_SR + 2 * g + bb));  // S may be overwritten now
-      hide(nt - 1 - t);
-      const float mn = fmaxf(m2, row_max(v) * c2);
-      const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // a fully hidden row so far
-      // 2^(a c2 - mref) by packed fma, summed by packed add (four chains)
-      float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-      const float2 cc = make_float2(c2, c2), mm = make_float2(-mref, -mref);
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float2 y = ffma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), cc, mm);
-        sm[(c >> 1) & 3] = fadd2(sm[(c >> 1) & 3], make_float2(ex2(y.x), ex2(y.y)));
-      }
-      const float2 st2 = fadd2(fadd2(sm[0], sm[1]), fadd2(sm[2], sm[3]));
-      z = z * ex2(m2 - mref) + (st2.x + st2.y);
-      m2 = mn;
-    }
     // keep iff the raw score a * sqrt(d) >= braw; a hidden key (-inf) never
     // passes the finite bound
-    const float braw = fmaxf((pre ? th : score_bound(p.mode, th, m2 * kLn2, z)) / p.sm_scale, -FLT_MAX);
+    const float braw = fmaxf(th / p.sm_scale, -FLT_MAX);
 
-    // pass 2 (post) or the single pass (pre): P where kept.  R sums the fp32
-    // weights (P.V multiplies them rounded to fp16: relative difference below
-    // 2^-11 per weight).  Pre: m2ref follows the row maximum, Z sums every
-    // weight (used by exact SDC; one packed add per two keys, cheaper than a
-    // second code path), m2max is the row maximum.
-    float m2ref = pre ? -CUDART_INF_F : m2, m2max = -CUDART_INF_F;
+    // The single pass: P where kept.  R sums the fp32 weights (P.V multiplies
+    // them rounded to fp16: relative difference below 2^-11 per weight).
+    // m2ref follows the row maximum, Z sums every weight (used by exact SDC;
+    // one packed add per two keys, cheaper than a second code path), m2max is
+    // the row maximum.
+    float m2ref = -CUDART_INF_F, m2max = -CUDART_INF_F;
     float R = 0.f, KEPT = 0.f, Z = 0.f;
     uint32_t* mrow = (p.mask && row_ok) ? p.mask + ((size_t)bh_q * p.S + i) * p.mask_words : nullptr;
     for (int u = 0; ok && u < nt; ++u) {
-      const int j = P1 + u, bb = j & 1;
+      const int bb = u & 1;
       const uint32_t sSb = sS + 64u * bb;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + 2 * g + bb), (j >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + 2 * g + bb), (u >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       tmem_ld<BN>(sSb, v);
@@ -440,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       hide(tile);
       float factor = 1.f;
       bool rescale_o = false;
-      if (pre) {
+      {
         const float t2 = row_max(v) * c2;
         m2max = fmaxf(m2max, t2);
         if (t2 > m2ref + kLazy) {  // -inf + kLazy = -inf: the first visible tile
@@ -473,7 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       R += tR.x + tR.y;
       KEPT += tk;
       Z += tZ.x + tZ.y;
-      if (pre && __any_sync(0xffffffffu, rescale_o)) {
+      if (__any_sync(0xffffffffu, rescale_o)) {
         // O += P V of the previous tile has finished; the next P.V of this
         // group starts only after this warp signals P full
         ok = __all_sync(0xffffffffu,
@@ -518,14 +475,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool have_o = o_written[g] != 0;
       float sc = 0.f, beta = 0.f;
       if (row_ok) {
-        // pre-softmax sums are relative to 2^m2ref; the offline E~ is
-        // relative to the row maximum
-        const float mref = pre ? m2ref : m2;
+        // the sums are relative to 2^m2ref; the offline E~ is relative to the
+        // row maximum
         float e_off = 0.f;
-        if (pre && p.sdc == TOPT_SDC_OFFLINE)
+        if (p.sdc == TOPT_SDC_OFFLINE)
           e_off = p.e_tilde[(size_t)h * p.Lmax + (min(Lrow, p.Lmax) - 1)] * ex2(m2max - m2ref);
-        out_scale_beta(p.mode, p.sdc, p.gamma, th, mref * kLn2, pre ? Z : z, R, Lrow, cnt, e_off, sc,
-                       beta);
+        out_scale_beta(p.mode, p.sdc, p.gamma, th, m2ref * kLn2, Z, R, Lrow, cnt, e_off, sc, beta);
       }
       const float f = sc * __int_as_float((127 + p.vexp[bh_kv]) << 23);
       float* st = stage + g * BM * D;
@@ -714,48 +669,13 @@ __global__ void __launch_bounds__(256) v16_kernel(const uint4* __restrict__ v, i
   if (blockIdx.x == 0 && threadIdx.x == 0) vexp[bh] = e;
 }
 
-// ------------------------------------------------------------ tensor maps --
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// [BH][S][D] 16-bit tensor; boxes of 64 elements x `rows` rows x 1, 128-byte
-// swizzle; rows beyond S read as zero.
-bool tensor_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int D, int S, int BH,
-                int rows) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-  const cuuint32_t estride[3] = {1, 1, 1};
-  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estride,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int NQ>
 cudaError_t launch_tc(const topt_prefill_args& a, const TcParams& p, void* v16, cudaStream_t s) {
   const int BHkv = a.batch * a.n_kv_heads;
   CUtensorMap tq, tk, tv;
-  if (!tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
-      !tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, D, a.seq, BHkv, BN) ||
-      !tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v16, D, a.seq, BHkv, BN))
+  if (!tensor_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, a.seq, a.batch * a.n_q_heads, BM) ||
+      !tensor_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.k, D, a.seq, BHkv, BN) ||
+      !tensor_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v16, D, a.seq, BHkv, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, NQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcLayout<D>::ALLOC);
@@ -802,8 +722,10 @@ cudaError_t run_d(const topt_prefill_args& a, const TcParams& p, void* v16, uint
                               const_cast<float*>(p.bsum), p.nqb)) != cudaSuccess)
     return e;
   if ((e = record_event(a.events[0], s)) != cudaSuccess) return e;
-  // two heads per CTA when they share a KV head
-  e = (a.n_q_heads / a.n_kv_heads) % 2 == 0 ? launch_tc<D, 2>(a, p, v16, s) : launch_tc<D, 1>(a, p, v16, s);
+  if (a.mode == TOPT_POST)  // two passes: the kernel of prefill_tc_post.cu
+    e = prefill_tc_post_launch(a, v16, vexp, p.bsum, s, p.withhold_k);
+  else  // one pass, two heads per CTA when they share a KV head
+    e = (a.n_q_heads / a.n_kv_heads) % 2 == 0 ? launch_tc<D, 2>(a, p, v16, s) : launch_tc<D, 1>(a, p, v16, s);
   if (e != cudaSuccess) return e;
   return record_event(a.events[1], s);
 }
@@ -819,7 +741,7 @@ size_t prefill_tc_v16_bytes(const topt_prefill_args& a) {
 }
 
 int prefill_tc_rows() { return BM; }
-int prefill_tc_keys() { return BN; }
+int prefill_tc_keys(int mode) { return mode == TOPT_POST ? prefill_tc_post_keys() : BN; }
 
 cudaError_t prefill_tc_run(const topt_prefill_args& a, void* v16, uint32_t* vmax, int32_t* vexp,
                            float* bsum, cudaStream_t s, int withhold_k) {
