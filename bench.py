@@ -63,10 +63,11 @@ CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
                   "source_sha256": "299e27949f1c896f2a58b0e5f2eb4b2abc6cf33ad978fd72fc9c33b28407c8b0",
                   "bytes_per_launch": 285350656 + 3795456}   # decode_kernel, one layer call (k = 128)
-PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "87ce9ab1f1e43f0fede6b1da3a71bf681c0f9e19312a24677a5c7da2ecb73f22",
-                   # prefill_tc_kernel per threshold mode (None: not captured for these sources)
-                   "bytes_per_launch": {0: 59839232 + 17040896, 1: 59756544 + 17250304}}
+PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "prefill_tc_post.cu", "tc.cuh", "common.cuh"],
+                   "source_sha256": "df35f8e29aa5e1a35fa23f12ac181bcb9e0b27b53758051f7dccff2112c6baf7",
+                   # the attention kernel of each threshold mode (pre: prefill_tc_kernel,
+                   # post: prefill_post_kernel)
+                   "bytes_per_launch": {0: 59916032 + 17154816, 1: 59517440 + 22559232}}
 
 
 def parse():
@@ -475,6 +476,7 @@ def kept_ratio_by_bucket(state):
 # the prefill workload
 # ---------------------------------------------------------------------------
 PREFILL_MODES = (("post-softmax+VMC", 1, 0), ("pre-softmax+exact SDC+VMC", 0, 1))
+PREFILL_KERNEL = {0: "prefill_tc_kernel", 1: "prefill_post_kernel"}  # the attention kernel per mode
 
 
 def prefill_mode(args):
@@ -581,7 +583,7 @@ def prefill_report(L, wl, dev, stream, steps, warmup):
             "mode": name, "tflops_call": useful / call / 1e12, "ms_per_call": call * 1e3,
             "kept_elem_tflops_call": kept_elem_flops(wl, kept_total) / call / 1e12,
             "tokens_per_s": wl.B * wl.S / call,
-            "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+            "roofline": {"bound": "tensor", "kernel": PREFILL_KERNEL[mode], "achieved": achieved,
                          "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                          if kind == "measured" else "fallback 1.9 PFLOP/s",
@@ -1031,7 +1033,7 @@ def main_prefill(args, dev, rank, local, world):
         "warmup": args.warmup, "ms_per_step": call * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": prefill_config(wl, name, world),
-        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": PREFILL_KERNEL[mode], "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
                      if kind == "measured" else "fallback 1.9 PFLOP/s",
