@@ -40,7 +40,10 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 32 * 6;
 constexpr uint32_t kTmemCols = 256;  // score buffers at columns 0 and 128
-constexpr int SS = 33;              // staging row stride in floats (conflict-free)
+// Staging tile of a writer warp: 32 rows x 32 floats, the 16-byte chunk c of
+// row r at chunk c ^ (r & 7), so both the row-wise writes and the 4-row x
+// 8-chunk reads of 16 bytes are free of bank conflicts.
+constexpr int SS = 32;
 
 template <int D>
 struct CalLayout {
@@ -187,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ writers
     float* stage = reinterpret_cast<float*>(gb + L::STAGE) + warp * 32 * SS;  // this warp's [32][SS]
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const bool vec = (p.Nk & 3) == 0;  // 16-byte aligned rows of the workspace
+    const int sub = lane >> 3, c4 = lane & 7;  // reads: row 4 i + sub, chunk c4
     for (int kt = 0; kt < nkt; ++kt) {
       const int bb = kt & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::B_SF + bb), (kt >> 1) & 1, abort_flag))) break;
@@ -196,15 +201,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lanes + 128u * bb + (uint32_t)c, v);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) stage[lane * SS + k] = __uint_as_float(v[k]) * p.scale;
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(stage + lane * SS + 4 * (q ^ (lane & 7))) =
+              make_float4(__uint_as_float(v[4 * q]) * p.scale, __uint_as_float(v[4 * q + 1]) * p.scale,
+                          __uint_as_float(v[4 * q + 2]) * p.scale, __uint_as_float(v[4 * q + 3]) * p.scale);
         __syncwarp();
-        // row rr of the warp: 32 consecutive keys, one 128-byte segment
-        const int col = kt * BN + c + lane;
-#pragma unroll 4
-        for (int rr = 0; rr < 32; ++rr) {
+        // four rows of the warp per store instruction: 8 lanes x 16 bytes,
+        // one 128-byte segment of each row
+        const int col = kt * BN + c + 4 * c4;
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + sub;
           const int len = __shfl_sync(0xffffffffu, Lr, rr);
-          if (col < len)
-            p.ws[(it_row0 + warp * 32 + rr - p.it0) * (long)p.Nk + col] = stage[rr * SS + lane];
+          if (col < len) {
+            const float4 x = *reinterpret_cast<const float4*>(stage + rr * SS + 4 * (c4 ^ (rr & 7)));
+            float* dst = p.ws + (it_row0 + warp * 32 + rr - p.it0) * (long)p.Nk + col;
+            if (vec && col + 3 < len) {
+              *reinterpret_cast<float4*>(dst) = x;
+            } else {
+              dst[0] = x.x;
+              if (col + 1 < len) dst[1] = x.y;
+              if (col + 2 < len) dst[2] = x.z;
+              if (col + 3 < len) dst[3] = x.w;
+            }
+          }
         }
         __syncwarp();
       }

@@ -211,6 +211,25 @@ def test_vmean_running_mean(dtype):
     assert int(status.item()) == 1
 
 
+def test_vmean_prepared_args_reused():
+    """topt.vmean_args prepares the call once; calling the C ABI with the same
+    struct for consecutive tokens gives the running mean (the serving-loop use)."""
+    import ctypes
+    B, Hkv, d, Nmax = 2, 2, 64, 300
+    gen = synth.generator(62, "cuda")
+    V = synth.values(gen, B, Hkv, Nmax, d, device="cuda")
+    mu = torch.zeros((B, Hkv, d), device="cuda")
+    n_old = torch.zeros(B, device="cuda", dtype=torch.int32)
+    topt.vmean_update(V, n_old, 200, mu)
+    a = topt.vmean_args(V, n_old, 1, mu)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for t in range(200, 300):
+        n_old.fill_(t)
+        assert topt.lib().topt_vmean_update(ctypes.byref(a), stream) == 0
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(mu.cpu().double().numpy(), np.mean(synth.as_f64(V), axis=2), rtol=0, atol=1e-5)
+
+
 # ---------------------------------------------------------------------------
 # prefill
 # ---------------------------------------------------------------------------
