@@ -111,42 +111,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// As tma_load_3d, delivered to the same shared-memory offset of every CTA of
-// the cluster named in `mask` (bit r = cluster rank r), each of which counts
-// the bytes on its own barrier at offset `bar`.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int x, int y, int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
-// ------------------------------------------------------------- clusters --
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster; orders the memory operations
-// before it (release) with those after it (acquire) across the cluster.
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// The address of the same shared-memory offset in the CTA of cluster rank `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// One arrival on a barrier of any CTA of the cluster (address from mapa_shared).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // -------------------------------------------------------------- tcgen05 --
 // Allocation is done by one whole warp; the TMEM address lands in *dst_smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -215,16 +179,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
-}
-
-// As tc_commit, arriving once on the barrier at offset `bar` of every CTA of
-// the cluster named in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
 }
 
 // Instruction descriptor of kind::f16 with fp32 accumulation, M = 128.
@@ -389,18 +343,8 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
       : "memory");
 }
 
-// Stores 16 consecutive 32-bit columns of this thread's lane without waiting;
+// Stores 64 consecutive 32-bit columns of this thread's lane without waiting;
 // tmem_wait_st() waits for every store this thread issued.
-__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-// Stores 64 consecutive 32-bit columns of this thread's lane without waiting.
 __device__ __forceinline__ void tmem_st64_async(uint32_t taddr, const uint32_t (&r)[64]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"

@@ -301,17 +301,19 @@ def test_prefill_dense_and_empty(d, dtype, S):
             torch.testing.assert_close(res["out"], want, rtol=2e-5, atol=2e-5)
 
 
-def test_prefill_wait_runs_out_and_context_survives():
-    """A wait of the tensor-core kernel that never completes (the test hook never
+@pytest.mark.parametrize("mode", [ref.PRE, ref.POST])
+def test_prefill_wait_runs_out_and_context_survives(mode):
+    """A wait of a tensor-core kernel (pre-softmax: the single-pass kernel;
+    post-softmax: the two-pass one) that never completes (the test hook never
     loads the first K tile of a block) gives up after its time limit: the call
     reports TOPT_ETIMEOUT, nothing faults, and the next call is correct."""
     import ctypes
     B, Hq, Hkv, d, S = 1, 2, 1, 128, 200
     Q, K, V = prefill_case(91, B, Hq, Hkv, d, S)
-    dense = torch.full((Hq, S), float("-inf"), device="cuda")
+    dense = torch.full((Hq, S), float("-inf") if mode == ref.PRE else 0.0, device="cuda")
     status = torch.zeros(1, device="cuda", dtype=torch.int32)
     out = torch.empty((B, Hq, S, d), device="cuda")
-    a = topt.prefill_args(Q, K, V, dense, mode=ref.PRE, out=out, status=status)
+    a = topt.prefill_args(Q, K, V, dense, mode=mode, out=out, status=status)
     ws = torch.empty(max(1, topt.prefill_workspace_bytes(a)), device="cuda", dtype=torch.uint8)
     a.workspace = ctypes.c_void_p(ws.data_ptr())
     a.workspace_bytes = ws.numel()
@@ -321,7 +323,7 @@ def test_prefill_wait_runs_out_and_context_survives():
     assert int(status.item()) == 5                               # TOPT_ETIMEOUT
     status.zero_()
     mask = torch.full((B, Hq, S, mask_words(S)), -1, device="cuda", dtype=torch.int32)
-    res = topt.prefill(Q, K, V, dense, mode=ref.PRE, mask=mask, status=status)
+    res = topt.prefill(Q, K, V, dense, mode=mode, mask=mask, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    check_prefill(Q, K, V, dense, ref.PRE, ref.SDC_NONE, False, res)
+    check_prefill(Q, K, V, dense, mode, ref.SDC_NONE, False, res)
