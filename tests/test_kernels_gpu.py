@@ -245,6 +245,7 @@ PREFILL_MODES = [
     (64, torch.bfloat16, 2, 4, 2, 100),
     (128, torch.bfloat16, 1, 4, 1, 300),    # three 128-row blocks, ragged last block and key tile
     (64, torch.bfloat16, 1, 2, 2, 257),     # one KV head per query head, ragged
+    (128, torch.bfloat16, 1, 3, 1, 200),    # odd GQA group: one head per CTA in the single-pass kernel
 ])
 def test_prefill_matches_oracle(d, dtype, B, Hq, Hkv, S):
     k = 8
