@@ -593,6 +593,7 @@ cudaError_t calib_pass(const CalibParams& p, long it0, int nrows, float* ws, cud
 constexpr int kMkcMaxSamples = 4096;  // calibration rows of one head and length per call
 constexpr int kMkcThreads = kSelThreads;
 constexpr int kMkcMaxK = 8;            // targets selected together (one warp each)
+constexpr int kMkcSmall = 8;           // rows of a group up to which events are counted in registers
 static_assert(kMkcThreads / kWarp >= kMkcMaxK, "a warp per target");
 constexpr int kIdxThreads = 1024;
 
@@ -820,20 +821,54 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
       __syncthreads();
     }
   }
-  // 3. P at every event: x > e <=> #{events >= x} <= #{events > e}
+  // 3. P at every event.  Up to kMkcSmall rows: every thread counts
+  // #{x > e} for each event e in registers, summed over the CTA into
+  // px[t] (t-th maximum) and pn[t] (t-th minimum).  More rows: histograms of
+  // #{events >= x} (x > e <=> #{events >= x} <= #{events > e}), scanned, read
+  // at px[#{maxima > e}] and pn[#{minima > e}].
+  const bool small = Nr <= kMkcSmall;
   for (int i = tid; i <= Nr; i += kMkcThreads) {
     sh.px[i] = 0u;
     sh.pn[i] = 0u;
   }
   __syncthreads();
-  for (int s = warp; s < Nr; s += nw) {
-    row_keys(s, [&](uint32_t key) {
-      atomicAdd(&sh.px[count_ge(sh.mx, Nr, key)], 1u);
-      atomicAdd(&sh.pn[count_ge(sh.mn, Nr, key)], 1u);
-    });
+  if (small) {
+    uint32_t ex[kMkcSmall], en[kMkcSmall], cx[kMkcSmall], cn[kMkcSmall];
+#pragma unroll
+    for (int t = 0; t < kMkcSmall; ++t) {
+      ex[t] = t < Nr ? sh.mx[t] : 0xffffffffu;  // padding: no key is above it
+      en[t] = t < Nr ? sh.mn[t] : 0xffffffffu;
+      cx[t] = cn[t] = 0u;
+    }
+    for (int s = warp; s < Nr; s += nw) {
+      row_keys(s, [&](uint32_t key) {
+#pragma unroll
+        for (int t = 0; t < kMkcSmall; ++t) {
+          cx[t] += key > ex[t];
+          cn[t] += key > en[t];
+        }
+      });
+    }
+#pragma unroll
+    for (int t = 0; t < kMkcSmall; ++t) {
+      const uint32_t a = __reduce_add_sync(0xffffffffu, cx[t]);
+      const uint32_t b2 = __reduce_add_sync(0xffffffffu, cn[t]);
+      if (lane == 0 && t < Nr) {
+        atomicAdd(&sh.px[t], a);
+        atomicAdd(&sh.pn[t], b2);
+      }
+    }
+    __syncthreads();
+  } else {
+    for (int s = warp; s < Nr; s += nw) {
+      row_keys(s, [&](uint32_t key) {
+        atomicAdd(&sh.px[count_ge(sh.mx, Nr, key)], 1u);
+        atomicAdd(&sh.pn[count_ge(sh.mn, Nr, key)], 1u);
+      });
+    }
+    __syncthreads();
+    cta_scan2(sh.px, sh.pn, Nr + 1);
   }
-  __syncthreads();
-  cta_scan2(sh.px, sh.pn, Nr + 1);
   // 4. every target k: the highest valid event e (its stretch [e, u)) gives
   // T; theta(k) = min(u, the T-th largest pooled value).  The selections of
   // up to kMkcMaxK targets run together: four digit sweeps over the pooled
@@ -855,7 +890,7 @@ __global__ void __launch_bounds__(kMkcThreads) mkc_group_kernel(const MkcParams 
         const int bx = count_gt(sh.mx, Nr, e);
         const int a = count_gt(sh.mn, Nr, e);
         if (bx - a <= 0) continue;
-        const uint32_t P = from_max ? sh.px[bx] : sh.pn[a];
+        const uint32_t P = small ? (from_max ? sh.px[t] : sh.pn[t - Nr]) : (from_max ? sh.px[bx] : sh.pn[a]);
         const long T = (long)k * bx + (long)(L - k) * a;
         if ((long)P >= T) best = max(best, e);
       }
