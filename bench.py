@@ -61,8 +61,8 @@ NOMINAL_HBM_GBS = 8000.0
 # on; reported as null once the sources differ.
 CSRC = os.path.join(ROOT, "calibrated_thresholding_gb300", "csrc")
 DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
-                  "source_sha256": "299e27949f1c896f2a58b0e5f2eb4b2abc6cf33ad978fd72fc9c33b28407c8b0",
-                  "bytes_per_launch": 285350656 + 3795456}   # decode_kernel, one layer call (k = 128)
+                  "source_sha256": "7b605ed92726ff074a8ac0386e4db346c6fe918ae09d8bb60643e8ea35294192",
+                  "bytes_per_launch": 285353216 + 3473152}   # decode_kernel, one layer call (k = 128)
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "prefill_tc_post.cu", "tc.cuh", "common.cuh"],
                    "source_sha256": "df35f8e29aa5e1a35fa23f12ac181bcb9e0b27b53758051f7dccff2112c6baf7",
                    # the attention kernel of each threshold mode (pre: prefill_tc_kernel,

@@ -128,6 +128,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, unsign
                "r"(src_bytes), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void cp_async16_full(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -353,13 +357,19 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const DecodeParams 
     const int t1 = min(2 * wu1, (L + kTile - 1) / kTile);  // this warp's 16-key tiles
     const uint32_t ring_s = smem_u32(&sm.u.ring[warp][0][0]);
     auto issue = [&](int tile, int slot) {
-      const char* src = reinterpret_cast<const char*>(kbase + (size_t)tile * kTile * D);
+      const char* src = reinterpret_cast<const char*>(kbase + (size_t)tile * kTile * D) + lane * 16;
+      const uint32_t dst = ring_s + slot * kTileBytes + lane * 16;
       const int rows = min(kTile, L - tile * kTile);
+      if (rows == kTile) {  // a whole tile: no per-chunk size
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int off = (i * kWarp + lane) * 16;
-        const bool ok = off / (D * 2) < rows;
-        cp_async16(ring_s + slot * kTileBytes + off, src + (ok ? off : 0), ok ? 16u : 0u, pol_k);
+        for (int i = 0; i < kChunks; ++i) cp_async16_full(dst + i * kWarp * 16, src + i * kWarp * 16, pol_k);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int off = (i * kWarp + lane) * 16;
+          const bool ok = off / (D * 2) < rows;
+          cp_async16(dst + i * kWarp * 16, src - lane * 16 + (ok ? off : 0), ok ? 16u : 0u, pol_k);
+        }
       }
       cp_async_commit();
     };
