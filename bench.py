@@ -233,18 +233,17 @@ class DecodeState:
         self.ws = topt.decode_workspace(a0, dev)
         self.dargs = []
         self.vargs = []
+        self.new_kv = []
         for l in range(layers):
             a = self.args(l)
             a.workspace = ctypes.c_void_p(self.ws.data_ptr())
             a.workspace_bytes = self.ws.numel()
             self.dargs.append(a)
-            v = topt.VmeanArgs()
-            v.batch, v.n_kv_heads, v.head_dim, v.cache_len = B, Hkv, d, n
-            v.dtype, v.n_new = topt.BF16, 1
-            v.v_cache = ctypes.c_void_p(self.V[l].data_ptr())
-            v.n_old = ctypes.c_void_p(self.n_old.data_ptr())
-            v.mu = ctypes.c_void_p(self.mu[l].data_ptr())
-            self.vargs.append(v)
+            # the step's new K, V rows (the current token, row n-1), appended
+            # by the vmean launch itself
+            self.new_kv.append(torch.stack([self.K[l][:, :, n - 1:], self.V[l][:, :, n - 1:]]).contiguous())
+            self.vargs.append(topt.vmean_args(self.V[l], self.n_old, 1, self.mu[l], k_cache=self.K[l],
+                                              k_new=self.new_kv[l][0], v_new=self.new_kv[l][1]))
         torch.cuda.synchronize()
 
     def args(self, l):
@@ -1289,50 +1288,78 @@ def prefill_e2e(st, args, dev, world):
 def run_e2e(state, args, dev, world):
     """The same step through the public API with host inputs and outputs: the
     per-layer calls are prepared once (topt.decode_args / topt.vmean_args, as a
-    serving loop would), and every step copies all layers' q and appended K/V
-    rows in from pinned host memory (one copy) and all outputs back (one copy)."""
+    serving loop would).  Every step copies all layers' q and new K/V rows in
+    from pinned host memory (one copy, into the other of two device buffers
+    while the previous step computes) and every layer's outputs back (one copy
+    per group of eight layers, as soon as the group is done); each layer's
+    topt_vmean_update appends its new K/V rows and updates mu, then
+    topt_decode runs."""
     wl = state.wl
     layers = state.layers
     B, Hq, Hkv, d = wl.B, wl.Hq, wl.Hkv, wl.d
-    # host inputs of a step: per layer q [B][Hq][d] and the new K, V rows [2][B][Hkv][d]
+    group = 8 if layers % 8 == 0 else 1
+    # host inputs of a step: per layer q [B][Hq][d] and the new K, V rows [2][B][Hkv][1][d]
     per_in = B * Hq * d + 2 * B * Hkv * d
     in_host = torch.empty(layers * per_in, dtype=torch.bfloat16).pin_memory()
     for l in range(layers):
         o = l * per_in
         in_host[o:o + B * Hq * d].copy_(state.q[l].reshape(-1).cpu())
-        kv = torch.stack([state.K[l][:, :, wl.n - 1], state.V[l][:, :, wl.n - 1]]).reshape(-1)
-        in_host[o + B * Hq * d:o + per_in].copy_(kv.cpu())
-    in_dev = torch.empty_like(in_host, device=dev)
+        in_host[o + B * Hq * d:o + per_in].copy_(state.new_kv[l].reshape(-1).cpu())
+    in_dev = [torch.empty_like(in_host, device=dev) for _ in range(2)]
     out_dev = torch.empty((layers, B, Hq, d), device=dev, dtype=torch.float32)
     out_host = torch.empty_like(out_dev, device="cpu").pin_memory()
     L = topt.lib()
-    sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-    views, dargs, vargs = [], [], []
-    for l in range(layers):
-        o = l * per_in
-        q_in = in_dev[o:o + B * Hq * d].view(B, Hq, d)
-        kv_in = in_dev[o + B * Hq * d:o + per_in].view(2, B, Hkv, d)
-        views.append((state.K[l][:, :, wl.n - 1], state.V[l][:, :, wl.n - 1], kv_in))
-        a = topt.decode_args(q_in, state.K[l], state.V[l], state.seq_len, state.theta[l],
-                             mode=wl.mode, sdc=wl.sdc, vmc=wl.vmc, mu=state.mu[l], out=out_dev[l],
-                             kept=state.kept[l], vrows=state.vrows[l])
-        a.workspace = ctypes.c_void_p(state.ws.data_ptr())
-        a.workspace_bytes = state.ws.numel()
-        dargs.append(a)
-        vargs.append(topt.vmean_args(state.V[l], state.n_old, 1, state.mu[l]))
+    comp = torch.cuda.current_stream(dev)
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    sh = ctypes.c_void_p(comp.cuda_stream)
+    dargs, vargs = [[], []], [[], []]
+    for buf in range(2):
+        for l in range(layers):
+            o = l * per_in
+            q_in = in_dev[buf][o:o + B * Hq * d].view(B, Hq, d)
+            kv_in = in_dev[buf][o + B * Hq * d:o + per_in].view(2, B, Hkv, 1, d)
+            a = topt.decode_args(q_in, state.K[l], state.V[l], state.seq_len, state.theta[l],
+                                 mode=wl.mode, sdc=wl.sdc, vmc=wl.vmc, mu=state.mu[l], out=out_dev[l],
+                                 kept=state.kept[l], vrows=state.vrows[l])
+            a.workspace = ctypes.c_void_p(state.ws.data_ptr())
+            a.workspace_bytes = state.ws.numel()
+            dargs[buf].append(a)
+            vargs[buf].append(topt.vmean_args(state.V[l], state.n_old, 1, state.mu[l], k_cache=state.K[l],
+                                              k_new=kv_in[0], v_new=kv_in[1]))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_used = [torch.cuda.Event() for _ in range(2)]
+    ev_grp = [torch.cuda.Event() for _ in range(layers // group)]
+    ev_out = torch.cuda.Event()
+    count = [0]
+
+    def h2d(buf):
+        with torch.cuda.stream(cin):
+            cin.wait_event(ev_used[buf])           # the step that read this buffer is done with it
+            in_dev[buf].copy_(in_host, non_blocking=True)
+            ev_in[buf].record(cin)
 
     def step():
-        in_dev.copy_(in_host, non_blocking=True)
+        buf = count[0] & 1
+        h2d(buf ^ 1)                               # the next step's inputs travel during this step
+        comp.wait_event(ev_in[buf])
+        comp.wait_event(ev_out)                    # the previous step's outputs have been read back
         for l in range(layers):
-            k_row, v_row, kv_in = views[l]
-            k_row.copy_(kv_in[0])
-            v_row.copy_(kv_in[1])
-            rc = L.topt_vmean_update(ctypes.byref(vargs[l]), sh)
-            rc = rc or L.topt_decode(ctypes.byref(dargs[l]), sh)
+            rc = L.topt_vmean_update(ctypes.byref(vargs[buf][l]), sh)
+            rc = rc or L.topt_decode(ctypes.byref(dargs[buf][l]), sh)
             if rc:
                 raise topt.ToptError("e2e step", rc)
-        out_host.copy_(out_dev, non_blocking=True)
+            if (l + 1) % group == 0:
+                g = l // group
+                ev_grp[g].record(comp)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_grp[g])
+                    out_host[g * group:(g + 1) * group].copy_(out_dev[g * group:(g + 1) * group],
+                                                              non_blocking=True)
+        ev_used[buf].record(comp)
+        ev_out.record(cout)
+        count[0] += 1
 
+    h2d(0)
     for _ in range(max(3, args.warmup)):
         step()
     steps = max(10, args.steps // 4)
@@ -1346,8 +1373,9 @@ def run_e2e(state, args, dev, world):
     dt_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     return {"value": wl.B * steps * world / dt_s, "unit": "tokens/s", "steps": steps,
             "h2d_bytes_per_step": in_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 4,
-            "calls": "topt_vmean_update + topt_decode per layer, prepared once (topt.vmean_args, "
-                     "topt.decode_args)"}
+            "calls": "topt_vmean_update (appends the new K/V rows, updates mu) + topt_decode per layer, "
+                     "prepared once (topt.vmean_args, topt.decode_args); next step's inputs copied in "
+                     "while this step computes, outputs copied back per group of 8 layers"}
 
 
 if __name__ == "__main__":

@@ -286,6 +286,8 @@ topt_status topt_vmean_update(const topt_vmean_args* a, topt_stream stream) {
   if (a->n_new > a->cache_len) return TOPT_ESHAPE;
   if (!a->v_cache || !a->n_old || !a->mu) return TOPT_EINVAL;
   if (!aligned16(a->v_cache)) return TOPT_EINVAL;
+  if (a->k_new && (!a->k_cache || !aligned16(a->k_cache) || !aligned16(a->k_new))) return TOPT_EINVAL;
+  if (a->v_new && !aligned16(a->v_new)) return TOPT_EINVAL;
   return cuda_status(vmean_launch(*a, (cudaStream_t)stream));
 }
 

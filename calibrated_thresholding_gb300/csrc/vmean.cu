@@ -7,7 +7,9 @@
 // mu <- mu + (sum of the t new rows - t * mu) / (n_old + t), which equals
 // (n_old * mu + sum) / (n_old + t).  One CTA per (batch, KV head); 16-byte
 // loads, LPR lanes per row, rows strided over the CTA, then a shared-memory
-// reduction over the row lanes.
+// reduction over the row lanes.  Given the step's new rows, the same threads
+// first append them to the caches (rows n_old..) and average the values they
+// loaded.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,8 +30,19 @@ __device__ __forceinline__ void load8f(const float* src, float f[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// Eight consecutive elements, copied as raw bytes.
+__device__ __forceinline__ void copy8(__nv_bfloat16* dst, const __nv_bfloat16* src) {
+  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+}
+__device__ __forceinline__ void copy8(float* dst, const float* src) {
+  reinterpret_cast<float4*>(dst)[0] = reinterpret_cast<const float4*>(src)[0];
+  reinterpret_cast<float4*>(dst)[1] = reinterpret_cast<const float4*>(src)[1];
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int t, const T* __restrict__ v,
+__global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int t, T* __restrict__ v,
+                                                         const T* __restrict__ v_new, T* __restrict__ k,
+                                                         const T* __restrict__ k_new,
                                                          const int32_t* __restrict__ n_old,
                                                          float* __restrict__ mu, int32_t* status) {
   constexpr int LPR = D / 8;
@@ -49,13 +62,20 @@ __global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int 
   }
   const int dl = threadIdx.x % LPR;
   const int rl = threadIdx.x / LPR;
-  const T* base = v + ((size_t)pair * Nmax + n0) * D + dl * 8;
+  T* base = v + ((size_t)pair * Nmax + n0) * D + dl * 8;
+  const T* src = v_new ? v_new + (size_t)pair * t * D + dl * 8 : base;
   float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int i = rl; i < t; i += RL) {
     float f[8];
-    load8f(base + (size_t)i * D, f);
+    load8f(src + (size_t)i * D, f);
+    if (v_new) copy8(base + (size_t)i * D, src + (size_t)i * D);
 #pragma unroll
     for (int e = 0; e < 8; ++e) s[e] += f[e];
+  }
+  if (k_new) {
+    T* kb = k + ((size_t)pair * Nmax + n0) * D + dl * 8;
+    const T* ks = k_new + (size_t)pair * t * D + dl * 8;
+    for (int i = rl; i < t; i += RL) copy8(kb + (size_t)i * D, ks + (size_t)i * D);
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[rl][dl * 8 + e] = s[e];
@@ -71,7 +91,10 @@ __global__ void __launch_bounds__(kThreads) vmean_kernel(int Hkv, int Nmax, int 
 
 template <typename T>
 cudaError_t launch_t(const topt_vmean_args& a, cudaStream_t s) {
-  const T* v = static_cast<const T*>(a.v_cache);
+  T* v = static_cast<T*>(a.v_cache);
+  const T* v_new = static_cast<const T*>(a.v_new);
+  T* k = static_cast<T*>(a.k_cache);
+  const T* k_new = static_cast<const T*>(a.k_new);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.batch * a.n_kv_heads));
   cfg.blockDim = dim3(kThreads);
@@ -82,10 +105,10 @@ cudaError_t launch_t(const topt_vmean_args& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (a.head_dim == 128)
-    return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 128>, a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu,
-                              a.status);
-  return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 64>, a.n_kv_heads, a.cache_len, a.n_new, v, a.n_old, a.mu,
-                            a.status);
+    return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 128>, a.n_kv_heads, a.cache_len, a.n_new, v, v_new, k, k_new,
+                              a.n_old, a.mu, a.status);
+  return cudaLaunchKernelEx(&cfg, vmean_kernel<T, 64>, a.n_kv_heads, a.cache_len, a.n_new, v, v_new, k, k_new,
+                            a.n_old, a.mu, a.status);
 }
 
 }  // namespace

@@ -79,7 +79,7 @@ class MkcArgs(ctypes.Structure):
 class VmeanArgs(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_kv_heads", i32), ("head_dim", i32), ("cache_len", i32),
                 ("dtype", i32), ("n_new", i32), ("v_cache", vp), ("n_old", vp), ("mu", vp),
-                ("status", vp)]
+                ("status", vp), ("k_cache", vp), ("k_new", vp), ("v_new", vp)]
 
 
 _lib = None
@@ -459,9 +459,11 @@ def select_kth(x, row_len, k, out=None, status=None, stream=None):
     return out
 
 
-def vmean_args(v_cache, n_old, n_new, mu, status=None) -> VmeanArgs:
+def vmean_args(v_cache, n_old, n_new, mu, status=None, k_cache=None, k_new=None, v_new=None) -> VmeanArgs:
     """The topt_vmean_update arguments for these tensors (validated once; the
-    struct can be passed to ``lib().topt_vmean_update`` for every step)."""
+    struct can be passed to ``lib().topt_vmean_update`` for every step).
+    k_new / v_new [B][Hkv][n_new][d] (optional): the step's new rows, appended
+    to k_cache / v_cache at rows n_old.. by the same launch."""
     B, Hkv, Nmax, d = v_cache.shape
     a = VmeanArgs()
     a.batch, a.n_kv_heads, a.head_dim, a.cache_len = B, Hkv, d, Nmax
@@ -470,11 +472,22 @@ def vmean_args(v_cache, n_old, n_new, mu, status=None) -> VmeanArgs:
     a.n_old = _ptr(_dev(n_old, "n_old", torch.int32))
     a.mu = _ptr(_dev(mu, "mu", torch.float32))
     a.status = _ptr(_dev(status, "status", torch.int32))
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t is not None and (tuple(t.shape) != (B, Hkv, int(n_new), d) or t.dtype != v_cache.dtype
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name}: a contiguous [{B}][{Hkv}][{int(n_new)}][{d}] {v_cache.dtype} tensor")
+    if k_new is not None and (k_cache is None or tuple(k_cache.shape) != tuple(v_cache.shape)
+                              or k_cache.dtype != v_cache.dtype):
+        raise ValueError("k_new needs k_cache shaped and typed as v_cache")
+    a.k_cache = _ptr(_dev(k_cache, "k_cache"))
+    a.k_new = _ptr(_dev(k_new, "k_new"))
+    a.v_new = _ptr(_dev(v_new, "v_new"))
     return a
 
 
-def vmean_update(v_cache, n_old, n_new, mu, status=None, stream=None):
-    """mu <- running mean after appending rows n_old..n_old+n_new-1 (topt_vmean_update)."""
-    a = vmean_args(v_cache, n_old, n_new, mu, status)
+def vmean_update(v_cache, n_old, n_new, mu, status=None, stream=None, k_cache=None, k_new=None, v_new=None):
+    """mu <- running mean after appending rows n_old..n_old+n_new-1 (topt_vmean_update);
+    with k_new / v_new the rows are first written into k_cache / v_cache."""
+    a = vmean_args(v_cache, n_old, n_new, mu, status, k_cache, k_new, v_new)
     _check("topt_vmean_update", lib().topt_vmean_update(ctypes.byref(a), _stream(stream)))
     return mu

@@ -363,16 +363,25 @@ topt_status topt_select_kth(const float* x, int32_t rows, int32_t row_stride,
 /* ------------------------------------------------------------------------ */
 typedef struct {
   int32_t batch, n_kv_heads, head_dim, cache_len;
-  int32_t dtype;        /* topt_dtype of v_cache */
+  int32_t dtype;        /* topt_dtype of v_cache (and of k_cache, k_new, v_new) */
   int32_t n_new;        /* t >= 1 rows appended per sequence */
-  const void* v_cache;  /* [B][Hkv][Nmax][d] */
+  void* v_cache;        /* [B][Hkv][Nmax][d]; written only when v_new is given */
   const int32_t* n_old; /* [B] rows already in mu; new rows are n_old..n_old+t-1 */
   float* mu;            /* [B][Hkv][d] fp32, updated in place */
   int32_t* status;
+  /* Optional append of the step's new rows (NULL: the caches already hold
+   * them).  v_new [B][Hkv][t][d] is copied to v_cache rows n_old.. and its
+   * values are the ones averaged; k_new [B][Hkv][t][d] is copied to k_cache
+   * [B][Hkv][Nmax][d] rows n_old.. (k_cache required with k_new).  16-byte
+   * aligned, dtype as v_cache. */
+  void* k_cache;
+  const void* k_new;
+  const void* v_new;
 } topt_vmean_args;
 
 /* mu <- (n_old * mu + sum of the t new rows) / (n_old + t).  t = 1 is the
- * per-token decode update; n_old = 0, t = S initialises mu from a prefill. */
+ * per-token decode update; n_old = 0, t = S initialises mu from a prefill.
+ * With k_new / v_new the same launch first appends the new K and V rows. */
 topt_status topt_vmean_update(const topt_vmean_args* args, topt_stream stream);
 
 /* Library version (major*10000 + minor*100 + patch) and status names. */

@@ -230,6 +230,53 @@ def test_vmean_prepared_args_reused():
     np.testing.assert_allclose(mu.cpu().double().numpy(), np.mean(synth.as_f64(V), axis=2), rtol=0, atol=1e-5)
 
 
+@pytest.mark.parametrize("dtype,t", [(torch.bfloat16, 1), (torch.float32, 3), (torch.bfloat16, 70)])
+def test_vmean_appends_new_rows(dtype, t):
+    """With k_new / v_new the same launch writes the new rows into both caches
+    at rows n_old.. (bit for bit, nothing else touched) and averages them: mu
+    then equals the update of a cache that already held those rows."""
+    B, Hkv, d, Nmax = 2, 3, 128, 400
+    gen = synth.generator(63, "cuda")
+    K = synth.iid_normal(gen, (B, Hkv, Nmax, d), "cuda", dtype)
+    V = synth.values(gen, B, Hkv, Nmax, d, device="cuda", dtype=dtype)
+    k_new = synth.iid_normal(gen, (B, Hkv, t, d), "cuda", dtype)
+    v_new = synth.iid_normal(gen, (B, Hkv, t, d), "cuda", dtype)
+    n_old = torch.tensor([250, 399 - t], device="cuda", dtype=torch.int32)
+    mu0 = torch.zeros((B, Hkv, d), device="cuda")
+    for b in range(B):
+        topt.vmean_update(V[b:b + 1], n_old[b:b + 1].clone().zero_(), int(n_old[b]), mu0[b:b + 1])
+    K2, V2, mu = K.clone(), V.clone(), mu0.clone()
+    topt.vmean_update(V2, n_old, t, mu, k_cache=K2, k_new=k_new, v_new=v_new)
+    # reference: the rows written by hand, then the plain update
+    K3, V3, mu_ref = K.clone(), V.clone(), mu0.clone()
+    for b in range(B):
+        n0 = int(n_old[b])
+        K3[b, :, n0:n0 + t] = k_new[b]
+        V3[b, :, n0:n0 + t] = v_new[b]
+    topt.vmean_update(V3, n_old, t, mu_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(K2, K3) and torch.equal(V2, V3)
+    assert torch.equal(mu, mu_ref)
+    # and against the float64 mean of the prefix plus the new rows
+    want = np.stack([np.mean(synth.as_f64(V3)[b, :, :int(n_old[b]) + t], axis=1) for b in range(B)])
+    np.testing.assert_allclose(mu.cpu().double().numpy(), want, rtol=0, atol=1e-5)
+
+
+def test_vmean_append_rejects_missing_k_cache():
+    import ctypes
+    B, Hkv, d, Nmax = 1, 1, 64, 16
+    V = torch.zeros((B, Hkv, Nmax, d), device="cuda", dtype=torch.bfloat16)
+    mu = torch.zeros((B, Hkv, d), device="cuda")
+    n_old = torch.zeros(B, device="cuda", dtype=torch.int32)
+    k_new = torch.zeros((B, Hkv, 1, d), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        topt.vmean_args(V, n_old, 1, mu, k_new=k_new)
+    a = topt.vmean_args(V, n_old, 1, mu)
+    a.k_new = ctypes.c_void_p(k_new.data_ptr())          # k_cache left NULL
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert topt.lib().topt_vmean_update(ctypes.byref(a), stream) == 1   # TOPT_EINVAL, nothing launched
+
+
 # ---------------------------------------------------------------------------
 # prefill
 # ---------------------------------------------------------------------------
