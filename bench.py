@@ -64,10 +64,10 @@ DECODE_TRAFFIC = {"sources": ["decode.cu", "common.cuh"],
                   "source_sha256": "7b605ed92726ff074a8ac0386e4db346c6fe918ae09d8bb60643e8ea35294192",
                   "bytes_per_launch": 285353216 + 3473152}   # decode_kernel, one layer call (k = 128)
 PREFILL_TRAFFIC = {"sources": ["prefill_tc.cu", "prefill_tc_post.cu", "tc.cuh", "common.cuh"],
-                   "source_sha256": "df35f8e29aa5e1a35fa23f12ac181bcb9e0b27b53758051f7dccff2112c6baf7",
+                   "source_sha256": "79e668380b2a8edbdd1b903880127feb756a209f111fb2309664c0e76a3fbbbe",
                    # the attention kernel of each threshold mode (pre: prefill_tc_kernel,
                    # post: prefill_post_kernel)
-                   "bytes_per_launch": {0: 59916032 + 17154816, 1: 59517440 + 22559232}}
+                   "bytes_per_launch": {0: 59804416 + 16286464, 1: 59526912 + 22288384}}
 
 
 def parse():
