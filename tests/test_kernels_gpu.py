@@ -122,8 +122,10 @@ def mean_rows(V, seq_len):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (16, 2), (6, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (16, 2), (6, 2), (4, 2), (10, 2), (14, 2)])
 def test_decode_matches_oracle(d, Hq, Hkv):
+    """Group sizes 1, 4, 8, 3, 2, 5, 7: every score-column layout (G, G padded
+    to even) the kernel is built for, at both head sizes."""
     B, Nmax, k = 3, 1100, 16
     seq = [1100, 1, 601]
     q, K, V, ch = decode_case(21, B, Hq, Hkv, d, Nmax, seq)
